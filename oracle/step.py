@@ -1,0 +1,166 @@
+"""The whole MoE step: route, place, quantise x, expert SwiGLU MLPs, combine.
+
+Oracle module (test infrastructure only). See ``oracle/__init__.py``.
+
+Passages followed:
+
+* "FlyDSL Mono Kernels for High-Interactivity LLM Serving in ATOM", section
+  "MiniMax-M3: Connecting Attention and Experts". Each expert does an
+  up/gate projection and a down projection.
+* "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang":
+  - section 2.1: MXFP8 activation quantisation, and the weighted reduction of
+    expert outputs fused with the shared-expert addition;
+  - section 3.1: the SwiGLU keeps the original intermediate rounding.
+
+Readings where the pages are silent (each listed in the design doc):
+
+* Intermediate rounding. g and u are rounded to bf16, as an unfused GEMM
+  would store them. silu(g)*u is formed in fp64 and rounded to fp32, then to
+  bf16. That h is quantised to MXFP8 along I before the down projection.
+* No SwiGLU clip is applied; the pages do not give the limit.
+* GEMMs: every product of two MXFP8 values is exact in fp64. The sum over K
+  is an fp64 matrix product (a library primitive). The result is rounded to
+  fp32, the type the device accumulates in.
+* Combine: y[t] = bf16( ((w_1*o_1 + w_2*o_2) + ...) + o_shared ), in binary32,
+  in rank order. The shared expert takes every row with weight 1.0.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Callable, Mapping
+
+import numpy as np
+
+from .formats import (bf16_bits_to_f64, f32_to_bf16_bits, mxfp8_dequantize,
+                      mxfp8_quantize)
+from .routing import placement, softmax_topk_weights, topk_ids
+
+
+@dataclass
+class ExpertWeights:
+    """One expert's MXFP8 weights in the canonical K-contiguous layout.
+
+    w_gate, w_up: uint8 E4M3 [I][H]; s_gate, s_up: uint8 UE8M0 [I][H/32]
+    w_down:       uint8 E4M3 [H][I]; s_down:       uint8 UE8M0 [H][I/32]
+    """
+    w_gate: np.ndarray
+    s_gate: np.ndarray
+    w_up: np.ndarray
+    s_up: np.ndarray
+    w_down: np.ndarray
+    s_down: np.ndarray
+
+
+def expert_weights_from_synth(seed: int, e, H: int, I: int) -> ExpertWeights:
+    """Draw expert e's bf16 weights from the seeded generator, then quantise
+    them with the oracle's own MXFP8 rule. e == "shared" selects the shared expert."""
+    import synth
+    if e == "shared":
+        sg, su, sd = synth.STREAM_SH_GATE, synth.STREAM_SH_UP, synth.STREAM_SH_DOWN
+    else:
+        sg, su, sd = synth.stream_gate(e), synth.stream_up(e), synth.stream_down(e)
+    g = bf16_bits_to_f64(synth.expert_weight_bf16(seed, sg, I, H))
+    u = bf16_bits_to_f64(synth.expert_weight_bf16(seed, su, I, H))
+    d = bf16_bits_to_f64(synth.expert_weight_bf16(seed, sd, H, I))
+    wg, sgc = mxfp8_quantize(g)
+    wu, suc = mxfp8_quantize(u)
+    wd, sdc = mxfp8_quantize(d)
+    return ExpertWeights(wg, sgc, wu, suc, wd, sdc)
+
+
+def _round_f32(v) -> np.ndarray:
+    return np.asarray(v, dtype=np.float64).astype(np.float32)
+
+
+def expert_mlp(xq, xs, w: ExpertWeights):
+    """SwiGLU expert MLP on MXFP8 token rows xq/xs [n][H].
+
+    Returns g_bf16, u_bf16, h_bf16 ([n][I] bf16 bits), the MXFP8 quantised h
+    (hq [n][I], hs [n][I/32]) and o (fp32 [n][H]).
+    """
+    x = mxfp8_dequantize(xq, xs)                              # exact, fp64 [n][H]
+    wg = mxfp8_dequantize(w.w_gate, w.s_gate)                 # [I][H]
+    wu = mxfp8_dequantize(w.w_up, w.s_up)
+    g = f32_to_bf16_bits(_round_f32(x @ wg.T))                # gate projection
+    u = f32_to_bf16_bits(_round_f32(x @ wu.T))                # up projection
+    gf = bf16_bits_to_f64(g)
+    uf = bf16_bits_to_f64(u)
+    silu = gf / (1.0 + np.exp(-gf))                           # SiLU(g) = g * sigmoid(g)
+    h = f32_to_bf16_bits(_round_f32(silu * uf))               # SwiGLU: SiLU(gate) * up
+    hq, hs = mxfp8_quantize(bf16_bits_to_f64(h))
+    wd = mxfp8_dequantize(w.w_down, w.s_down)                 # [H][I]
+    o = _round_f32(mxfp8_dequantize(hq, hs) @ wd.T)           # down projection
+    return g, u, h, hq, hs, o
+
+
+def moe_step(x_bits, logits, k: int,
+             experts: Mapping[int, ExpertWeights] | Callable[[int], ExpertWeights],
+             shared: ExpertWeights | None = None,
+             rows=None):
+    """One MoE step over T token rows.
+
+    x_bits: bf16 bit patterns uint16 [T][H]; logits: fp32 [T][E].
+    experts: a mapping or callable giving ExpertWeights for an expert id.
+    shared: the always-active shared expert, or None.
+    rows: optional subset of token rows. The expert MLPs and the combine run
+      only for these rows. Routing, placement and x quantisation still cover
+      all T rows, and the rows left out of y are 0.
+
+    Returns a dict with every intermediate:
+      ids, w, bitmap, counts, tiles, slot_e/slot_tile/slot_row, rows_of,
+      xq, xs, and, indexed by pair id p = t*k + j (shared pairs: T*k + t),
+      g, u, h (bf16 bits), hq, hs, o (fp32), plus y (bf16 bits [T][H]).
+    """
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    logits = np.asarray(logits, dtype=np.float32)
+    T, H = x_bits.shape
+    E = logits.shape[1]
+    get = experts if callable(experts) else experts.__getitem__
+    ids = topk_ids(logits, k)
+    w = softmax_topk_weights(logits, ids)
+    plc = placement(ids, E)
+    xq, xs = mxfp8_quantize(bf16_bits_to_f64(x_bits))
+
+    row_set = set(range(T)) if rows is None else set(int(r) for r in rows)
+    n_pairs = T * k + (T if shared is not None else 0)
+    out = {"ids": ids, "w": w, "xq": xq, "xs": xs, **plc}
+    I = None
+    pair_res = {}
+
+    def run(pair_ids, weights):
+        nonlocal I
+        toks = np.array([p // k if p < T * k else p - T * k for p in pair_ids])
+        g, u, h, hq, hs, o = expert_mlp(xq[toks], xs[toks], weights)
+        I = g.shape[1]
+        for n, p in enumerate(pair_ids):
+            pair_res[int(p)] = (g[n], u[n], h[n], hq[n], hs[n], o[n])
+
+    for e in range(E):
+        pairs = [int(p) for p in plc["rows_of"][e] if (int(p) // k) in row_set]
+        if pairs:
+            run(pairs, get(e))
+    if shared is not None:
+        pairs = [T * k + t for t in range(T) if t in row_set]
+        if pairs:
+            run(pairs, shared)
+
+    y = np.zeros((T, H), dtype=np.uint16)
+    if I is not None:
+        g_all = np.zeros((n_pairs, I), dtype=np.uint16)
+        u_all = np.zeros((n_pairs, I), dtype=np.uint16)
+        h_all = np.zeros((n_pairs, I), dtype=np.uint16)
+        hq_all = np.zeros((n_pairs, I), dtype=np.uint8)
+        hs_all = np.zeros((n_pairs, I // 32), dtype=np.uint8)
+        o_all = np.zeros((n_pairs, H), dtype=np.float32)
+        for p, (g, u, h, hq, hs, o) in pair_res.items():
+            g_all[p], u_all[p], h_all[p], hq_all[p], hs_all[p], o_all[p] = g, u, h, hq, hs, o
+        out.update(g=g_all, u=u_all, h=h_all, hq=hq_all, hs=hs_all, o=o_all)
+        for t in sorted(row_set):
+            acc = w[t, 0] * o_all[t * k + 0]                      # binary32 products and sums
+            for j in range(1, k):
+                acc = acc + w[t, j] * o_all[t * k + j]
+            if shared is not None:
+                acc = acc + o_all[T * k + t]
+            y[t] = f32_to_bf16_bits(acc.astype(np.float32))
+    out["y"] = y
+    return out
