@@ -1,0 +1,439 @@
+"""Benchmark of the small-batch MXFP8 MoE step on GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+route + place + quantise x, expert SwiGLU MLPs (gate/up, then down), combine.
+
+Default workload: the bs1 speculative-verify shape. That is T=6 token rows,
+H=4096, E=256 routed experts, top-8, I=2048, MXFP8 weights (group-32 UE8M0
+along K), uniform routing, seed 42.
+
+The JSON line reports:
+* value: microseconds per step, with inputs resident in HBM and L2 flushed
+  before every step.
+* roofline: the expert kernel's achieved HBM GB/s on the active experts'
+  weight bytes, against the measured copy bandwidth.
+* e2e: the same metric through the C ABI with host buffers (moe_forward_host).
+* cpu_baseline: the oracle timed on the host cores on a bounded sample.
+* also: the other row counts (24/96/384) as context.
+
+--impl reference times the oracle instead (the CPU restatement).
+Under torchrun each rank runs an independent replica. There is no collective
+in the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "bs1"
+SAMPLE_ROWS = 2        # oracle sample: this many token rows of the step, with every expert they touch
+ORACLE_WORKERS = 8     # spawn workers that prepare the oracle's weights (not timed)
+
+
+# ----------------------------------------------------------------------------- oracle side (CPU)
+
+def _oracle_expert(args):
+    seed, e, H, I = args
+    import oracle
+    w = oracle.expert_weights_from_synth(seed, e, H, I)
+    return e, w
+
+
+def _oracle_prepare(seed, wl_name, rows, pool):
+    import numpy as np  # noqa: F401
+    import oracle
+    import synth
+    wl = synth.WORKLOADS[wl_name]
+    x_bits = synth.x_bf16(seed, wl.T, wl.H)
+    lg = synth.router_logits(seed, wl.T, wl.E, wl.k, wl.routing)
+    ids = oracle.topk_ids(lg, wl.k)
+    experts = sorted(set(int(e) for t in rows for e in ids[t]))
+    jobs = [(seed, e, wl.H, wl.I) for e in experts]
+    if wl.shared:
+        jobs.append((seed, "shared", wl.H, wl.I))
+    return x_bits, lg, experts, jobs
+
+
+def oracle_baseline(seed: int, wl_name: str, steps: int, warmup: int, result_q):
+    """Runs in a spawned process: times the oracle on a bounded sample of the workload."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import oracle
+    import synth
+    wl = synth.WORKLOADS[wl_name]
+    rows = list(range(min(SAMPLE_ROWS, wl.T)))
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(ORACLE_WORKERS) as pool:
+        x_bits, lg, experts, jobs = _oracle_prepare(seed, wl_name, rows, pool)
+        got = dict(pool.map(_oracle_expert, jobs))
+    shared = got.pop("shared", None)
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        oracle.moe_step(x_bits, lg, wl.k, got, shared=shared, rows=rows)
+        dt = time.perf_counter() - t0
+        if i >= warmup:
+            times.append(dt)
+    per_sample = statistics.median(times)
+    scale = wl.T / len(rows)
+    result_q.put({
+        "us_per_step": per_sample * scale * 1e6,
+        "sample_s": per_sample,
+        "rows": len(rows),
+        "experts": len(experts) + (1 if shared is not None else 0),
+        "scale": scale,
+        "steps": steps,
+        "cores": 1,
+    })
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, out_path: str | None):
+        self.proc = None
+        self.out_path = out_path
+        self.gpu_index = gpu_index
+        try:
+            self.f = open(out_path, "w") if out_path else subprocess.DEVNULL
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw_slowdown": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power_cap": parts[8]})
+            except ValueError:
+                continue
+        if self.out_path:
+            with open(self.out_path, "w") as f:
+                f.write(out)
+        return rows
+
+
+def summarise_clocks(rows):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    loaded = [r for r in rows if r["power"] > 200] or rows
+    reasons = set()
+    for r in loaded:
+        for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+            if r[key].lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
+            "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+# ----------------------------------------------------------------------------- GPU side
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def active_experts(lg, k, shared):
+    import numpy as np
+    ids = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+    return len(set(ids.ravel().tolist())) + (1 if shared else 0)
+
+
+def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
+    """Times `steps` steps (L2 flushed before each, outside the events). Returns a dict."""
+    import torch
+    from moe_expert_layer_top_gb300 import abi, synthetic
+    from moe_expert_layer_top_gb300.layer import MoEStep, MoEWeightsMXFP8
+    w = weights if wl.shared else MoEWeightsMXFP8(weights.w_gate, weights.s_gate, weights.w_up, weights.s_up,
+                                                  weights.w_down, weights.s_down)
+    x, lg, _, lg_np = synthetic.make_inputs(seed, wl.T, wl.H, wl.E, wl.k, wl.routing)
+    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING)
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush_buf.zero_()
+        step.forward(x, lg, y=y)
+    torch.cuda.synchronize()
+    step.kernel_times()  # reset the expert-kernel event log
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush_buf.zero_()
+        starts[i].record(stream)
+        step.forward(x, lg, y=y)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    expert_ms, launches = step.kernel_times()
+    status = step.status()
+    A = active_experts(lg_np, wl.k, wl.shared)
+    weight_bytes = A * wl.expert_bytes
+    step_bytes = weight_bytes + wl.T * wl.H * 2 + wl.T * wl.E * 4 + wl.T * wl.H * 2
+    res = {
+        "ms_steps": per_step,
+        "ms_mean": sum(per_step) / len(per_step),
+        "ms_median": statistics.median(per_step),
+        "ms_min": min(per_step),
+        "ms_max": max(per_step),
+        "expert_ms_mean": expert_ms / max(launches, 1),
+        "expert_launches": launches,
+        "active_experts": A,
+        "weight_bytes": weight_bytes,
+        "step_bytes": step_bytes,
+        "status": status,
+        "step": step,
+        "x": x,
+        "lg": lg,
+    }
+    return res
+
+
+def time_e2e(step, wl, seed, steps, warmup):
+    """moe_forward_host: pinned host x/logits in, host y out, copies inside the timed region."""
+    import numpy as np
+    import torch
+    import synth
+    from moe_expert_layer_top_gb300 import abi
+    xh = torch.from_numpy(synth.x_bf16(seed, wl.T, wl.H).view(np.int16).copy()).pin_memory()
+    lh = torch.from_numpy(synth.router_logits(seed, wl.T, wl.E, wl.k, wl.routing)).pin_memory()
+    yh = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+    for _ in range(warmup):
+        assert step.forward_host(xh, lh, yh) == abi.MOE_OK
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        st = step.forward_host(xh, lh, yh)
+        times.append(time.perf_counter() - t0)
+        assert st == abi.MOE_OK
+    h2d = wl.T * wl.H * 2 + wl.T * wl.E * 4
+    d2h = wl.T * wl.H * 2 + 4
+    return {"value": statistics.mean(times) * 1e6, "unit": "us/step", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "median_us": statistics.median(times) * 1e6}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    import synth
+    from moe_expert_layer_top_gb300 import build as _build
+    from moe_expert_layer_top_gb300 import synthetic
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    seed = synth.BASE_SEED
+    wl = synth.WORKLOADS[args.workload]
+
+    # The oracle's worker pool is spawned before the first GPU call.
+    cpu_q = None
+    cpu_proc = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ctx = mp.get_context("spawn")
+        cpu_q = ctx.Queue()
+        cpu_proc = ctx.Process(target=oracle_baseline, args=(seed, wl.name, 3, 1, cpu_q))
+        cpu_proc.start()
+
+    _build.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev_props = torch.cuda.get_device_properties(local)
+    l2 = getattr(dev_props, "L2_cache_size", 128 << 20)
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+
+    weights = synthetic.make_weights(seed, wl.E, wl.H, wl.I, shared=1)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else None)
+    time.sleep(0.05)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    main = time_gpu_workload(wl, weights, args.steps, args.warmup, flush_buf, seed)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clock_rows = clocks.stop()
+
+    ms = main["ms_mean"]
+    exp_ms = main["expert_ms_mean"]
+    if world > 1:
+        t = torch.tensor([ms, exp_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, exp_ms = float(t[0]), float(t[1])
+
+    e2e = time_e2e(main["step"], wl, seed, max(args.steps, 10), 3)
+
+    also = {}
+    if not args.no_others and world == 1:
+        for name in ("bs4", "bs16", "bs64"):
+            if name == wl.name:
+                continue
+            o = synth.WORKLOADS[name]
+            r = time_gpu_workload(o, weights, max(args.steps // 2, 5), max(args.warmup, 3), flush_buf, seed)
+            peak, _ = measured_peaks()
+            also[name] = {"T": o.T, "us_per_step": round(r["ms_mean"] * 1e3, 2),
+                          "us_median": round(r["ms_median"] * 1e3, 2),
+                          "expert_kernel_us": round(r["expert_ms_mean"] * 1e3, 2),
+                          "active_experts": r["active_experts"],
+                          "expert_gbs": round(r["weight_bytes"] / (r["expert_ms_mean"] * 1e-3) / 1e9, 1),
+                          "expert_frac": round(r["weight_bytes"] / (r["expert_ms_mean"] * 1e-3) / 1e9 / peak, 3),
+                          "status": r["status"]}
+            r["step"].close()
+
+    if rank != 0:
+        main["step"].close()
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if cpu_q is not None:
+        cpu = cpu_q.get(timeout=900)
+        cpu_proc.join(timeout=60)
+
+    peak, peak_kind = measured_peaks()
+    achieved = main["weight_bytes"] / (exp_ms * 1e-3) / 1e9
+    line = {
+        "metric": "MoE step us & achieved HBM GB/s (% of roofline) at 6/24/96/384 token rows",
+        "value": round(ms * 1e3, 3),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3xe4m3->f32 (MXFP8 weights and activations, bf16 in/out)",
+        "data": "synthetic (seeded counter-based generator; random-init weights, MXFP8-quantised on device)",
+        "config": {
+            "workload": f"{wl.name}: T={wl.T} token rows, H={wl.H}, E={wl.E}, top-{wl.k}, I={wl.I}, "
+                        f"shared={wl.shared}, routing={wl.routing}",
+            "T": wl.T, "H": wl.H, "E": wl.E, "top_k": wl.k, "I": wl.I, "shared": wl.shared,
+            "active_experts": main["active_experts"],
+            "step_bytes": main["step_bytes"],
+            "step_gbs": round(main["step_bytes"] / (ms * 1e-3) / 1e9, 1),
+            "us_median": round(main["ms_median"] * 1e3, 3),
+            "us_min": round(main["ms_min"] * 1e3, 3),
+            "us_max": round(main["ms_max"] * 1e3, 3),
+            "l2": "flushed before every step (memset of a buffer >= 2x L2, outside the timed events)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "status": main["status"],
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "experts_kernel (persistent gate/up + down)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": main["weight_bytes"],
+            "kernel_us": round(exp_ms * 1e3, 3),
+        },
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": summarise_clocks(clock_rows),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = {
+            "value": round(cpu["us_per_step"], 1), "unit": "us/step", "cores": cpu["cores"], "kind": "oracle",
+            "sample": f"{cpu['rows']} of {wl.T} token rows ({cpu['experts']} expert MLPs), median of "
+                      f"{cpu['steps']} runs of {cpu['sample_s']:.2f} s, scaled x{cpu['scale']:.0f} to a step",
+        }
+    if also:
+        line["also"] = also
+    main["step"].close()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=oracle_baseline, args=(synth.BASE_SEED, wl.name, args.steps, args.warmup, q))
+    p.start()
+    r = q.get(timeout=3600)
+    p.join(timeout=60)
+    v = round(r["us_per_step"], 1)
+    line = {
+        "impl": "reference",
+        "metric": "MoE step us & achieved HBM GB/s (% of roofline) at 6/24/96/384 token rows",
+        "value": v, "unit": "us/step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle)", "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E}, top-{wl.k}, I={wl.I}, shared={wl.shared}",
+                   "T": wl.T, "H": wl.H, "E": wl.E, "top_k": wl.k, "I": wl.I},
+        "cpu_baseline": {"value": v, "unit": "us/step", "cores": r["cores"], "kind": "oracle",
+                         "sample": f"{r['rows']} of {wl.T} token rows ({r['experts']} expert MLPs) per step, "
+                                   f"scaled x{r['scale']:.0f}"},
+        "e2e": {"value": v, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=["tiny", "bs1", "bs4", "bs16", "bs64"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * moe.h — C ABI of the GB300 small-batch MXFP8 MoE step.
+ *
+ * One decode MoE step of a DeepSeek-V4.1-Flash-style layer, on one GPU:
+ *   router top-k + softmax weights
+ *   -> sort-free placement of (token, expert) pairs into 8-row tiles
+ *   -> MXFP8 quantisation of the token rows
+ *   -> SwiGLU gate/up projection, bf16 intermediate, MXFP8 quantisation of h
+ *   -> down projection
+ *   -> weighted combine (+ an optional always-active shared expert).
+ *
+ * Passages that define the operation (page title, section):
+ *  - "SGLang's Low-Latency Mode Boosts DeepSeek-V4.1-Flash Speed by 1.56x on
+ *    AMD", "NVIDIA overlaps the dependency chain", bullet "Routing without
+ *    sorting". Each expert's rows fit 8-row tiles, and a bitmap plus population
+ *    counts place them with no scan or sort, keeping the top-k choices.
+ *  - Same page, "Four stages keep megakernels outside core". The plugin
+ *    contract is Register / Guard / Build / Runtime, and unsupported shapes
+ *    fall back. Here:
+ *      Register = loading this library and checking moe_abi_version();
+ *      Guard + Build = moe_plan();
+ *      Runtime = moe_forward();
+ *      teardown = moe_destroy().
+ *    The fallback is the caller's business: moe_plan and moe_forward return
+ *    MOE_ERR_UNSUPPORTED, and this library has no CPU fallback.
+ *  - "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", section 2.1:
+ *      - group-32 FP8 weights and scales reorganised for Blackwell MXFP8;
+ *      - MXFP8 activation quantisation fused into the producer;
+ *      - the router emits the downstream layout;
+ *      - the weighted reduction of expert outputs is fused with the
+ *        shared-expert addition;
+ *      - scratch buffers are reused across calls.
+ *  - Same page, section 3.1. The MoE kernels fuse the clipped SwiGLU and keep
+ *    the original intermediate rounding. Here g and u are rounded to bf16,
+ *    and h = bf16(silu(g) * u) is then quantised to MXFP8. No clip is applied.
+ *  - "FlyDSL Mono Kernels for High-Interactivity LLM Serving in ATOM",
+ *    "MiniMax-M3: Connecting Attention and Experts". Each expert does an
+ *    up/gate and a down projection, for the shared and the routed experts.
+ *
+ * Formats (OCP Microscaling Formats v1.0):
+ *   E4M3 has bias 7, a largest finite value of 448 and NaN codes 0x7F/0xFF.
+ *   A UE8M0 scale code c has value 2^(c - 127).
+ *   The shared scale of a 32-group is 2^(floor(log2 amax) - 8), with the code
+ *   clamped to [0, 254]; amax = 0 gives code 0. Elements are rounded to
+ *   nearest-even and saturate at +-448.
+ *
+ * Conventions shared by every entry point:
+ *  - Every call returns a moe_status_t. None aborts, exits or traps. An
+ *    out-parameter is written only on MOE_OK.
+ *  - Device pointers are CUDA device memory on the plan's device, owned by the
+ *    caller, 16-byte aligned unless stated otherwise. Rows are contiguous
+ *    (row stride = row length).
+ *  - `cuda_stream` is a cudaStream_t (NULL = the legacy default stream).
+ *    Work is enqueued on it. Only moe_plan, moe_destroy, moe_forward_host and
+ *    moe_kernel_times synchronise.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* NULL or misaligned pointer, a size out of range, T > max_rows */
+  MOE_ERR_UNSUPPORTED = 2,   /* Guard: shape or device this library does not handle */
+  MOE_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+  MOE_ERR_OOM = 4,           /* device memory for the plan could not be allocated */
+  MOE_ERR_TIMEOUT = 5,       /* device side: a bounded wait gave up (reported through d_status) */
+  MOE_ERR_DEVICE_BOUNDS = 6  /* device side: an index check failed; the access was skipped */
+} moe_status_t;
+
+/* moe_config_t.flags */
+#define MOE_FLAG_TIMING (1u << 0)
+/* Record CUDA events around the expert kernel of every moe_forward. Read the
+ * times back with moe_kernel_times. Events are recorded on the launch stream. */
+
+#define MOE_FLAG_TEST_SKIP_READY (1u << 8)
+/* Host-side fault injection for tests. The gate/up units of the first placed
+ * tile never publish their ready count. The down units of that tile then give
+ * up after wait_timeout_ns, and MOE_ERR_TIMEOUT appears in *d_status; y is
+ * undefined for that step. The GPU does not fault or hang, and the next
+ * moe_forward on a plan without this flag is unaffected. */
+
+typedef struct moe_config {
+  int32_t hidden;        /* H: token width, the K of gate/up. Power of two, 512..4096. */
+  int32_t intermediate;  /* I: expert width, the K of down. Power of two, 256..4096. */
+  int32_t num_experts;   /* E: routed experts, 1..1024 */
+  int32_t top_k;         /* k: experts per token, 1..min(E, 32) */
+  int32_t num_shared;    /* 0 or 1 always-active shared expert (weight 1.0 in the combine) */
+  int32_t max_rows;      /* largest T a moe_forward on this plan may pass, 1..4096 */
+  uint32_t flags;        /* MOE_FLAG_* */
+  int64_t wait_timeout_ns; /* bound on every device-side wait; <= 0 selects 200 ms */
+} moe_config_t;
+
+/* Expert weights in the canonical MXFP8 layout: group-32 scales along K, K contiguous.
+ *   w_gate, w_up: E4M3 [E][I][H]     s_gate, s_up: UE8M0 [E][I][H/32]
+ *   w_down:       E4M3 [E][H][I]     s_down:       UE8M0 [E][H][I/32]
+ * The sh_* pointers are the same for one shared expert, without the E axis. They
+ * must be NULL when num_shared == 0.
+ * Ownership: the plan keeps these pointers. It does not copy the weights. They
+ * must stay valid and unchanged until moe_destroy. */
+typedef struct moe_weights {
+  const uint8_t *w_gate, *s_gate, *w_up, *s_up, *w_down, *s_down;
+  const uint8_t *sh_w_gate, *sh_s_gate, *sh_w_up, *sh_s_up, *sh_w_down, *sh_s_down;
+} moe_weights_t;
+
+/* Optional debug taps: device buffers that moe_forward fills with intermediate
+ * results after the step (device-to-device copies on the same stream). Any
+ * member may be NULL. A "pair" p is a (token t, slot j) choice, p = t*k + j;
+ * the shared expert's pairs are p = T*k + t. P = T*k + T*num_shared.
+ *   topk_ids int32 [T][k]  expert ids in rank order (descending logit, ties -> lower id)
+ *   topk_w   fp32  [T][k]  softmax over the selected logits
+ *   bitmap   uint32 [E][ceil(T/32)]  bit t of row e set iff token t chose expert e
+ *   counts   int32 [E]     rows placed on each expert
+ *   slot     int32 [T][k]  (e << 16) | rank, rank = tile*8 + row
+ *   xq, xs   uint8 [T][H], [T][H/32]  MXFP8 token rows
+ *   h_bf16   uint16 [P][I] SwiGLU output before quantisation (bf16 bits)
+ *   hq, hs   uint8 [P][I], [P][I/32]  MXFP8 h
+ *   o        fp32  [P][H]  expert outputs before the combine */
+typedef struct moe_taps {
+  int32_t *topk_ids;
+  float *topk_w;
+  uint32_t *bitmap;
+  int32_t *counts;
+  int32_t *slot;
+  uint8_t *xq, *xs;
+  uint16_t *h_bf16;
+  uint8_t *hq, *hs;
+  float *o;
+} moe_taps_t;
+
+/* Register: the ABI version this library implements (MOE_ABI_VERSION). */
+int32_t moe_abi_version(void);
+
+/* Human-readable name of a status code (a static string). */
+const char *moe_status_string(moe_status_t status);
+
+/* Guard + Build.
+ * The Guard checks the config and the device and returns MOE_ERR_UNSUPPORTED
+ * or MOE_ERR_INVALID_ARG before touching the device when a check fails. The
+ * device must be compute capability 10.3 (sm_103).
+ * The Build step allocates every scratch buffer for max_rows. moe_forward
+ * allocates nothing. It also records the weight pointers.
+ * On success *plan_out receives an opaque handle; on failure it is set to NULL.
+ * The plan belongs to the device that is current at this call. */
+moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights,
+                      void *cuda_stream, void **plan_out);
+
+/* Runtime: one MoE step over T token rows, enqueued on cuda_stream.
+ *   x      device bf16 [T][H]   token rows (not aliased with y)
+ *   logits device fp32 [T][E]   router logits (finite)
+ *   y      device bf16 [T][H]   output: sum_j w[t][j] * expert_{ids[t][j]}(x[t]) (+ shared(x[t]))
+ *   taps   optional debug outputs (NULL for none)
+ *   d_status optional device int32. It is set to MOE_OK at the start of the
+ *            step and to the first device-side error (MOE_ERR_TIMEOUT,
+ *            MOE_ERR_DEVICE_BOUNDS) if one occurs. Read it after the stream
+ *            has synchronised. NULL: errors go to a plan-owned word instead.
+ * T = 0 is valid and enqueues nothing. T > max_rows returns MOE_ERR_INVALID_ARG.
+ * The call allocates nothing and never synchronises. A plan serves one stream
+ * at a time: calls on one plan must not overlap on the GPU. */
+moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t T,
+                         void *y, const moe_taps_t *taps, int32_t *d_status,
+                         void *cuda_stream);
+
+/* Runtime with host buffers: copies x and logits from host memory into
+ * plan-owned device buffers, runs moe_forward and copies y back to y_host. It
+ * then synchronises cuda_stream and returns the device-side status of the
+ * step. Pinned host memory gives asynchronous copies; pageable memory works
+ * too. x_host: bf16 [T][H]; logits_host: fp32 [T][E]; y_host: bf16 [T][H]. */
+moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logits_host,
+                              int32_t T, void *y_host, void *cuda_stream);
+
+/* MXFP8 quantisation of bf16 rows along their last axis, groups of 32. This is
+ * the same device routine moe_forward applies to x.
+ *   x bf16 [rows][cols] (device), cols a multiple of 32
+ *   q E4M3 [rows][cols] (device), s UE8M0 [rows][cols/32] (device)
+ * This also prepares canonical MXFP8 weights from bf16 checkpoints: W_gate[e]
+ * is [I][H], quantised along H. The pages' checkpoints are already group-32 FP8. */
+moe_status_t moe_quantize_mxfp8(const void *x, int64_t rows, int32_t cols,
+                                uint8_t *q, uint8_t *s, void *cuda_stream);
+
+/* Timing read-back for plans built with MOE_FLAG_TIMING. Synchronises with
+ * the recorded events. Returns the summed expert-kernel time in ms over the
+ * moe_forward calls since the last reset, and the number of such calls; then
+ * resets both. At most 4096 calls are recorded between two reads; later ones
+ * are not timed. */
+moe_status_t moe_kernel_times(void *plan, double *expert_ms_out, int32_t *launches_out);
+
+/* Device-side status word of a plan (used when moe_forward got d_status ==
+ * NULL). Synchronises the plan's device and then reads it. */
+moe_status_t moe_plan_status(void *plan, int32_t *status_out);
+
+/* Teardown: frees the plan's device memory and events, after a device-wide
+ * synchronise. NULL is a no-op. */
+moe_status_t moe_destroy(void *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,558 @@
+// experts.cu — persistent expert kernel: gate/up GEMV + SwiGLU + MXFP8(h), then down GEMV.
+//
+// Work units, claimed in order from one global counter:
+//   gate/up unit (tile g, block b): 32 gate rows + 32 up rows, i in [32b, 32b+32),
+//       for the <= 8 token rows of tile g. Output: h for those rows, quantised
+//       to MXFP8 along I (one 32-group per unit). Then ready[g] is bumped.
+//   down unit (tile g, block b): DB rows of W_down, h in [b*DB, (b+1)*DB), for the
+//       rows of tile g. It waits (bounded) until ready[g] counts every gate/up
+//       unit of g, then writes o[pair][h] in fp32.
+// All gate/up units come before all down units in the claim order. So a down
+// unit waits only on units that running blocks have already claimed, and those
+// never wait. The schedule cannot deadlock, and every wait is bounded anyway.
+//
+// Pages followed:
+// - "FlyDSL Mono Kernels for High-Interactivity LLM Serving in ATOM",
+//   "MiniMax-M3: Connecting Attention and Experts":
+//     - blocks take on the next task (persistent blocks);
+//     - a later stage's weight loads start before its input is ready (the
+//       down-projection weights are fetched before the wait on h);
+//     - tagged buffers signal ready data (the per-tile ready counters).
+// - "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", 2.1: GEMV at
+//   small batch, with the reduction fused with MXFP8 quantisation of its
+//   output (h is quantised in the epilogue of the gate/up unit).
+// - Same page, 3.1: SwiGLU with the original intermediate rounding. g and u are
+//   rounded to bf16, and h = bf16(silu(g) * u) is then quantised.
+//
+// Block layout: 8 compute warps + 1 producer warp. The producer's elected lane
+// streams the unit's weight rows with bulk copies (TMA, no tensor map, no
+// multicast) into a 5-stage ring of 32 KB + scales.
+//
+// Each compute thread owns 16 consecutive K columns of every row in a stage:
+//  - K/16 threads cover a row, and 256/(K/16) row groups split the stage's rows;
+//  - it keeps its 16 columns of the tile's token rows in registers as fp32
+//    (dequantised once per unit);
+//  - per row it reads 16 weight bytes (one 16-byte shared load) and its
+//    group's scale, decodes E4M3 to fp32, and accumulates with packed FFMA2.
+// A transposing butterfly reduces 8 rows x NP tokens across the lanes, and a
+// fixed-order sum reduces across warps. Every output goes through the same
+// addition tree whatever the tile's row count, so results do not depend on
+// tile-mates.
+#include <stdint.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr uint32_t kDone = 0xFFFFFFFFu;
+constexpr int kConsumers = kConsumerWarps * 32;  // 256
+constexpr int kStageScaleBytes = kStageBytes / kGroup;
+constexpr int kStageStride = kStageBytes + kStageScaleBytes;
+constexpr int kMaxSlots = 16;  // reduction slots (K = 256 uses half-warps)
+
+struct __align__(16) ExpertSmem {
+  unsigned char stage[kStages][kStageStride];
+  float red[2][2][kMaxSlots][32];       // [stage parity][pass][slot][value]
+  float gu[kTileRows][2][32];           // gate/up results of the unit, [token][gate|up][i]
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint32_t meta_unit[kStages];
+  uint32_t meta_step[kStages];
+  int32_t abort_unit;
+};
+
+template <int KG, int KD>
+struct Shape {
+  static constexpr int H = KG, I = KD;
+  static constexpr int RS_G = kStageBytes / KG;    // rows per stage (gate/up)
+  static constexpr int RS_D = kStageBytes / KD;    // rows per stage (down)
+  static constexpr int SPU_G = 64 / RS_G;          // stages per gate/up unit (64 rows)
+  static constexpr int SPU_D = (H / RS_D) < 8 ? (H / RS_D) : 8;
+  static constexpr int DB = SPU_D * RS_D;          // rows of W_down per down unit
+  static constexpr int NBG = I / 32;               // gate/up units per tile
+  static constexpr int NBD = H / DB;               // down units per tile
+  static_assert(KG >= 512 && KG <= 4096 && (KG & (KG - 1)) == 0, "H: power of two in [512, 4096]");
+  static_assert(KD >= 256 && KD <= 4096 && (KD & (KD - 1)) == 0, "I: power of two in [256, 4096]");
+  static_assert(SPU_G >= 1 && 64 % RS_G == 0, "gate/up unit spans whole stages");
+  static_assert(H % DB == 0, "down units tile H");
+};
+
+// ------------------------------------------------------------------ per-thread math
+
+struct XRegs {
+  uint4 raw[kTileRows];     // 16 E4M3 codes per token row (this thread's columns)
+  uint32_t sc[kTileRows];   // UE8M0 code of the group holding these columns
+  float2 f[4][8];           // dequantised pass tokens, 16 values as 8 pairs
+};
+
+__device__ __forceinline__ void decode16(const uint4 v, float2 (&o)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = e4m3x2_to_float2(uint16_t(w[i] & 0xFFFFu));
+    o[2 * i + 1] = e4m3x2_to_float2(uint16_t(w[i] >> 16));
+  }
+}
+
+// x (or h) for tokens [4*pass, 4*pass + 4) into fp32 registers, with their scales applied.
+template <int NP>
+__device__ __forceinline__ void load_pass(XRegs &x, int pass, int n) {
+#pragma unroll
+  for (int t = 0; t < NP; ++t) {
+    const int tok = 4 * pass + t;
+    float2 v[8];
+    if (tok < n) {
+      // static register indices only (pass is 0 or 1)
+      decode16(pass ? x.raw[(4 + t) & 7] : x.raw[t], v);
+      const float s = ue8m0_to_float(pass ? x.sc[(4 + t) & 7] : x.sc[t]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = make_float2(v[i].x * s, v[i].y * s);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x.f[t][i] = v[i];
+  }
+}
+
+// This thread's partial dot products for its 8 rows of the stage and NP tokens.
+template <int K, int NP>
+__device__ __forceinline__ void stage_dot(const unsigned char *st, int g, int c, const XRegs &x,
+                                          float (&acc)[8 * NP]) {
+  constexpr int RG = 256 / (K / 16);
+  const unsigned char *sw = st;
+  const unsigned char *ss = st + kStageBytes;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = g + RG * j;
+    const uint4 wv = *reinterpret_cast<const uint4 *>(sw + r * K + 16 * c);
+    const float ws = ue8m0_to_float(ss[r * (K / kGroup) + (c >> 1)]);
+    float2 w[8];
+    decode16(wv, w);
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+      float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a = __ffma2_rn(w[i], x.f[t][i], a);
+      acc[j * NP + t] = ws * (a.x + a.y);
+    }
+  }
+}
+
+// Transposing butterfly over LANES lanes. On return, lane l holds CNT values;
+// value i has original index i + sum over halving steps s of
+// (l & (LANES >> (s+1))) ? (V >> (s+1)) : 0. Each is the full LANES-lane sum.
+// The additions follow the same tree (offsets LANES/2 ... 1) for every V.
+template <int V, int LANES>
+struct Butterfly {
+  static constexpr int LOGV = V == 8 ? 3 : V == 16 ? 4 : 5;
+  static constexpr int LOGL = LANES == 32 ? 5 : 4;
+  static constexpr int HSTEPS = LOGV < LOGL ? LOGV : LOGL;
+  static constexpr int CNT = V >> HSTEPS;
+  static constexpr int TAILMASK = (LANES >> HSTEPS) - 1;
+
+  __device__ __forceinline__ static void run(float (&a)[V], int l) {
+#pragma unroll
+    for (int s = 0; s < HSTEPS; ++s) {
+      const int off = LANES >> (s + 1);
+      const int half = (V >> s) / 2;
+      const bool upper = (l & off) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = upper ? a[i] : a[i + half];
+        const float keep = upper ? a[i + half] : a[i];
+        a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+      }
+    }
+#pragma unroll
+    for (int off = (LANES >> HSTEPS) / 2; off >= 1; off >>= 1)
+#pragma unroll
+      for (int i = 0; i < CNT; ++i) a[i] += __shfl_xor_sync(0xFFFFFFFFu, a[i], off);
+  }
+
+  __device__ __forceinline__ static int index(int l, int i) {
+    int idx = i;
+#pragma unroll
+    for (int s = 0; s < HSTEPS; ++s)
+      if (l & (LANES >> (s + 1))) idx += V >> (s + 1);
+    return idx;
+  }
+};
+
+__device__ __forceinline__ int32_t pick8(const int32_t (&v)[kTileRows], int i) {
+  int32_t r = v[0];
+#pragma unroll
+  for (int j = 1; j < kTileRows; ++j) r = (i == j) ? v[j] : r;
+  return r;
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// ------------------------------------------------------------------ unit decoding
+
+struct Unit {
+  int down;     // 0: gate/up, 1: down
+  int tile;     // index into tile_list
+  int block;    // b
+  int expert;   // e (E = shared)
+  int tile_in;  // j within the expert
+  int n;        // rows in this tile (1..8)
+};
+
+template <class S>
+__device__ __forceinline__ Unit decode_unit(const ExpertArgs &a, uint32_t u, int n_tiles) {
+  Unit r;
+  const uint32_t ngu = uint32_t(n_tiles) * S::NBG;
+  if (u < ngu) {
+    r.down = 0;
+    r.tile = int(u / S::NBG);
+    r.block = int(u % S::NBG);
+  } else {
+    const uint32_t v = u - ngu;
+    r.down = 1;
+    r.tile = int(v / S::NBD);
+    r.block = int(v % S::NBD);
+  }
+  const int32_t te = __ldg(a.tile_list + r.tile);
+  r.expert = te >> 16;
+  r.tile_in = te & 0xFFFF;
+  const int cnt = __ldg(a.counts + r.expert);
+  const int n = cnt - kTileRows * r.tile_in;
+  r.n = n < kTileRows ? n : kTileRows;
+  return r;
+}
+
+// ------------------------------------------------------------------ producer
+
+template <class S>
+__device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
+  const uint64_t pol = l2_evict_first_policy();
+  const uint32_t total = uint32_t(n_tiles) * (S::NBG + S::NBD);
+  const uint64_t pol_reuse = l2_evict_normal_policy();
+  // The producer's waits outlast the consumers' bounded ready wait, so a
+  // consumer that gives up on a tile always drains the ring first.
+  const int64_t wait_ns = 4 * a.timeout_ns;
+  int stage = 0;
+  uint32_t phase = 0;  // flips each time the ring wraps; empty-barrier parity is phase ^ 1
+  while (true) {
+    uint32_t u = atomicAdd(a.work, 1u);
+    if (ld_volatile(a.work + 1) != 0) u = total;  // abort: stop claiming
+    if (u >= total) {
+      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns)) {
+        report_error(a.status, MOE_ERR_TIMEOUT);
+        return;
+      }
+      sm.meta_unit[stage] = kDone;
+      sm.meta_step[stage] = 0;
+      mbar_arrive(&sm.full[stage]);
+      return;
+    }
+    const Unit un = decode_unit<S>(a, u, n_tiles);
+    const bool sh = un.expert == a.E;
+    const int e = sh ? 0 : un.expert;
+    // Weights of a single-tile expert are read once per step: evict first.
+    // A multi-tile expert's weights are read once per tile: keep them in L2.
+    const uint64_t pol_u = __ldg(a.counts + un.expert) > kTileRows ? pol_reuse : pol;
+    const int steps = un.down ? S::SPU_D : S::SPU_G;
+    for (int s = 0; s < steps; ++s) {
+      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns)) {
+        report_error(a.status, MOE_ERR_TIMEOUT);
+        atomicExch(a.work + 1, 1u);
+        return;
+      }
+      sm.meta_unit[stage] = u;
+      sm.meta_step[stage] = uint32_t(s);
+      unsigned char *dst = sm.stage[stage];
+      mbar_arrive_expect_tx(&sm.full[stage], uint32_t(kStageStride));
+      if (!un.down) {
+        // gate rows i0 .. i0 + RS/2, then up rows i0 .. i0 + RS/2
+        constexpr int HALF = S::RS_G / 2;
+        const int64_t i0 = int64_t(un.block) * 32 + int64_t(s) * HALF;
+        const uint8_t *wg = sh ? a.sh_w_gate : a.w_gate + int64_t(e) * S::I * S::H;
+        const uint8_t *wu = sh ? a.sh_w_up : a.w_up + int64_t(e) * S::I * S::H;
+        const uint8_t *sg = sh ? a.sh_s_gate : a.s_gate + int64_t(e) * S::I * (S::H / kGroup);
+        const uint8_t *su = sh ? a.sh_s_up : a.s_up + int64_t(e) * S::I * (S::H / kGroup);
+        bulk_g2s(dst, wg + i0 * S::H, HALF * S::H, &sm.full[stage], pol_u);
+        bulk_g2s(dst + kStageBytes / 2, wu + i0 * S::H, HALF * S::H, &sm.full[stage], pol_u);
+        bulk_g2s(dst + kStageBytes, sg + i0 * (S::H / kGroup), HALF * (S::H / kGroup), &sm.full[stage], pol_u);
+        bulk_g2s(dst + kStageBytes + kStageScaleBytes / 2, su + i0 * (S::H / kGroup), HALF * (S::H / kGroup),
+                 &sm.full[stage], pol_u);
+      } else {
+        const int64_t r0 = int64_t(un.block) * S::DB + int64_t(s) * S::RS_D;
+        const uint8_t *wd = sh ? a.sh_w_down : a.w_down + int64_t(e) * S::H * S::I;
+        const uint8_t *sd = sh ? a.sh_s_down : a.s_down + int64_t(e) * S::H * (S::I / kGroup);
+        bulk_g2s(dst, wd + r0 * S::I, kStageBytes, &sm.full[stage], pol_u);
+        bulk_g2s(dst + kStageBytes, sd + r0 * (S::I / kGroup), kStageScaleBytes, &sm.full[stage], pol_u);
+      }
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ consumers
+
+// Process one stage's rows for one pass of NP tokens: dot products, warp
+// reduction, and write the per-slot partial sums to red[par][pass].
+template <int K, int NP>
+__device__ __forceinline__ void stage_pass(ExpertSmem &sm, const unsigned char *st, int par, int pass,
+                                           const XRegs &x) {
+  constexpr int TPR = K / 16;
+  constexpr int LANES = TPR < 32 ? TPR : 32;
+  constexpr int V = 8 * NP;
+  using BF = Butterfly<V, LANES>;
+  const int tid = threadIdx.x;
+  const int g = tid / TPR, c = tid % TPR;
+  const int l = tid & (LANES - 1);
+  const int slot = tid / LANES;
+  float acc[V];
+  stage_dot<K, NP>(st, g, c, x, acc);
+  BF::run(acc, l);
+  if ((l & BF::TAILMASK) == 0) {
+#pragma unroll
+    for (int i = 0; i < BF::CNT; ++i) sm.red[par][pass][slot][BF::index(l, i)] = acc[i];
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void stage_pass_any(ExpertSmem &sm, const unsigned char *st, int par, int pass, int np,
+                                               const XRegs &x) {
+  if (np == 1) stage_pass<K, 1>(sm, st, par, pass, x);
+  else if (np == 2) stage_pass<K, 2>(sm, st, par, pass, x);
+  else stage_pass<K, 4>(sm, st, par, pass, x);
+}
+
+__device__ __forceinline__ void load_pass_any(XRegs &x, int pass, int np, int n) {
+  if (np == 1) load_pass<1>(x, pass, n);
+  else if (np == 2) load_pass<2>(x, pass, n);
+  else load_pass<4>(x, pass, n);
+}
+
+// Final cross-slot sums of one stage. Calls out(row_in_stage, token, value).
+template <int K, class F>
+__device__ __forceinline__ void stage_outputs(const ExpertSmem &sm, int par, int passes, int np, int n, F &&out) {
+  constexpr int TPR = K / 16;
+  constexpr int LANES = TPR < 32 ? TPR : 32;
+  constexpr int SPG = TPR / LANES;  // slots per row group
+  constexpr int RG = 256 / TPR;
+  const int per_pass = RG * 8 * np;
+  for (int o = threadIdx.x; o < passes * per_pass; o += kConsumers) {
+    const int pass = o / per_pass;
+    const int q = o % per_pass;
+    const int g = q / (8 * np);
+    const int v = q % (8 * np);
+    const int j = v / np, t = v % np;
+    const int tok = 4 * pass + t;
+    if (tok >= n) continue;
+    float s = sm.red[par][pass][g * SPG][v];
+#pragma unroll
+    for (int k = 1; k < SPG; ++k) s += sm.red[par][pass][g * SPG + k][v];
+    out(g + RG * j, tok, s);
+  }
+}
+
+template <class S>
+__device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
+  const int tid = threadIdx.x;
+  int stage = 0;
+  uint32_t phase = 0;  // full-barrier parity; flips each time the ring wraps
+  int par = 0;
+  Unit un{};
+  int32_t pairs[kTileRows];
+  XRegs x;
+  int np = 1, passes = 1;
+  bool skip = false;
+  while (true) {
+    if (!mbar_wait(&sm.full[stage], phase, 16 * a.timeout_ns)) {
+      report_error(a.status, MOE_ERR_TIMEOUT);
+      atomicExch(a.work + 1, 1u);
+      return;
+    }
+    const uint32_t u = sm.meta_unit[stage];
+    const int s = int(sm.meta_step[stage]);
+    if (u == kDone) return;
+    const unsigned char *st = sm.stage[stage];
+    if (s == 0) {
+      // ---- unit start: rows of the tile, and their x (or h) columns in registers
+      un = decode_unit<S>(a, u, n_tiles);
+      const int kcols = un.down ? S::I : S::H;
+      const int c = tid % (kcols / 16);
+      const int64_t rbase = int64_t(un.expert) * a.Tmax + int64_t(un.tile_in) * kTileRows;
+#pragma unroll
+      for (int r = 0; r < kTileRows; ++r) pairs[r] = r < un.n ? __ldg(a.rows_of + rbase + r) : 0;
+      skip = false;
+      if (un.down) {
+        if (tid == 0) {
+          int32_t ab = 0;
+          const uint64_t t0 = global_ns();
+          while (ld_acquire_gpu(a.ready + un.tile) < uint32_t(S::NBG)) {
+            if ((int64_t)(global_ns() - t0) > a.timeout_ns) {
+              report_error(a.status, MOE_ERR_TIMEOUT);
+              atomicExch(a.work + 1, 1u);
+              ab = 1;
+              break;
+            }
+            __nanosleep(64);
+          }
+          sm.abort_unit = ab;
+        }
+        consumer_sync();
+        skip = sm.abort_unit != 0;
+        if (!skip) {
+#pragma unroll
+          for (int r = 0; r < kTileRows; ++r) {
+            if (r < un.n) {
+              x.raw[r] = __ldcg(reinterpret_cast<const uint4 *>(a.hq + int64_t(pairs[r]) * S::I) + c);
+              x.sc[r] = __ldcg(a.hs + int64_t(pairs[r]) * (S::I / kGroup) + (c >> 1));
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < kTileRows; ++r) {
+          if (r < un.n) {
+            const int64_t tok = un.expert == a.E ? int64_t(pairs[r]) - int64_t(a.T) * a.k : int64_t(pairs[r] / a.k);
+            x.raw[r] = __ldg(reinterpret_cast<const uint4 *>(a.xq + tok * S::H) + c);
+            x.sc[r] = __ldg(a.xs + tok * (S::H / kGroup) + (c >> 1));
+          }
+        }
+      }
+      np = un.n <= 1 ? 1 : un.n <= 2 ? 2 : 4;
+      passes = un.n > 4 ? 2 : 1;
+      if (passes == 1) load_pass_any(x, 0, np, un.n);
+    }
+    // ---- this stage: dot products and warp reductions
+    if (!skip) {
+      for (int p = 0; p < passes; ++p) {
+        if (passes > 1) load_pass_any(x, p, np, un.n);
+        if (un.down) stage_pass_any<S::I>(sm, st, par, p, np, x);
+        else stage_pass_any<S::H>(sm, st, par, p, np, x);
+      }
+    }
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(&sm.empty[stage]);
+    consumer_sync();
+    // ---- cross-warp sums and outputs
+    if (!skip) {
+      if (un.down) {
+        const int64_t hrow0 = int64_t(un.block) * S::DB + int64_t(s) * S::RS_D;
+        stage_outputs<S::I>(sm, par, passes, np, un.n, [&](int r, int tok, float v) {
+          a.o[int64_t(pick8(pairs, tok)) * S::H + hrow0 + r] = v;
+        });
+      } else {
+        constexpr int HALF = S::RS_G / 2;
+        stage_outputs<S::H>(sm, par, passes, np, un.n, [&](int r, int tok, float v) {
+          const int which = r < HALF ? 0 : 1;
+          const int i = s * HALF + (r < HALF ? r : r - HALF);
+          sm.gu[tok][which][i] = v;
+        });
+      }
+    }
+    const bool last = s == (un.down ? S::SPU_D : S::SPU_G) - 1;
+    if (last && !un.down && !skip) {
+      // ---- gate/up epilogue: h = bf16(silu(bf16 g) * bf16 u), MXFP8 along I
+      consumer_sync();
+      const int w = tid >> 5, lane = tid & 31;
+      if (w < un.n) {
+        const float gb = bf16_bits_to_float(float_to_bf16_bits(sm.gu[w][0][lane]));
+        const float ub = bf16_bits_to_float(float_to_bf16_bits(sm.gu[w][1][lane]));
+        const float silu = gb / (1.0f + expf(-gb));
+        const uint16_t hb = float_to_bf16_bits(silu * ub);
+        const float hv = bf16_bits_to_float(hb);
+        float amax = fabsf(hv);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        const uint32_t code = mx_scale_code(amax);
+        const int64_t p = pick8(pairs, w);
+        a.hq[p * S::I + int64_t(un.block) * 32 + lane] = float_to_e4m3(mx_unscale(hv, code));
+        if (lane == 0) a.hs[p * (S::I / kGroup) + un.block] = uint8_t(code);
+        if (a.h_bf16) a.h_bf16[p * S::I + int64_t(un.block) * 32 + lane] = hb;
+        __threadfence();
+      }
+      consumer_sync();
+      if (tid == 0 && un.tile != a.skip_ready_tile) red_release_gpu_add(a.ready + un.tile, 1u);
+    }
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    par ^= 1;
+  }
+}
+
+template <int KG, int KD>
+__global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const ExpertArgs a) {
+  using S = Shape<KG, KD>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ExpertSmem &sm = *reinterpret_cast<ExpertSmem *>(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Everything below reads the router's outputs.
+  pdl_wait_primary();
+  const int n_tiles = __ldg(a.n_tiles);
+  if (warp == kConsumerWarps) {
+    if ((threadIdx.x & 31) == 0) producer<S>(a, sm, n_tiles);
+    return;
+  }
+  consumers<S>(a, sm, n_tiles);
+}
+
+template <int KG, int KD>
+cudaError_t prepare_shape() {
+  return cudaFuncSetAttribute(experts_kernel<KG, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(sizeof(ExpertSmem)));
+}
+
+template <int KG, int KD>
+cudaError_t launch_shape(const ExpertArgs &a, int grid, cudaStream_t st) {
+  const size_t smem = sizeof(ExpertSmem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kExpertThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, experts_kernel<KG, KD>, a);
+}
+
+}  // namespace
+
+size_t experts_smem_bytes() { return sizeof(ExpertSmem); }
+
+// Shapes compiled into the library: (H, I) = (4096, 2048), (1024, 512), (512, 256).
+bool experts_shape_supported(int H, int I) {
+  return (H == 4096 && I == 2048) || (H == 1024 && I == 512) || (H == 512 && I == 256);
+}
+
+cudaError_t prepare_experts(int H, int I) {
+  if (H == 4096 && I == 2048) return prepare_shape<4096, 2048>();
+  if (H == 1024 && I == 512) return prepare_shape<1024, 512>();
+  if (H == 512 && I == 256) return prepare_shape<512, 256>();
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_experts(const ExpertArgs &a, int grid, cudaStream_t st) {
+  if (a.H == 4096 && a.I == 2048) return launch_shape<4096, 2048>(a, grid, st);
+  if (a.H == 1024 && a.I == 512) return launch_shape<1024, 512>(a, grid, st);
+  if (a.H == 512 && a.I == 256) return launch_shape<512, 256>(a, grid, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

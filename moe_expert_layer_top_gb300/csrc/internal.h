@@ -1,0 +1,118 @@
+// internal.h — plan layout and kernel launchers shared by the .cu files of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kTileRows = 8;            // rows per expert tile
+constexpr int kGroup = 32;              // MXFP8 group along K
+constexpr int kConsumerWarps = 8;       // expert kernel: compute warps
+constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kStageBytes = 32768;      // weight bytes per pipeline stage
+constexpr int kStages = 5;              // pipeline depth
+constexpr int kRouteThreads = 1024;     // route kernel: block 0 (router + placement)
+constexpr int kQuantThreads = 256;      // route kernel: x-quantisation blocks (one group per thread)
+constexpr int kMaxTimedCalls = 4096;
+
+// Device scratch and schedule of one plan (all sized for max_rows).
+struct Scratch {
+  int32_t *topk_ids;    // [Tmax][k]
+  float *topk_w;        // [Tmax][k]
+  uint32_t *bitmap;     // [E][words]
+  int32_t *counts;      // [E + 1]    (index E: shared expert)
+  int32_t *slot;        // [Tmax][k]
+  int32_t *rows_of;     // [E + 1][Tmax] pair ids in rank order
+  int32_t *tile_list;   // [n_tiles_max] (expert << 16) | tile
+  int32_t *n_tiles;     // [1]
+  uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile
+  uint32_t *work;       // [2] unit counter, abort flag
+  int32_t *status;      // [1] plan-owned status word
+  uint8_t *xq, *xs;     // [Tmax][H], [Tmax][H/32]
+  uint8_t *hq, *hs;     // [P][I], [P][I/32]
+  uint16_t *h_bf16;     // [P][I]
+  float *o;             // [P][H]
+  // staging for moe_forward_host
+  void *x_dev;
+  float *logits_dev;
+  void *y_dev;
+};
+
+struct Plan {
+  moe_config_t cfg;
+  moe_weights_t w;
+  int device;
+  int num_sms;
+  int words;             // ceil(max_rows / 32)
+  int n_tiles_max;       // upper bound on tiles in a step
+  int64_t pairs_max;     // P for T = max_rows
+  int64_t timeout_ns;
+  Scratch s;
+  void *arena;           // single device allocation backing Scratch
+  size_t arena_bytes;
+  // timing
+  cudaEvent_t ev_start[kMaxTimedCalls];
+  cudaEvent_t ev_stop[kMaxTimedCalls];
+  int timed_calls;
+  bool events_created;
+};
+
+struct RouteArgs {
+  const float *logits;
+  const uint16_t *x;
+  int T, H, E, k, shared, words, Tmax;
+  int32_t *topk_ids;
+  float *topk_w;
+  uint32_t *bitmap;
+  int32_t *counts;
+  int32_t *slot;
+  int32_t *rows_of;
+  int32_t *tile_list;
+  int32_t *n_tiles;
+  uint32_t *ready;
+  int n_tiles_max;
+  uint32_t *work;
+  int32_t *status;
+  uint8_t *xq, *xs;
+};
+
+struct ExpertArgs {
+  const uint8_t *w_gate, *s_gate, *w_up, *s_up, *w_down, *s_down;
+  const uint8_t *sh_w_gate, *sh_s_gate, *sh_w_up, *sh_s_up, *sh_w_down, *sh_s_down;
+  int T, H, I, E, k, Tmax;
+  const int32_t *counts;
+  const int32_t *rows_of;
+  const int32_t *tile_list;
+  const int32_t *n_tiles;
+  const uint8_t *xq, *xs;
+  uint8_t *hq, *hs;
+  uint16_t *h_bf16;  // NULL unless the h tap is requested
+  float *o;
+  uint32_t *ready;
+  uint32_t *work;
+  int32_t *status;
+  int64_t timeout_ns;
+  int skip_ready_tile;  // fault injection: tile index whose ready count is never published, or -1
+};
+
+struct CombineArgs {
+  const float *o;
+  const float *topk_w;
+  int T, H, k, shared;
+  uint16_t *y;
+};
+
+size_t route_smem_bytes(int E, int words);
+cudaError_t prepare_route(size_t smem);
+cudaError_t prepare_experts(int H, int I);
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
+cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int cols, uint8_t *q, uint8_t *s, cudaStream_t st);
+cudaError_t launch_experts(const ExpertArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t st);
+bool experts_shape_supported(int H, int I);
+size_t experts_smem_bytes();
+
+}  // namespace moe

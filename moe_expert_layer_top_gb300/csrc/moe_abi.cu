@@ -1,0 +1,413 @@
+// moe_abi.cu — the C ABI: Guard + Build (moe_plan), Runtime (moe_forward), teardown.
+//
+// The four-stage plugin contract follows "SGLang's Low-Latency Mode Boosts
+// DeepSeek-V4.1-Flash Speed by 1.56x on AMD", "Four stages keep megakernels
+// outside core": Register, Guard, Build, Runtime.
+// - Guard rejects unsupported shapes and devices with MOE_ERR_UNSUPPORTED. It
+//   does not fall back.
+// - Build allocates every scratch buffer once for max_rows. "Beyond Day-0:
+//   Optimizing DeepSeek-V4.1 Flash in SGLang" 2.1 reuses scratch buffers
+//   across calls to avoid re-initialisation.
+// - Runtime enqueues three kernels:
+//     1. route + place + quantise x;
+//     2. the persistent expert kernel, launched with Programmatic Dependent
+//        Launch;
+//     3. the combine.
+//   It allocates nothing and does not synchronise.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+
+#include "internal.h"
+#include "moe.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// Pure host checks of the Guard (no device access).
+moe_status_t guard_config(const moe_config_t &c) {
+  if (c.hidden <= 0 || c.intermediate <= 0 || c.num_experts <= 0 || c.top_k <= 0 || c.max_rows <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c.num_shared != 0 && c.num_shared != 1) return MOE_ERR_INVALID_ARG;
+  if (c.top_k > c.num_experts) return MOE_ERR_INVALID_ARG;
+  if (c.hidden % 32 || c.intermediate % 32) return MOE_ERR_UNSUPPORTED;
+  if (!is_pow2(c.hidden) || !is_pow2(c.intermediate)) return MOE_ERR_UNSUPPORTED;
+  if (!experts_shape_supported(c.hidden, c.intermediate)) return MOE_ERR_UNSUPPORTED;
+  if (c.num_experts + c.num_shared > kRouteThreads) return MOE_ERR_UNSUPPORTED;
+  if (c.top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (c.max_rows > 4096) return MOE_ERR_UNSUPPORTED;
+  const int words = (c.max_rows + 31) / 32;
+  if (route_smem_bytes(c.num_experts, words) > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t guard_weights(const moe_config_t &c, const moe_weights_t &w) {
+  const void *routed[6] = {w.w_gate, w.s_gate, w.w_up, w.s_up, w.w_down, w.s_down};
+  const void *shared[6] = {w.sh_w_gate, w.sh_s_gate, w.sh_w_up, w.sh_s_up, w.sh_w_down, w.sh_s_down};
+  for (const void *p : routed)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  for (const void *p : shared) {
+    if (c.num_shared && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
+    if (!c.num_shared && p) return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+void destroy_plan(Plan *p) {
+  if (!p) return;
+  if (p->events_created) {
+    for (int i = 0; i < kMaxTimedCalls; ++i) {
+      if (p->ev_start[i]) cudaEventDestroy(p->ev_start[i]);
+      if (p->ev_stop[i]) cudaEventDestroy(p->ev_stop[i]);
+    }
+  }
+  if (p->arena) cudaFree(p->arena);
+  delete p;
+}
+
+moe_status_t copy_taps(Plan *p, const moe_taps_t *t, int T, cudaStream_t st) {
+  if (!t) return MOE_OK;
+  const moe_config_t &c = p->cfg;
+  const int64_t P = int64_t(T) * c.top_k + int64_t(T) * c.num_shared;
+  const int words = (T + 31) / 32;
+  auto cp = [&](void *dst, const void *src, size_t bytes) -> bool {
+    if (!dst || bytes == 0) return true;
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st) == cudaSuccess;
+  };
+  bool ok = true;
+  ok &= cp(t->topk_ids, p->s.topk_ids, size_t(T) * c.top_k * 4);
+  ok &= cp(t->topk_w, p->s.topk_w, size_t(T) * c.top_k * 4);
+  ok &= cp(t->counts, p->s.counts, size_t(c.num_experts) * 4);
+  ok &= cp(t->slot, p->s.slot, size_t(T) * c.top_k * 4);
+  ok &= cp(t->xq, p->s.xq, size_t(T) * c.hidden);
+  ok &= cp(t->xs, p->s.xs, size_t(T) * (c.hidden / 32));
+  ok &= cp(t->hq, p->s.hq, size_t(P) * c.intermediate);
+  ok &= cp(t->hs, p->s.hs, size_t(P) * (c.intermediate / 32));
+  ok &= cp(t->h_bf16, p->s.h_bf16, size_t(P) * c.intermediate * 2);
+  ok &= cp(t->o, p->s.o, size_t(P) * c.hidden * 4);
+  if (t->bitmap) {
+    // plan rows are ceil(max_rows/32) words wide; the tap is ceil(T/32) wide
+    ok &= cudaMemcpy2DAsync(t->bitmap, size_t(words) * 4, p->s.bitmap, size_t(p->words) * 4, size_t(words) * 4,
+                            c.num_experts, cudaMemcpyDeviceToDevice, st) == cudaSuccess;
+  }
+  return ok ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_OOM: return "MOE_ERR_OOM";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, void *cuda_stream,
+                      void **plan_out) {
+  (void)cuda_stream;
+  if (plan_out) *plan_out = nullptr;
+  if (!config || !weights || !plan_out) return MOE_ERR_INVALID_ARG;
+  const moe_config_t c = *config;
+  moe_status_t g = guard_config(c);
+  if (g != MOE_OK) return g;
+  g = guard_weights(c, *weights);
+  if (g != MOE_OK) return g;
+
+  // ---- device part of the Guard
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
+
+  // ---- Build
+  Plan *p = new (std::nothrow) Plan();
+  if (!p) return MOE_ERR_OOM;
+  memset(p, 0, sizeof(Plan));
+  p->cfg = c;
+  p->w = *weights;
+  p->device = dev;
+  p->num_sms = sms;
+  p->timeout_ns = c.wait_timeout_ns > 0 ? c.wait_timeout_ns : 200000000LL;
+  const int Tm = c.max_rows, E = c.num_experts, k = c.top_k, H = c.hidden, I = c.intermediate;
+  p->words = (Tm + 31) / 32;
+  const int64_t pairs_routed = int64_t(Tm) * k;
+  p->pairs_max = pairs_routed + int64_t(Tm) * c.num_shared;
+  const int64_t active_max = pairs_routed < E ? pairs_routed : E;
+  p->n_tiles_max = int(pairs_routed / kTileRows + active_max + (c.num_shared ? (Tm + kTileRows - 1) / kTileRows : 0));
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  const size_t o_ids = take(pairs_routed * 4), o_w = take(pairs_routed * 4);
+  const size_t o_bm = take(size_t(E) * p->words * 4), o_cnt = take(size_t(E + 1) * 4);
+  const size_t o_slot = take(pairs_routed * 4), o_rows = take(size_t(E + 1) * Tm * 4);
+  const size_t o_tl = take(size_t(p->n_tiles_max) * 4), o_nt = take(4);
+  const size_t o_ready = take(size_t(p->n_tiles_max) * 4), o_work = take(8), o_status = take(4);
+  const size_t o_xq = take(size_t(Tm) * H), o_xs = take(size_t(Tm) * (H / 32));
+  const size_t o_hq = take(size_t(p->pairs_max) * I), o_hs = take(size_t(p->pairs_max) * (I / 32));
+  const size_t o_hb = take(size_t(p->pairs_max) * I * 2), o_o = take(size_t(p->pairs_max) * H * 4);
+  const size_t o_xd = take(size_t(Tm) * H * 2), o_ld = take(size_t(Tm) * E * 4), o_yd = take(size_t(Tm) * H * 2);
+  p->arena_bytes = off;
+  if (cudaMalloc(&p->arena, off) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return MOE_ERR_OOM;
+  }
+  unsigned char *base = static_cast<unsigned char *>(p->arena);
+  Scratch &s = p->s;
+  s.topk_ids = reinterpret_cast<int32_t *>(base + o_ids);
+  s.topk_w = reinterpret_cast<float *>(base + o_w);
+  s.bitmap = reinterpret_cast<uint32_t *>(base + o_bm);
+  s.counts = reinterpret_cast<int32_t *>(base + o_cnt);
+  s.slot = reinterpret_cast<int32_t *>(base + o_slot);
+  s.rows_of = reinterpret_cast<int32_t *>(base + o_rows);
+  s.tile_list = reinterpret_cast<int32_t *>(base + o_tl);
+  s.n_tiles = reinterpret_cast<int32_t *>(base + o_nt);
+  s.ready = reinterpret_cast<uint32_t *>(base + o_ready);
+  s.work = reinterpret_cast<uint32_t *>(base + o_work);
+  s.status = reinterpret_cast<int32_t *>(base + o_status);
+  s.xq = base + o_xq;
+  s.xs = base + o_xs;
+  s.hq = base + o_hq;
+  s.hs = base + o_hs;
+  s.h_bf16 = reinterpret_cast<uint16_t *>(base + o_hb);
+  s.o = reinterpret_cast<float *>(base + o_o);
+  s.x_dev = base + o_xd;
+  s.logits_dev = reinterpret_cast<float *>(base + o_ld);
+  s.y_dev = base + o_yd;
+  if (cudaMemset(p->arena, 0, off) != cudaSuccess) {
+    destroy_plan(p);
+    return MOE_ERR_CUDA;
+  }
+  if (prepare_route(route_smem_bytes(E, p->words)) != cudaSuccess || prepare_experts(H, I) != cudaSuccess) {
+    destroy_plan(p);
+    return MOE_ERR_CUDA;
+  }
+  if (c.flags & MOE_FLAG_TIMING) {
+    for (int i = 0; i < kMaxTimedCalls; ++i) {
+      if (cudaEventCreate(&p->ev_start[i]) != cudaSuccess || cudaEventCreate(&p->ev_stop[i]) != cudaSuccess) {
+        p->events_created = true;
+        destroy_plan(p);
+        return MOE_ERR_CUDA;
+      }
+    }
+    p->events_created = true;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    destroy_plan(p);
+    return MOE_ERR_CUDA;
+  }
+  *plan_out = p;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t T, void *y,
+                         const moe_taps_t *taps, int32_t *d_status, void *cuda_stream) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > p->cfg.max_rows) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !logits || !y || !aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(logits) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(p->device);
+  if (!dg.ok) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const moe_config_t &c = p->cfg;
+  Scratch &s = p->s;
+  int32_t *status = d_status ? d_status : s.status;
+
+  RouteArgs ra;
+  ra.logits = logits;
+  ra.x = static_cast<const uint16_t *>(x);
+  ra.T = T;
+  ra.H = c.hidden;
+  ra.E = c.num_experts;
+  ra.k = c.top_k;
+  ra.shared = c.num_shared;
+  ra.words = p->words;
+  ra.Tmax = c.max_rows;
+  ra.topk_ids = s.topk_ids;
+  ra.topk_w = s.topk_w;
+  ra.bitmap = s.bitmap;
+  ra.counts = s.counts;
+  ra.slot = s.slot;
+  ra.rows_of = s.rows_of;
+  ra.tile_list = s.tile_list;
+  ra.n_tiles = s.n_tiles;
+  ra.ready = s.ready;
+  ra.n_tiles_max = p->n_tiles_max;
+  ra.work = s.work;
+  ra.status = status;
+  ra.xq = s.xq;
+  ra.xs = s.xs;
+  if (launch_route(ra, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  ExpertArgs ea;
+  ea.w_gate = p->w.w_gate;
+  ea.s_gate = p->w.s_gate;
+  ea.w_up = p->w.w_up;
+  ea.s_up = p->w.s_up;
+  ea.w_down = p->w.w_down;
+  ea.s_down = p->w.s_down;
+  ea.sh_w_gate = p->w.sh_w_gate;
+  ea.sh_s_gate = p->w.sh_s_gate;
+  ea.sh_w_up = p->w.sh_w_up;
+  ea.sh_s_up = p->w.sh_s_up;
+  ea.sh_w_down = p->w.sh_w_down;
+  ea.sh_s_down = p->w.sh_s_down;
+  ea.T = T;
+  ea.H = c.hidden;
+  ea.I = c.intermediate;
+  ea.E = c.num_experts;
+  ea.k = c.top_k;
+  ea.Tmax = c.max_rows;
+  ea.counts = s.counts;
+  ea.rows_of = s.rows_of;
+  ea.tile_list = s.tile_list;
+  ea.n_tiles = s.n_tiles;
+  ea.xq = s.xq;
+  ea.xs = s.xs;
+  ea.hq = s.hq;
+  ea.hs = s.hs;
+  ea.h_bf16 = (taps && taps->h_bf16) ? s.h_bf16 : nullptr;
+  ea.o = s.o;
+  ea.ready = s.ready;
+  ea.work = s.work;
+  ea.status = status;
+  ea.timeout_ns = p->timeout_ns;
+  ea.skip_ready_tile = (c.flags & MOE_FLAG_TEST_SKIP_READY) ? 0 : -1;
+  const bool timed = (c.flags & MOE_FLAG_TIMING) && p->timed_calls < kMaxTimedCalls;
+  if (timed && cudaEventRecord(p->ev_start[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_experts(ea, p->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (timed) {
+    if (cudaEventRecord(p->ev_stop[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
+    ++p->timed_calls;
+  }
+
+  CombineArgs ca;
+  ca.o = s.o;
+  ca.topk_w = s.topk_w;
+  ca.T = T;
+  ca.H = c.hidden;
+  ca.k = c.top_k;
+  ca.shared = c.num_shared;
+  ca.y = static_cast<uint16_t *>(y);
+  if (launch_combine(ca, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return copy_taps(p, taps, T, st);
+}
+
+moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logits_host, int32_t T, void *y_host,
+                              void *cuda_stream) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > p->cfg.max_rows) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !logits_host || !y_host) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(p->device);
+  if (!dg.ok) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const moe_config_t &c = p->cfg;
+  const size_t xb = size_t(T) * c.hidden * 2, lb = size_t(T) * c.num_experts * 4;
+  if (cudaMemcpyAsync(p->s.x_dev, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(p->s.logits_dev, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status_t r = moe_forward(plan, p->s.x_dev, p->s.logits_dev, T, p->s.y_dev, nullptr, nullptr, cuda_stream);
+  if (r != MOE_OK) return r;
+  if (cudaMemcpyAsync(y_host, p->s.y_dev, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t dev_status = 0;
+  if (cudaMemcpyAsync(&dev_status, p->s.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status_t>(dev_status);
+}
+
+moe_status_t moe_quantize_mxfp8(const void *x, int64_t rows, int32_t cols, uint8_t *q, uint8_t *s, void *cuda_stream) {
+  if (rows < 0 || cols <= 0 || cols % 32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || !s || !aligned16(x) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (launch_quantize(static_cast<const uint16_t *>(x), rows, cols, q, s, static_cast<cudaStream_t>(cuda_stream)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_kernel_times(void *plan, double *expert_ms_out, int32_t *launches_out) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p || !expert_ms_out || !launches_out) return MOE_ERR_INVALID_ARG;
+  if (!(p->cfg.flags & MOE_FLAG_TIMING)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(p->device);
+  double total = 0.0;
+  for (int i = 0; i < p->timed_calls; ++i) {
+    if (cudaEventSynchronize(p->ev_stop[i]) != cudaSuccess) return MOE_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p->ev_start[i], p->ev_stop[i]) != cudaSuccess) return MOE_ERR_CUDA;
+    total += ms;
+  }
+  *expert_ms_out = total;
+  *launches_out = p->timed_calls;
+  p->timed_calls = 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_plan_status(void *plan, int32_t *status_out) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p || !status_out) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(p->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, p->s.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  *status_out = v;
+  return MOE_OK;
+}
+
+moe_status_t moe_destroy(void *plan) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p) return MOE_OK;
+  DeviceGuard dg(p->device);
+  const bool ok = cudaDeviceSynchronize() == cudaSuccess;
+  destroy_plan(p);
+  return ok ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

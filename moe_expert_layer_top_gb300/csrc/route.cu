@@ -1,0 +1,253 @@
+// route.cu — router top-k + combine weights, sort-free tile placement, and
+// MXFP8 quantisation of the token rows, in one launch.
+//
+// Block 0 routes and places.
+//  - Top-k per token row uses one warp per row, in k rounds of warp argmax.
+//  - The combine weights are a softmax over the selected logits in binary32,
+//    using exp_rn.
+//  - Token bitmaps are built per expert in shared memory.
+//  - Placement uses population counts: rank(t, e) = popc(bits of expert e
+//    below t). Tile = rank / 8 and row = rank % 8.
+// This follows "SGLang's Low-Latency Mode Boosts DeepSeek-V4.1-Flash Speed by
+// 1.56x on AMD", "NVIDIA overlaps the dependency chain", bullet "Routing
+// without sorting". A bitmap and population counts place the 8-row tiles with
+// no scan or sort, keeping the top-k choices. It also follows "Beyond Day-0:
+// Optimizing DeepSeek-V4.1 Flash in SGLang" 2.1: the router writes the layout
+// the expert kernel consumes. That layout is:
+//   rows_of[e][rank]   pair ids (t*k + j), in token order;
+//   tile_list[]        (expert, tile) work items for the expert kernel.
+// The tile list's per-expert offsets come from one block-wide prefix over
+// the E+1 tile counts. That is work enumeration, not row placement.
+//
+// Blocks 1.. quantise x to MXFP8 (one 32-group per thread). "Beyond Day-0"
+// 2.1 fuses activation quantisation into the producer, and here it shares
+// the launch with the router.
+#include <stdint.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ MXFP8 group quantiser (shared by x and moe_quantize_mxfp8)
+
+__device__ __forceinline__ void quantize_group32(const uint16_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                                 uint8_t *__restrict__ scale) {
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 r = __ldg(s4 + i);
+    w[4 * i + 0] = r.x;
+    w[4 * i + 1] = r.y;
+    w[4 * i + 2] = r.z;
+    w[4 * i + 3] = r.w;
+  }
+  float v[32];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+  }
+  const uint32_t code = mx_scale_code(amax);
+  uint32_t q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t b0 = float_to_e4m3(mx_unscale(v[4 * i + 0], code));
+    uint32_t b1 = float_to_e4m3(mx_unscale(v[4 * i + 1], code));
+    uint32_t b2 = float_to_e4m3(mx_unscale(v[4 * i + 2], code));
+    uint32_t b3 = float_to_e4m3(mx_unscale(v[4 * i + 3], code));
+    q[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+  d4[0] = make_uint4(q[0], q[1], q[2], q[3]);
+  d4[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  *scale = static_cast<uint8_t>(code);
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const uint16_t *__restrict__ x, int64_t groups,
+                                                                 uint8_t *__restrict__ q, uint8_t *__restrict__ s) {
+  for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < groups; g += int64_t(gridDim.x) * blockDim.x)
+    quantize_group32(x + g * kGroup, q + g * kGroup, s + g);
+}
+
+// ------------------------------------------------------------------ router + placement (block 0)
+
+struct RouteSmem {
+  // followed in dynamic shared memory by uint32_t bitmap[E][words]
+  int32_t sel_i[kRouteThreads / 32][32];
+  float sel_v[kRouteThreads / 32][32];
+  int32_t tiles[kRouteThreads];
+  int32_t offs[kRouteThreads];
+  int32_t warp_sums[kRouteThreads / 32];
+};
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E, k = a.k, T = a.T, W = a.words;
+
+  if (tid == 0) {
+    *a.status = MOE_OK;  // start of the step
+    a.work[0] = 0;       // unit counter
+    a.work[1] = 0;       // abort flag
+  }
+  for (int i = tid; i < a.n_tiles_max; i += blockDim.x) a.ready[i] = 0;
+  for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0;
+  __syncthreads();
+
+  // --- top-k + combine weights: one warp per token row
+  for (int t = warp; t < T; t += kRouteThreads / 32) {
+    const float *row = a.logits + int64_t(t) * E;
+    uint32_t taken = 0;  // bit j: this lane's candidate lane + 32*j already selected
+    for (int r = 0; r < k; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7FFFFFFF;
+      for (int j = 0; j * 32 + lane < E; ++j) {
+        if (taken & (1u << j)) continue;
+        const int i = j * 32 + lane;
+        const float v = __ldg(row + i);
+        if (better(v, i, bv, bi)) { bv = v; bi = i; }
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (bi >= E) {  // only possible with NaN logits: take the lowest unselected id
+        report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
+        int cand = 0x7FFFFFFF;
+        for (int j = 0; j * 32 + lane < E; ++j)
+          if (!(taken & (1u << j))) { cand = j * 32 + lane; break; }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) cand = min(cand, __shfl_xor_sync(0xFFFFFFFFu, cand, off));
+        bi = cand;
+        bv = __ldg(row + bi);
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == 0) { sm.sel_i[warp][r] = bi; sm.sel_v[warp][r] = bv; }
+    }
+    __syncwarp();
+    // weights: e_j = exp_rn(l_j - l_0); s = ((e_0 + e_1) + ...) ; w_j = e_j / s
+    float e = 0.0f;
+    if (lane < k) e = exp_rn(__fsub_rn(sm.sel_v[warp][lane], sm.sel_v[warp][0]));
+    float s = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const float ej = __shfl_sync(0xFFFFFFFFu, e, j);
+      s = (j == 0) ? ej : __fadd_rn(s, ej);
+    }
+    if (lane < k) {
+      const int id = sm.sel_i[warp][lane];
+      a.topk_ids[int64_t(t) * k + lane] = id;
+      a.topk_w[int64_t(t) * k + lane] = __fdiv_rn(e, s);
+      atomicOr(&bm[id * W + (t >> 5)], 1u << (t & 31));
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // --- counts and tiles per expert (index E: the shared expert, every row)
+  const int nexp = E + a.shared;
+  if (tid < nexp) {
+    int cnt;
+    if (tid < E) {
+      cnt = 0;
+      for (int w = 0; w < W; ++w) cnt += __popc(bm[tid * W + w]);
+    } else {
+      cnt = T;
+    }
+    a.counts[tid] = cnt;
+    sm.tiles[tid] = (cnt + kTileRows - 1) / kTileRows;
+  } else {
+    sm.tiles[tid] = 0;
+  }
+  // block-wide exclusive prefix of tiles[] (work enumeration for the expert kernel)
+  int v = sm.tiles[tid];
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, v, off);
+    if (lane >= off) v += u;
+  }
+  if (lane == 31) sm.warp_sums[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = sm.warp_sums[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, ws, off);
+      if (lane >= off) ws += u;
+    }
+    sm.warp_sums[lane] = ws;  // inclusive
+  }
+  __syncthreads();
+  const int excl = v - sm.tiles[tid] + (warp ? sm.warp_sums[warp - 1] : 0);
+  if (tid < nexp) {
+    for (int j = 0; j < sm.tiles[tid]; ++j) {
+      const int idx = excl + j;
+      if (idx < a.n_tiles_max) a.tile_list[idx] = (tid << 16) | j;
+      else report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
+    }
+  }
+  if (tid == kRouteThreads - 1) *a.n_tiles = min(excl + sm.tiles[tid], a.n_tiles_max);
+
+  // --- placement: rank by population count of lower token bits
+  for (int p = tid; p < T * k; p += blockDim.x) {
+    const int t = p / k;
+    const int e = a.topk_ids[p];
+    const uint32_t *b = bm + e * W;
+    int rank = __popc(b[t >> 5] & ((1u << (t & 31)) - 1u));
+    for (int w = 0; w < (t >> 5); ++w) rank += __popc(b[w]);
+    a.slot[p] = (e << 16) | rank;
+    a.rows_of[int64_t(e) * a.Tmax + rank] = p;
+  }
+  if (a.shared)
+    for (int t = tid; t < T; t += blockDim.x) a.rows_of[int64_t(E) * a.Tmax + t] = T * k + t;
+  for (int i = tid; i < E * W; i += blockDim.x) a.bitmap[i] = bm[i];
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a) {
+  extern __shared__ __align__(16) unsigned char route_smem[];
+  // Let the expert kernel's blocks get scheduled early; it waits for this grid before reading.
+  pdl_launch_dependents();
+  if (blockIdx.x == 0) {
+    RouteSmem &sm = *reinterpret_cast<RouteSmem *>(route_smem);
+    uint32_t *bm = reinterpret_cast<uint32_t *>(route_smem + sizeof(RouteSmem));
+    route_block(a, sm, bm);
+    return;
+  }
+  const int64_t groups = int64_t(a.T) * (a.H / kGroup);
+  for (int64_t g = int64_t(blockIdx.x - 1) * blockDim.x + threadIdx.x; g < groups;
+       g += int64_t(gridDim.x - 1) * blockDim.x)
+    quantize_group32(a.x + g * kGroup, a.xq + g * kGroup, a.xs + g);
+}
+
+size_t route_smem_bytes(int E, int words) { return sizeof(RouteSmem) + size_t(E) * words * sizeof(uint32_t); }
+
+cudaError_t prepare_route(size_t smem) {
+  return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+}
+
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
+  const size_t smem = route_smem_bytes(a.E, a.words);
+  const int64_t groups = int64_t(a.T) * (a.H / kGroup);
+  const int qblocks = int((groups + kRouteThreads - 1) / kRouteThreads);
+  route_kernel<<<1 + qblocks, kRouteThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int cols, uint8_t *q, uint8_t *s, cudaStream_t st) {
+  const int64_t groups = rows * (cols / kGroup);
+  if (groups == 0) return cudaSuccess;
+  int64_t blocks = (groups + kQuantThreads - 1) / kQuantThreads;
+  if (blocks > 65535 * 16) blocks = 65535 * 16;
+  quantize_kernel<<<unsigned(blocks), kQuantThreads, 0, st>>>(x, groups, q, s);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

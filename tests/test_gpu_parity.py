@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, on seeded inputs.
+
+Small cases are compared element by element. They span several tiles, ragged
+tail tiles, multi-tile experts, k = 1, k = E and a shared expert.
+* Routing, placement and x quantisation: bit-exact.
+* h quantisation: bit-exact on the GPU's own bf16 h.
+* y: within the stated tolerance.
+Properties are also checked: determinism, token-permutation invariance, the
+empty step, argument errors, and a host-injected bounded-wait timeout.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from moe_expert_layer_top_gb300 import abi, synthetic
+from moe_expert_layer_top_gb300.layer import MoEStep, quantize_mxfp8
+
+from gpu_cases import (GpuRun, bf16_dev_to_bits, check_h_close, check_h_quantizer_bit_exact,
+                       check_routing_bit_exact, check_xquant_bit_exact, check_y, oracle_experts, rel_fro, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import moe_expert_layer_top_gb300 as pkg
+    pkg.build.build()
+    abi.load()
+    assert torch.cuda.is_available()
+
+
+# ----------------------------------------------------------------- generator and quantiser
+
+def test_device_generator_matches_host_generator():
+    import synth.gpu
+    n, start = 1 << 20, 12345
+    out = torch.empty(n, dtype=torch.int16, device="cuda")
+    synth.gpu.normal_bf16(42, synth.stream_gate(7), start, n, synth.expert_sigma(4096), out.data_ptr(),
+                          torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    ref = synth.normal_bf16(42, synth.stream_gate(7), start, n, synth.expert_sigma(4096))
+    np.testing.assert_array_equal(to_np(out).view(np.uint16), ref)
+
+
+def _quant_both(bits: np.ndarray):
+    x = torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    q, s = quantize_mxfp8(x)
+    torch.cuda.synchronize()
+    qr, sr = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(bits))
+    np.testing.assert_array_equal(to_np(q), qr)
+    np.testing.assert_array_equal(to_np(s), sr)
+
+
+def test_quantiser_exhaustive_bf16_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_bits_to_f64(bits)
+    finite = bits[np.isfinite(vals)]
+    pad = (-len(finite)) % 32
+    finite = np.concatenate([finite, np.zeros(pad, dtype=np.uint16)])
+    _quant_both(finite.reshape(-1, 32))                                   # sorted: similar magnitudes
+    rng = np.random.default_rng(0)
+    _quant_both(rng.permutation(finite).reshape(-1, 32))                   # mixed magnitudes
+    # every pattern against fixed group maxima 1.0, 2^-100 and 2^100 (small values relative to the scale)
+    for amax_bits in (0x3F80, 0x0D80, 0x7180):
+        g = finite.reshape(-1, 32).copy()
+        g[:, 0] = amax_bits
+        keep = np.abs(oracle.bf16_bits_to_f64(g)).max(axis=1) <= oracle.bf16_bits_to_f64(np.uint16(amax_bits))
+        _quant_both(g[keep])
+
+
+def test_quantiser_special_groups():
+    rows = []
+    rows.append(np.zeros(32, dtype=np.uint16))                                 # all +0
+    rows.append(np.full(32, 0x8000, dtype=np.uint16))                          # all -0
+    rows.append(np.arange(1, 33, dtype=np.uint16))                             # bf16 subnormals only
+    rows.append(np.full(32, 0x7F7F, dtype=np.uint16))                          # largest finite bf16
+    rows.append(np.array([0x3F80] + [0x3780] * 31, dtype=np.uint16))          # 1.0 with 2^-16 entries
+    _quant_both(np.stack(rows))
+
+
+# ----------------------------------------------------------------- small cases, full comparison
+
+SMALL = [
+    # T, H, E, k, I, routing, shared
+    (6, 512, 8, 2, 256, "uniform", 0),        # the tiny workload
+    (40, 512, 8, 2, 256, "zipf", 0),          # multi-tile experts with ragged tails
+    (1, 512, 8, 1, 256, "uniform", 0),        # single row, k = 1
+    (13, 512, 8, 8, 256, "uniform", 0),       # k = E: every expert active
+    (24, 512, 16, 4, 256, "zipf", 1),         # shared expert
+    (20, 1024, 16, 4, 512, "uniform", 0),     # second compiled shape
+    (70, 512, 8, 3, 256, "zipf", 1),          # > 64 rows: several bitmap words, hot expert with 9 tiles
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"T{c[0]}_H{c[1]}_E{c[2]}_k{c[3]}_sh{c[6]}" for c in SMALL])
+def test_small_case_parity(case):
+    T, H, E, k, I, routing, shared = case
+    g = GpuRun(T, H, E, k, I, routing, shared, seed=42 + T).run()
+    assert g.status_code == abi.MOE_OK
+    get = oracle_experts(42 + T, E, H, I)
+    sh = oracle.expert_weights_from_synth(42 + T, "shared", H, I) if shared else None
+    r = oracle.moe_step(g.x_bits, g.lg, k, get, shared=sh)
+    check_routing_bit_exact(g, r)
+    check_xquant_bit_exact(g, r)
+    check_h_quantizer_bit_exact(g)
+    P = T * k + T * shared
+    check_h_close(g, r, np.arange(P))
+    assert rel_fro(g.t["o"], r["o"]) <= 1e-2
+    check_y(g.y_bits, r["y"])
+    g.close()
+
+
+def test_weights_prepared_on_device_match_oracle_quantisation():
+    w = synthetic.make_weights(7, 3, 512, 256, 1)
+    for e in range(3):
+        ref = oracle.expert_weights_from_synth(7, e, 512, 256)
+        np.testing.assert_array_equal(to_np(w.w_gate[e]), ref.w_gate)
+        np.testing.assert_array_equal(to_np(w.s_up[e]), ref.s_up)
+        np.testing.assert_array_equal(to_np(w.w_down[e]), ref.w_down)
+        np.testing.assert_array_equal(to_np(w.s_down[e]), ref.s_down)
+    ref = oracle.expert_weights_from_synth(7, "shared", 512, 256)
+    np.testing.assert_array_equal(to_np(w.sh_w_up), ref.w_up)
+
+
+def test_routing_tie_break_on_device():
+    T, H, E, k, I = 4, 512, 8, 3, 256
+    lg = np.zeros((T, E), dtype=np.float32)
+    lg[0] = [1, 2, 2, 2, 0, 0, 0, 0]          # tie among 1, 2, 3
+    lg[1] = [0.5] * 8                          # all equal
+    lg[2] = [-1, 3, 3, -2, 3, 0, 1, 1]
+    lg[3] = np.arange(8)[::-1]
+    x = synth.x_bf16(3, T, H)
+    g = GpuRun(T, H, E, k, I, x_lg=(x, lg)).run()
+    r = oracle.moe_step(x, lg, k, oracle_experts(42, E, H, I))
+    check_routing_bit_exact(g, r)
+    np.testing.assert_array_equal(g.t["topk_ids"][0], [1, 2, 3])
+    check_y(g.y_bits, r["y"])
+    g.close()
+
+
+# ----------------------------------------------------------------- properties
+
+def test_deterministic_and_token_permutation_invariant():
+    T, H, E, k, I = 40, 512, 8, 2, 256
+    g = GpuRun(T, H, E, k, I, "zipf").run()
+    y1 = g.y_bits.copy()
+    g.run()
+    np.testing.assert_array_equal(g.y_bits, y1)             # same input twice -> same bits
+    perm = np.random.default_rng(5).permutation(T)
+    g2 = GpuRun(T, H, E, k, I, weights=g.weights, x_lg=(g.x_bits[perm], g.lg[perm])).run()
+    # each row's arithmetic does not depend on its tile-mates
+    np.testing.assert_array_equal(g2.y_bits, y1[perm])
+    g.close()
+    g2.close()
+
+
+def test_empty_step_and_argument_errors():
+    T, H, E, k, I = 6, 512, 8, 2, 256
+    g = GpuRun(T, H, E, k, I)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream()
+    assert abi.moe_forward(g.step.plan, g.x_dev, g.lg_dev, 0, y, None, None, st) == abi.MOE_OK
+    assert abi.moe_forward(g.step.plan, g.x_dev, g.lg_dev, T + 1, y, None, None, st) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_forward(g.step.plan, g.x_dev, g.lg_dev, -1, y, None, None, st) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_forward(g.step.plan, g.x_dev.data_ptr() + 2, g.lg_dev, T, y, None, None, st) == \
+        abi.MOE_ERR_INVALID_ARG
+    g.run()
+    assert g.status_code == abi.MOE_OK
+    g.close()
+
+
+def test_fewer_rows_than_planned():
+    T, H, E, k, I = 9, 512, 8, 2, 256
+    g = GpuRun(T, H, E, k, I, max_rows=64).run()
+    r = oracle.moe_step(g.x_bits, g.lg, k, oracle_experts(42, E, H, I))
+    check_routing_bit_exact(g, r)
+    check_y(g.y_bits, r["y"])
+    g.close()
+
+
+def test_bounded_wait_timeout_is_reported_and_recoverable():
+    """Host-injected fault: one tile never publishes its ready count. The down
+    units' bounded wait gives up, the step reports MOE_ERR_TIMEOUT, and the GPU
+    stays usable: a normal plan afterwards matches the oracle."""
+    T, H, E, k, I = 6, 512, 8, 2, 256
+    g = GpuRun(T, H, E, k, I, flags=abi.MOE_FLAG_TEST_SKIP_READY, timeout_ns=20_000_000).run()
+    assert g.status_code == abi.MOE_ERR_TIMEOUT
+    g.close()
+    ok = GpuRun(T, H, E, k, I).run()
+    assert ok.status_code == abi.MOE_OK
+    r = oracle.moe_step(ok.x_bits, ok.lg, k, oracle_experts(42, E, H, I))
+    check_y(ok.y_bits, r["y"])
+    ok.close()
+
+
+def test_forward_host_matches_device_forward():
+    T, H, E, k, I = 6, 512, 8, 2, 256
+    g = GpuRun(T, H, E, k, I).run()
+    xh = torch.from_numpy(g.x_bits.view(np.int16).copy()).pin_memory()
+    lh = torch.from_numpy(g.lg.copy()).pin_memory()
+    yh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    assert g.step.forward_host(xh, lh, yh) == abi.MOE_OK
+    np.testing.assert_array_equal(yh.numpy().view(np.uint16), g.y_bits)
+    g.close()
+
+
+def test_timing_flag_records_expert_kernel():
+    T, H, E, k, I = 6, 512, 8, 2, 256
+    g = GpuRun(T, H, E, k, I, flags=abi.MOE_FLAG_TIMING)
+    for _ in range(3):
+        g.run()
+    ms, n = g.step.kernel_times()
+    assert n == 3 and ms > 0
+    g.close()

@@ -134,3 +134,25 @@ def test_placement_popcount_formula_and_invariants():
             for j in range(int(p["tiles"][e]) - 1):                 # all but the last tile are full
                 assert sum(1 for (ee, tt, _) in seen if ee == e and tt == j) == TILE_ROWS
         assert p["bitmap"].shape == (E, words)
+
+
+def test_exp_rn_constants_are_correctly_rounded():
+    """The binary32 constants of exp_rn are the correctly rounded values of
+    log2(e), ln2 - ln2_hi and 1/i!, computed here from 60-digit references."""
+    sympy = __import__("pytest").importorskip("sympy")
+    from fractions import Fraction
+
+    from oracle import routing as R
+
+    def rn32(fr):
+        f = np.float32(float(fr))
+        cands = [np.nextafter(f, np.float32(0)), f, np.nextafter(f, np.float32(np.inf))]
+        return min(cands, key=lambda c: abs(Fraction(float(c)) - fr))
+
+    fact = [1, 1, 2, 6, 24, 120, 720, 5040, 40320]
+    for i, f in enumerate(fact):
+        assert R._INV_FACT[i] == rn32(Fraction(1, f))
+    assert R._LOG2E == rn32(Fraction(str(sympy.N(1 / sympy.log(2), 60))))
+    hi = Fraction(45426, 65536)
+    assert Fraction(float(R._LN2_HI)) == hi
+    assert R._LN2_LO == rn32(Fraction(str(sympy.N(sympy.log(2), 60))) - hi)
