@@ -183,9 +183,11 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
     step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
-    for _ in range(warmup):
+    # one device status word per step: every step must finish with MOE_OK
+    st_words = torch.full((warmup + steps,), -1, dtype=torch.int32, device="cuda")
+    for i in range(warmup):
         flush_buf.zero_()
-        step.forward(x, lg, y=y)
+        step.forward(x, lg, y=y, d_status=st_words[i:i + 1])
     torch.cuda.synchronize()
     step.kernel_times()  # reset the expert-kernel event log
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -193,12 +195,17 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
     for i in range(steps):
         flush_buf.zero_()
         starts[i].record(stream)
-        step.forward(x, lg, y=y)
+        step.forward(x, lg, y=y, d_status=st_words[warmup + i:warmup + i + 1])
         ends[i].record(stream)
     torch.cuda.synchronize()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     expert_ms, launches = step.kernel_times()
-    status = step.status()
+    words = st_words.cpu().tolist()
+    bad = [(i, w) for i, w in enumerate(words) if w != abi.MOE_OK]
+    status = 0 if not bad else bad[0][1]
+    if bad:
+        print(f"warning: {len(bad)} of {len(words)} steps reported a device status: first {bad[0]}, "
+              f"diagnostics {step.diagnostics()}", file=sys.stderr)
     A = active_experts(lg_np, wl.k, wl.shared)
     weight_bytes = A * wl.expert_bytes
     step_bytes = weight_bytes + wl.T * wl.H * 2 + wl.T * wl.E * 4 + wl.T * wl.H * 2
@@ -214,6 +221,7 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
         "weight_bytes": weight_bytes,
         "step_bytes": step_bytes,
         "status": status,
+        "bad_steps": len(bad),
         "step": step,
         "x": x,
         "lg": lg,
@@ -355,6 +363,7 @@ def run_gpu(args):
             "l2": "flushed before every step (memset of a buffer >= 2x L2, outside the timed events)",
             "parallelism": "replicas" if world > 1 else "single GPU",
             "status": main["status"],
+            "steps_with_device_error": main["bad_steps"],
         },
         "roofline": {
             "bound": "hbm",

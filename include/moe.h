@@ -196,6 +196,13 @@ moe_status_t moe_kernel_times(void *plan, double *expert_ms_out, int32_t *launch
  * NULL). Synchronises the plan's device and then reads it. */
 moe_status_t moe_plan_status(void *plan, int32_t *status_out);
 
+/* Diagnostics of the last device-side error on this plan: 8 int64 words
+ *   [0] site: 1 ready-counter wait, 2 pipeline full wait, 3 pipeline empty wait, 4 router
+ *   [1] work unit, [2] tile (or ring stage), [3] value observed, [4] value expected,
+ *   [5] ns waited, [6] SM cycles waited, [7] block index.
+ * All zero when the last step had no device-side error. Synchronises the device. */
+moe_status_t moe_plan_diagnostics(void *plan, int64_t *out8);
+
 /* Teardown: frees the plan's device memory and events, after a device-wide
  * synchronise. NULL is a no-op. */
 moe_status_t moe_destroy(void *plan);

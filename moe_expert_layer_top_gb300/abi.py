@@ -35,6 +35,7 @@ EXPORTED = (
     "moe_quantize_mxfp8",
     "moe_kernel_times",
     "moe_plan_status",
+    "moe_plan_diagnostics",
     "moe_destroy",
 )
 
@@ -104,6 +105,8 @@ def load(path: str | None = None):
     lib.moe_kernel_times.argtypes = [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)]
     lib.moe_plan_status.restype = ctypes.c_int
     lib.moe_plan_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32)]
+    lib.moe_plan_diagnostics.restype = ctypes.c_int
+    lib.moe_plan_diagnostics.argtypes = [_P, ctypes.POINTER(ctypes.c_int64)]
     lib.moe_destroy.restype = ctypes.c_int
     lib.moe_destroy.argtypes = [_P]
     if lib.moe_abi_version() != MOE_ABI_VERSION:
@@ -192,6 +195,13 @@ def moe_plan_status(plan: int) -> int:
     v = ctypes.c_int32()
     check("moe_plan_status", lib.moe_plan_status(plan, ctypes.byref(v)))
     return v.value
+
+
+def moe_plan_diagnostics(plan: int) -> list[int]:
+    lib = load()
+    out = (ctypes.c_int64 * 8)()
+    check("moe_plan_diagnostics", lib.moe_plan_diagnostics(plan, out))
+    return list(out)
 
 
 def moe_destroy(plan: int | None) -> int:

@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
   for (int j = 0; j < a.k; ++j) {
-    const float w = __ldg(a.topk_w + int64_t(t) * a.k + j);
+    const float w = __ldcg(a.topk_w + int64_t(t) * a.k + j);
     const float4 *src = reinterpret_cast<const float4 *>(a.o + (int64_t(t) * a.k + j) * a.H + h0);
     const float4 v0 = __ldcs(src), v1 = __ldcs(src + 1);
     const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};

@@ -22,9 +22,46 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// First device-side error wins; later ones are dropped.
-__device__ __forceinline__ void report_error(int32_t *status, int32_t code) {
-  atomicCAS(status, (int32_t)MOE_OK, code);
+__device__ __forceinline__ uint64_t sm_cycles() { return clock64(); }
+
+// First device-side error wins; later ones are dropped. Returns true for the winner.
+__device__ __forceinline__ bool report_error(int32_t *status, int32_t code) {
+  return atomicCAS(status, (int32_t)MOE_OK, code) == (int32_t)MOE_OK;
+}
+
+// A bounded wait gives up only when both the global timer and the SM cycle
+// counter say the limit has passed. The cycle test assumes at least 1 GHz, so
+// a forward jump of the global timer alone cannot end a wait early. A stalled
+// global timer cannot stretch a wait past 4x the limit in cycles.
+struct WaitClock {
+  uint64_t t0, c0;
+  __device__ __forceinline__ WaitClock() : t0(global_ns()), c0(sm_cycles()) {}
+  __device__ __forceinline__ bool expired(int64_t limit_ns) const {
+    const int64_t dc = (int64_t)(sm_cycles() - c0);
+    const int64_t dt = (int64_t)(global_ns() - t0);
+    return (dt > limit_ns && dc > limit_ns) || dc > 4 * limit_ns;
+  }
+  __device__ __forceinline__ int64_t ns() const { return (int64_t)(global_ns() - t0); }
+  __device__ __forceinline__ int64_t cycles() const { return (int64_t)(sm_cycles() - c0); }
+};
+
+// Diagnostic record of the first device-side error of a step (plan-owned, 8 words):
+// site, unit, tile, observed, expected, elapsed ns, elapsed cycles, block.
+enum DiagSite : int64_t { kDiagReadyWait = 1, kDiagFullWait = 2, kDiagEmptyWait = 3, kDiagRoute = 4 };
+
+__device__ __forceinline__ void report_diag(int32_t *status, int64_t *diag, int32_t code, int64_t site, int64_t unit,
+                                            int64_t tile, int64_t observed, int64_t expected, int64_t ns,
+                                            int64_t cycles) {
+  if (report_error(status, code) && diag) {
+    diag[0] = site;
+    diag[1] = unit;
+    diag[2] = tile;
+    diag[3] = observed;
+    diag[4] = expected;
+    diag[5] = ns;
+    diag[6] = cycles;
+    diag[7] = blockIdx.x;
+  }
 }
 
 // ------------------------------------------------------------------ mbarrier
@@ -63,13 +100,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete. Gives up after
-// timeout_ns and returns false; the caller reports MOE_ERR_TIMEOUT.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int64_t timeout_ns) {
+// timeout_ns (see WaitClock) and returns false; the caller reports MOE_ERR_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int64_t timeout_ns,
+                                         int64_t *waited_ns = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t start = global_ns();
+  const WaitClock wc;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((int64_t)(global_ns() - start) > timeout_ns) return false;
+    if (wc.expired(timeout_ns)) {
+      if (waited_ns) *waited_ns = wc.ns();
+      return false;
+    }
   }
 }
 

@@ -217,10 +217,10 @@ __device__ __forceinline__ Unit decode_unit(const ExpertArgs &a, uint32_t u, int
     r.tile = int(v / S::NBD);
     r.block = int(v % S::NBD);
   }
-  const int32_t te = __ldg(a.tile_list + r.tile);
+  const int32_t te = __ldcg(a.tile_list + r.tile);
   r.expert = te >> 16;
   r.tile_in = te & 0xFFFF;
-  const int cnt = __ldg(a.counts + r.expert);
+  const int cnt = __ldcg(a.counts + r.expert);
   const int n = cnt - kTileRows * r.tile_in;
   r.n = n < kTileRows ? n : kTileRows;
   return r;
@@ -242,8 +242,9 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     uint32_t u = atomicAdd(a.work, 1u);
     if (ld_volatile(a.work + 1) != 0) u = total;  // abort: stop claiming
     if (u >= total) {
-      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns)) {
-        report_error(a.status, MOE_ERR_TIMEOUT);
+      int64_t waited = 0;
+      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns, &waited)) {
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagEmptyWait, u, stage, phase, -1, waited, 0);
         return;
       }
       sm.meta_unit[stage] = kDone;
@@ -256,11 +257,12 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     const int e = sh ? 0 : un.expert;
     // Weights of a single-tile expert are read once per step: evict first.
     // A multi-tile expert's weights are read once per tile: keep them in L2.
-    const uint64_t pol_u = __ldg(a.counts + un.expert) > kTileRows ? pol_reuse : pol;
+    const uint64_t pol_u = __ldcg(a.counts + un.expert) > kTileRows ? pol_reuse : pol;
     const int steps = un.down ? S::SPU_D : S::SPU_G;
     for (int s = 0; s < steps; ++s) {
-      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns)) {
-        report_error(a.status, MOE_ERR_TIMEOUT);
+      int64_t waited = 0;
+      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns, &waited)) {
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagEmptyWait, u, stage, phase, s, waited, 0);
         atomicExch(a.work + 1, 1u);
         return;
       }
@@ -369,8 +371,9 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
   int np = 1, passes = 1;
   bool skip = false;
   while (true) {
-    if (!mbar_wait(&sm.full[stage], phase, 16 * a.timeout_ns)) {
-      report_error(a.status, MOE_ERR_TIMEOUT);
+    int64_t waited = 0;
+    if (!mbar_wait(&sm.full[stage], phase, 16 * a.timeout_ns, &waited)) {
+      report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, -1, stage, phase, -1, waited, 0);
       atomicExch(a.work + 1, 1u);
       return;
     }
@@ -385,15 +388,17 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
       const int c = tid % (kcols / 16);
       const int64_t rbase = int64_t(un.expert) * a.Tmax + int64_t(un.tile_in) * kTileRows;
 #pragma unroll
-      for (int r = 0; r < kTileRows; ++r) pairs[r] = r < un.n ? __ldg(a.rows_of + rbase + r) : 0;
+      for (int r = 0; r < kTileRows; ++r) pairs[r] = r < un.n ? __ldcg(a.rows_of + rbase + r) : 0;
       skip = false;
       if (un.down) {
         if (tid == 0) {
           int32_t ab = 0;
-          const uint64_t t0 = global_ns();
-          while (ld_acquire_gpu(a.ready + un.tile) < uint32_t(S::NBG)) {
-            if ((int64_t)(global_ns() - t0) > a.timeout_ns) {
-              report_error(a.status, MOE_ERR_TIMEOUT);
+          const WaitClock wc;
+          uint32_t seen;
+          while ((seen = ld_acquire_gpu(a.ready + un.tile)) < uint32_t(S::NBG)) {
+            if (wc.expired(a.timeout_ns)) {
+              report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagReadyWait, u, un.tile, seen, S::NBG, wc.ns(),
+                          wc.cycles());
               atomicExch(a.work + 1, 1u);
               ab = 1;
               break;
@@ -418,8 +423,8 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
         for (int r = 0; r < kTileRows; ++r) {
           if (r < un.n) {
             const int64_t tok = un.expert == a.E ? int64_t(pairs[r]) - int64_t(a.T) * a.k : int64_t(pairs[r] / a.k);
-            x.raw[r] = __ldg(reinterpret_cast<const uint4 *>(a.xq + tok * S::H) + c);
-            x.sc[r] = __ldg(a.xs + tok * (S::H / kGroup) + (c >> 1));
+            x.raw[r] = __ldcg(reinterpret_cast<const uint4 *>(a.xq + tok * S::H) + c);
+            x.sc[r] = __ldcg(a.xs + tok * (S::H / kGroup) + (c >> 1));
           }
         }
       }
@@ -502,7 +507,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
   __syncthreads();
   // Everything below reads the router's outputs.
   pdl_wait_primary();
-  const int n_tiles = __ldg(a.n_tiles);
+  const int n_tiles = __ldcg(a.n_tiles);
   if (warp == kConsumerWarps) {
     if ((threadIdx.x & 31) == 0) producer<S>(a, sm, n_tiles);
     return;

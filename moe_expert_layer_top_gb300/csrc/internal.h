@@ -31,6 +31,7 @@ struct Scratch {
   uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile
   uint32_t *work;       // [2] unit counter, abort flag
   int32_t *status;      // [1] plan-owned status word
+  int64_t *diag;        // [8] first device-side error of the last step (site, unit, tile, ...)
   uint8_t *xq, *xs;     // [Tmax][H], [Tmax][H/32]
   uint8_t *hq, *hs;     // [P][I], [P][I/32]
   uint16_t *h_bf16;     // [P][I]
@@ -76,6 +77,7 @@ struct RouteArgs {
   int n_tiles_max;
   uint32_t *work;
   int32_t *status;
+  int64_t *diag;
   uint8_t *xq, *xs;
 };
 
@@ -94,6 +96,7 @@ struct ExpertArgs {
   uint32_t *ready;
   uint32_t *work;
   int32_t *status;
+  int64_t *diag;
   int64_t timeout_ns;
   int skip_ready_tile;  // fault injection: tile index whose ready count is never published, or -1
 };

@@ -184,6 +184,7 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   const size_t o_slot = take(pairs_routed * 4), o_rows = take(size_t(E + 1) * Tm * 4);
   const size_t o_tl = take(size_t(p->n_tiles_max) * 4), o_nt = take(4);
   const size_t o_ready = take(size_t(p->n_tiles_max) * 4), o_work = take(8), o_status = take(4);
+  const size_t o_diag = take(8 * 8);
   const size_t o_xq = take(size_t(Tm) * H), o_xs = take(size_t(Tm) * (H / 32));
   const size_t o_hq = take(size_t(p->pairs_max) * I), o_hs = take(size_t(p->pairs_max) * (I / 32));
   const size_t o_hb = take(size_t(p->pairs_max) * I * 2), o_o = take(size_t(p->pairs_max) * H * 4);
@@ -207,6 +208,7 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   s.ready = reinterpret_cast<uint32_t *>(base + o_ready);
   s.work = reinterpret_cast<uint32_t *>(base + o_work);
   s.status = reinterpret_cast<int32_t *>(base + o_status);
+  s.diag = reinterpret_cast<int64_t *>(base + o_diag);
   s.xq = base + o_xq;
   s.xs = base + o_xs;
   s.hq = base + o_hq;
@@ -280,6 +282,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ra.n_tiles_max = p->n_tiles_max;
   ra.work = s.work;
   ra.status = status;
+  ra.diag = s.diag;
   ra.xq = s.xq;
   ra.xs = s.xs;
   if (launch_route(ra, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -316,6 +319,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ea.ready = s.ready;
   ea.work = s.work;
   ea.status = status;
+  ea.diag = s.diag;
   ea.timeout_ns = p->timeout_ns;
   ea.skip_ready_tile = (c.flags & MOE_FLAG_TEST_SKIP_READY) ? 0 : -1;
   const bool timed = (c.flags & MOE_FLAG_TIMING) && p->timed_calls < kMaxTimedCalls;
@@ -398,6 +402,15 @@ moe_status_t moe_plan_status(void *plan, int32_t *status_out) {
   int32_t v = 0;
   if (cudaMemcpy(&v, p->s.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   *status_out = v;
+  return MOE_OK;
+}
+
+moe_status_t moe_plan_diagnostics(void *plan, int64_t *out8) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p || !out8) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(p->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(out8, p->s.diag, 8 * sizeof(int64_t), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

@@ -92,6 +92,7 @@ __device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, k = a.k, T = a.T, W = a.words;
 
+  if (tid < 8) a.diag[tid] = 0;
   if (tid == 0) {
     *a.status = MOE_OK;  // start of the step
     a.work[0] = 0;       // unit counter

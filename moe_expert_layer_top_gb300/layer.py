@@ -85,6 +85,9 @@ class MoEStep:
     def status(self) -> int:
         return abi.moe_plan_status(self.plan)
 
+    def diagnostics(self) -> list[int]:
+        return abi.moe_plan_diagnostics(self.plan)
+
     def close(self):
         if self.plan:
             abi.moe_destroy(self.plan)

@@ -69,6 +69,7 @@ class GpuRun:
         self.y_bits = bf16_dev_to_bits(y)
         self.t = {n: to_np(v) for n, v in self.taps.items()}
         self.status_code = int(self.status.item())
+        self.diag = self.step.diagnostics() if self.status_code != abi.MOE_OK else None
         return self
 
     def close(self):

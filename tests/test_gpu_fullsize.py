@@ -47,7 +47,7 @@ def test_fullsize_parity(name, weights):
     wl = synth.WORKLOADS[name]
     w = weights if wl.shared else routed_only(weights)
     g = GpuRun(wl.T, wl.H, wl.E, wl.k, wl.I, wl.routing, wl.shared, seed=SEED, weights=w).run()
-    assert g.status_code == abi.MOE_OK
+    assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     # sampled rows: the first and the last token row
     rows = [0, wl.T - 1]
     get = oracle_experts(SEED, wl.E, wl.H, wl.I, _CACHE)

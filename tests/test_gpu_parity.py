@@ -98,7 +98,7 @@ SMALL = [
 def test_small_case_parity(case):
     T, H, E, k, I, routing, shared = case
     g = GpuRun(T, H, E, k, I, routing, shared, seed=42 + T).run()
-    assert g.status_code == abi.MOE_OK
+    assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     get = oracle_experts(42 + T, E, H, I)
     sh = oracle.expert_weights_from_synth(42 + T, "shared", H, I) if shared else None
     r = oracle.moe_step(g.x_bits, g.lg, k, get, shared=sh)
@@ -167,7 +167,7 @@ def test_empty_step_and_argument_errors():
     assert abi.moe_forward(g.step.plan, g.x_dev.data_ptr() + 2, g.lg_dev, T, y, None, None, st) == \
         abi.MOE_ERR_INVALID_ARG
     g.run()
-    assert g.status_code == abi.MOE_OK
+    assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     g.close()
 
 
