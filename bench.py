@@ -265,6 +265,10 @@ def run_gpu(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     seed = synth.BASE_SEED
     wl = synth.WORKLOADS[args.workload]
+    if args.experts:
+        import dataclasses
+        wl = dataclasses.replace(wl, E=args.experts, name=f"{wl.name}-E{args.experts}")
+        args.no_cpu_baseline = args.no_others = True
 
     # The oracle's worker pool is spawned before the first GPU call.
     cpu_q = None
@@ -272,7 +276,7 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ctx = mp.get_context("spawn")
         cpu_q = ctx.Queue()
-        cpu_proc = ctx.Process(target=oracle_baseline, args=(seed, wl.name, 3, 1, cpu_q))
+        cpu_proc = ctx.Process(target=oracle_baseline, args=(seed, args.workload, 3, 1, cpu_q))
         cpu_proc.start()
 
     _build.build()
@@ -305,7 +309,7 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, exp_ms = float(t[0]), float(t[1])
 
-    e2e = time_e2e(main["step"], wl, seed, max(args.steps, 10), 3)
+    e2e = None if args.no_e2e else time_e2e(main["step"], wl, seed, max(args.steps, 10), 3)
 
     also = {}
     if not args.no_others and world == 1:
@@ -435,6 +439,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=["tiny", "bs1", "bs4", "bs16", "bs64"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="smaller expert count for profiling captures (default: the workload's E)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
