@@ -24,20 +24,22 @@
 // - Same page, 3.1: SwiGLU with the original intermediate rounding. g and u are
 //   rounded to bf16, and h = bf16(silu(g) * u) is then quantised.
 //
-// Block layout: 8 compute warps + 1 producer warp. The producer's elected lane
-// streams the unit's weight rows with bulk copies (TMA, no tensor map, no
+// Block layout: 16 compute warps + 1 producer warp. The producer's elected
+// lane streams the unit's weight rows with bulk copies (TMA, no tensor map, no
 // multicast) into a 5-stage ring of 32 KB + scales.
 //
-// Each compute thread owns 16 consecutive K columns of every row in a stage:
-//  - K/16 threads cover a row, and 256/(K/16) row groups split the stage's rows;
-//  - it keeps its 16 columns of the tile's token rows in registers as fp32
-//    (dequantised once per unit);
-//  - per row it reads 16 weight bytes (one 16-byte shared load) and its
-//    group's scale, decodes E4M3 to fp32, and accumulates with packed FFMA2.
-// A transposing butterfly reduces 8 rows x NP tokens across the lanes, and a
-// fixed-order sum reduces across warps. Every output goes through the same
-// addition tree whatever the tile's row count, so results do not depend on
-// tile-mates.
+// Each compute thread owns 16 consecutive K columns of 4 rows of every stage:
+//  - K/16 threads cover a row, and 512/(K/16) row groups split the stage's rows;
+//  - per row it reads 16 weight bytes (one 16-byte shared load) and the
+//    group's scale, decodes E4M3 to fp32, and accumulates with packed FFMA2
+//    against its 16 columns of the token rows (fp32 registers, 2 tokens per
+//    pass).
+// A transposing butterfly reduces 4 rows x NP tokens across the lanes. Each
+// warp then posts its partial sums to shared memory and arrives on the stage's
+// reduction barrier. One warp per stage, rotating, sums the partials across
+// warps in a fixed order and writes the outputs. No block-wide barrier runs
+// in steady state. Every output goes through the same addition tree
+// whatever the tile's row count, so results do not depend on tile-mates.
 #include <stdint.h>
 
 #include "device.cuh"
@@ -48,20 +50,23 @@ namespace moe {
 namespace {
 
 constexpr uint32_t kDone = 0xFFFFFFFFu;
-constexpr int kConsumers = kConsumerWarps * 32;  // 256
+constexpr int kConsumers = kConsumerWarps * 32;   // 512
 constexpr int kStageScaleBytes = kStageBytes / kGroup;
 constexpr int kStageStride = kStageBytes + kStageScaleBytes;
-constexpr int kMaxSlots = 16;  // reduction slots (K = 256 uses half-warps)
+constexpr int kMaxSlots = kConsumers / 16;        // reduction slots (K = 256 uses half-warps)
+constexpr int kRedValues = 32;                    // per slot: passes x 4 rows x NP tokens
+constexpr int kUnitSlots = 8;                     // gate/up units in flight per block
 
 struct __align__(16) ExpertSmem {
   unsigned char stage[kStages][kStageStride];
-  float red[2][2][kMaxSlots][32];       // [stage parity][pass][slot][value]
-  float gu[kTileRows][2][32];           // gate/up results of the unit, [token][gate|up][i]
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  float red[kStages][kMaxSlots][kRedValues];      // per-warp partial sums of a stage
+  float gu[kUnitSlots][kTileRows][2][32];         // gate/up results of a unit, [token][gate|up][i]
+  uint64_t full[kStages];                         // weights landed (producer arrive + tx bytes)
+  uint64_t empty[kStages];                        // stage free again (16 consumer warps)
+  uint64_t red_full[kStages];                     // partial sums posted (16 consumer warps)
   uint32_t meta_unit[kStages];
   uint32_t meta_step[kStages];
-  int32_t abort_unit;
+  uint32_t unit_done[kUnitSlots];                 // stages of a gate/up unit already reduced
 };
 
 template <int KG, int KD>
@@ -80,12 +85,22 @@ struct Shape {
   static_assert(H % DB == 0, "down units tile H");
 };
 
+// Row geometry of a stage for a K-wide weight matrix and 512 compute threads.
+template <int K>
+struct Rows {
+  static constexpr int TPR = K / 16;                 // threads per row
+  static constexpr int RG = kConsumers / TPR;        // row groups
+  static constexpr int RS = kStageBytes / K;         // rows per stage
+  static constexpr int PER_THREAD = RS / RG;         // rows per thread per stage (4)
+  static constexpr int LANES = TPR < 32 ? TPR : 32;  // lanes of a row group inside one warp
+  static constexpr int SPG = TPR / LANES;            // reduction slots per row group
+  static_assert(PER_THREAD == 4, "4 rows per thread per stage");
+};
+
 // ------------------------------------------------------------------ per-thread math
 
 struct XRegs {
-  uint4 raw[kTileRows];     // 16 E4M3 codes per token row (this thread's columns)
-  uint32_t sc[kTileRows];   // UE8M0 code of the group holding these columns
-  float2 f[4][8];           // dequantised pass tokens, 16 values as 8 pairs
+  float2 f[2][8];           // the pass's tokens, dequantised: 16 values as 8 pairs each
 };
 
 __device__ __forceinline__ void decode16(const uint4 v, float2 (&o)[8]) {
@@ -97,19 +112,20 @@ __device__ __forceinline__ void decode16(const uint4 v, float2 (&o)[8]) {
   }
 }
 
-// x (or h) for tokens [4*pass, 4*pass + 4) into fp32 registers, with their scales applied.
-template <int NP>
-__device__ __forceinline__ void load_pass(XRegs &x, int pass, int n) {
+// Tokens [NP*pass, NP*pass + NP) of the tile into fp32 registers, scales applied.
+// row_q(tok) / row_s(tok) give the thread's 16 E4M3 codes and the group's scale
+// code of a tile row. They are read through L2: an earlier grid or block wrote them.
+template <int NP, class FQ, class FS>
+__device__ __forceinline__ void load_pass(XRegs &x, int pass, int n, FQ &&row_q, FS &&row_s) {
 #pragma unroll
   for (int t = 0; t < NP; ++t) {
-    const int tok = 4 * pass + t;
+    const int tok = NP * pass + t;
     float2 v[8];
     if (tok < n) {
-      // static register indices only (pass is 0 or 1)
-      decode16(pass ? x.raw[(4 + t) & 7] : x.raw[t], v);
-      const float s = ue8m0_to_float(pass ? x.sc[(4 + t) & 7] : x.sc[t]);
+      decode16(__ldcg(reinterpret_cast<const uint4 *>(row_q(tok))), v);
+      const float sc = ue8m0_to_float(__ldcg(row_s(tok)));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = make_float2(v[i].x * s, v[i].y * s);
+      for (int i = 0; i < 8; ++i) v[i] = make_float2(v[i].x * sc, v[i].y * sc);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = make_float2(0.f, 0.f);
@@ -119,26 +135,29 @@ __device__ __forceinline__ void load_pass(XRegs &x, int pass, int n) {
   }
 }
 
-// This thread's partial dot products for its 8 rows of the stage and NP tokens.
+// This thread's partial dot products for its 4 rows of the stage and NP tokens.
 template <int K, int NP>
 __device__ __forceinline__ void stage_dot(const unsigned char *st, int g, int c, const XRegs &x,
-                                          float (&acc)[8 * NP]) {
-  constexpr int RG = 256 / (K / 16);
+                                          float (&acc)[4 * NP]) {
+  using R = Rows<K>;
   const unsigned char *sw = st;
   const unsigned char *ss = st + kStageBytes;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int r = g + RG * j;
+  for (int j = 0; j < 4; ++j) {
+    const int r = g + R::RG * j;
     const uint4 wv = *reinterpret_cast<const uint4 *>(sw + r * K + 16 * c);
     const float ws = ue8m0_to_float(ss[r * (K / kGroup) + (c >> 1)]);
     float2 w[8];
     decode16(wv, w);
 #pragma unroll
     for (int t = 0; t < NP; ++t) {
-      float2 a = make_float2(0.f, 0.f);
+      float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a = __ffma2_rn(w[i], x.f[t][i], a);
-      acc[j * NP + t] = ws * (a.x + a.y);
+      for (int i = 0; i < 8; i += 2) {
+        a0 = __ffma2_rn(w[i], x.f[t][i], a0);
+        a1 = __ffma2_rn(w[i + 1], x.f[t][i + 1], a1);
+      }
+      acc[j * NP + t] = ws * ((a0.x + a1.x) + (a0.y + a1.y));
     }
   }
 }
@@ -149,7 +168,7 @@ __device__ __forceinline__ void stage_dot(const unsigned char *st, int g, int c,
 // The additions follow the same tree (offsets LANES/2 ... 1) for every V.
 template <int V, int LANES>
 struct Butterfly {
-  static constexpr int LOGV = V == 8 ? 3 : V == 16 ? 4 : 5;
+  static constexpr int LOGV = V == 4 ? 2 : V == 8 ? 3 : V == 16 ? 4 : 5;
   static constexpr int LOGL = LANES == 32 ? 5 : 4;
   static constexpr int HSTEPS = LOGV < LOGL ? LOGV : LOGL;
   static constexpr int CNT = V >> HSTEPS;
@@ -189,8 +208,6 @@ __device__ __forceinline__ int32_t pick8(const int32_t (&v)[kTileRows], int i) {
   for (int j = 1; j < kTileRows; ++j) r = (i == j) ? v[j] : r;
   return r;
 }
-
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
 // ------------------------------------------------------------------ unit decoding
 
@@ -300,74 +317,102 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
 
 // ------------------------------------------------------------------ consumers
 
-// Process one stage's rows for one pass of NP tokens: dot products, warp
-// reduction, and write the per-slot partial sums to red[par][pass].
+// One pass (NP tokens) over this thread's 4 rows of the stage: dot products,
+// warp reduction, and the per-slot partial sums into red[stage].
 template <int K, int NP>
-__device__ __forceinline__ void stage_pass(ExpertSmem &sm, const unsigned char *st, int par, int pass,
+__device__ __forceinline__ void stage_pass(ExpertSmem &sm, const unsigned char *st, int stage, int pass,
                                            const XRegs &x) {
-  constexpr int TPR = K / 16;
-  constexpr int LANES = TPR < 32 ? TPR : 32;
-  constexpr int V = 8 * NP;
-  using BF = Butterfly<V, LANES>;
+  using R = Rows<K>;
+  constexpr int V = 4 * NP;
+  using BF = Butterfly<V, R::LANES>;
   const int tid = threadIdx.x;
-  const int g = tid / TPR, c = tid % TPR;
-  const int l = tid & (LANES - 1);
-  const int slot = tid / LANES;
+  const int g = tid / R::TPR, c = tid % R::TPR;
+  const int l = tid & (R::LANES - 1);
+  const int slot = tid / R::LANES;
   float acc[V];
   stage_dot<K, NP>(st, g, c, x, acc);
   BF::run(acc, l);
   if ((l & BF::TAILMASK) == 0) {
 #pragma unroll
-    for (int i = 0; i < BF::CNT; ++i) sm.red[par][pass][slot][BF::index(l, i)] = acc[i];
+    for (int i = 0; i < BF::CNT; ++i) sm.red[stage][slot][pass * V + BF::index(l, i)] = acc[i];
   }
 }
 
-template <int K>
-__device__ __forceinline__ void stage_pass_any(ExpertSmem &sm, const unsigned char *st, int par, int pass, int np,
-                                               const XRegs &x) {
-  if (np == 1) stage_pass<K, 1>(sm, st, par, pass, x);
-  else if (np == 2) stage_pass<K, 2>(sm, st, par, pass, x);
-  else stage_pass<K, 4>(sm, st, par, pass, x);
-}
-
-__device__ __forceinline__ void load_pass_any(XRegs &x, int pass, int np, int n) {
-  if (np == 1) load_pass<1>(x, pass, n);
-  else if (np == 2) load_pass<2>(x, pass, n);
-  else load_pass<4>(x, pass, n);
-}
-
-// Final cross-slot sums of one stage. Calls out(row_in_stage, token, value).
+// The rotating reducer: sums one stage's partials across the warps of each
+// row group, in slot order. Calls out(row_in_stage, token, value).
 template <int K, class F>
-__device__ __forceinline__ void stage_outputs(const ExpertSmem &sm, int par, int passes, int np, int n, F &&out) {
-  constexpr int TPR = K / 16;
-  constexpr int LANES = TPR < 32 ? TPR : 32;
-  constexpr int SPG = TPR / LANES;  // slots per row group
-  constexpr int RG = 256 / TPR;
-  const int per_pass = RG * 8 * np;
-  for (int o = threadIdx.x; o < passes * per_pass; o += kConsumers) {
+__device__ __forceinline__ void reduce_stage(const ExpertSmem &sm, int stage, int passes, int np, int n, int lane,
+                                             F &&out) {
+  using R = Rows<K>;
+  const int V = 4 * np;
+  const int per_pass = R::RG * V;
+  for (int o = lane; o < passes * per_pass; o += 32) {
     const int pass = o / per_pass;
     const int q = o % per_pass;
-    const int g = q / (8 * np);
-    const int v = q % (8 * np);
+    const int g = q / V;
+    const int v = q % V;
     const int j = v / np, t = v % np;
-    const int tok = 4 * pass + t;
+    const int tok = np * pass + t;
     if (tok >= n) continue;
-    float s = sm.red[par][pass][g * SPG][v];
+    const int idx = pass * V + v;
+    float s = sm.red[stage][g * R::SPG][idx];
 #pragma unroll
-    for (int k = 1; k < SPG; ++k) s += sm.red[par][pass][g * SPG + k][v];
-    out(g + RG * j, tok, s);
+    for (int k = 1; k < R::SPG; ++k) s += sm.red[stage][g * R::SPG + k][idx];
+    out(g + R::RG * j, tok, s);
   }
+}
+
+// gate/up epilogue, one warp: h = bf16(silu(bf16 g) * bf16 u), MXFP8 along I; then publish.
+template <class S>
+__device__ __forceinline__ void gate_up_epilogue(const ExpertArgs &a, ExpertSmem &sm, int uslot, const Unit &un,
+                                                 const int32_t (&pairs)[kTileRows], int lane) {
+  for (int t = 0; t < un.n; ++t) {
+    const float gb = bf16_bits_to_float(float_to_bf16_bits(sm.gu[uslot][t][0][lane]));
+    const float ub = bf16_bits_to_float(float_to_bf16_bits(sm.gu[uslot][t][1][lane]));
+    const float silu = gb / (1.0f + expf(-gb));
+    const uint16_t hb = float_to_bf16_bits(silu * ub);
+    const float hv = bf16_bits_to_float(hb);
+    float amax = fabsf(hv);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const uint32_t code = mx_scale_code(amax);
+    const int64_t p = pick8(pairs, t);
+    a.hq[p * S::I + int64_t(un.block) * 32 + lane] = float_to_e4m3(mx_unscale(hv, code));
+    if (lane == 0) a.hs[p * (S::I / kGroup) + un.block] = uint8_t(code);
+    if (a.h_bf16) a.h_bf16[p * S::I + int64_t(un.block) * 32 + lane] = hb;
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) {
+    if (un.tile != a.skip_ready_tile) red_release_gpu_add(a.ready + un.tile, 1u);
+    sm.unit_done[uslot] = 0;
+  }
+  __syncwarp();
 }
 
 template <class S>
 __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int stage = 0;
-  uint32_t phase = 0;  // full-barrier parity; flips each time the ring wraps
-  int par = 0;
+  uint32_t phase = 0;   // barrier parity of the current ring pass
+  uint32_t seq = 0;     // stages processed by this block: the reducer of stage seq is warp seq % 16
+  int uslot = -1;       // unit sequence number mod kUnitSlots
   Unit un{};
   int32_t pairs[kTileRows];
   XRegs x;
+  // this thread's columns of tile row `tok`: h rows (down) or x rows (gate/up)
+  auto row_q = [&](int tok) -> const uint8_t * {
+    const int64_t p = pick8(pairs, tok);
+    if (un.down) return a.hq + p * S::I + 16 * (tid % (S::I / 16));
+    const int64_t t = un.expert == a.E ? p - int64_t(a.T) * a.k : p / a.k;
+    return a.xq + t * S::H + 16 * (tid % (S::H / 16));
+  };
+  auto row_s = [&](int tok) -> const uint8_t * {
+    const int64_t p = pick8(pairs, tok);
+    if (un.down) return a.hs + p * (S::I / kGroup) + ((tid % (S::I / 16)) >> 1);
+    const int64_t t = un.expert == a.E ? p - int64_t(a.T) * a.k : p / a.k;
+    return a.xs + t * (S::H / kGroup) + ((tid % (S::H / 16)) >> 1);
+  };
   int np = 1, passes = 1;
   bool skip = false;
   while (true) {
@@ -382,17 +427,17 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     if (u == kDone) return;
     const unsigned char *st = sm.stage[stage];
     if (s == 0) {
-      // ---- unit start: rows of the tile, and their x (or h) columns in registers
+      // ---- unit start: rows of the tile, and this thread's x (or h) columns in registers
       un = decode_unit<S>(a, u, n_tiles);
-      const int kcols = un.down ? S::I : S::H;
-      const int c = tid % (kcols / 16);
+      uslot = (uslot + 1) & (kUnitSlots - 1);
       const int64_t rbase = int64_t(un.expert) * a.Tmax + int64_t(un.tile_in) * kTileRows;
 #pragma unroll
-      for (int r = 0; r < kTileRows; ++r) pairs[r] = r < un.n ? __ldcg(a.rows_of + rbase + r) : 0;
+      for (int r = 0; r < kTileRows; ++r) pairs[r] = r < un.n ? __ldcg(a.rows_of + rbase + r) : pairs[0];
       skip = false;
       if (un.down) {
-        if (tid == 0) {
-          int32_t ab = 0;
+        // h of this tile must be complete: bounded wait on the tile's ready count (one lane per warp)
+        int ab = 0;
+        if (lane == 0) {
           const WaitClock wc;
           uint32_t seen;
           while ((seen = ld_acquire_gpu(a.ready + un.tile)) < uint32_t(S::NBG)) {
@@ -405,89 +450,73 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
             }
             __nanosleep(64);
           }
-          sm.abort_unit = ab;
         }
-        consumer_sync();
-        skip = sm.abort_unit != 0;
-        if (!skip) {
-#pragma unroll
-          for (int r = 0; r < kTileRows; ++r) {
-            if (r < un.n) {
-              x.raw[r] = __ldcg(reinterpret_cast<const uint4 *>(a.hq + int64_t(pairs[r]) * S::I) + c);
-              x.sc[r] = __ldcg(a.hs + int64_t(pairs[r]) * (S::I / kGroup) + (c >> 1));
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < kTileRows; ++r) {
-          if (r < un.n) {
-            const int64_t tok = un.expert == a.E ? int64_t(pairs[r]) - int64_t(a.T) * a.k : int64_t(pairs[r] / a.k);
-            x.raw[r] = __ldcg(reinterpret_cast<const uint4 *>(a.xq + tok * S::H) + c);
-            x.sc[r] = __ldcg(a.xs + tok * (S::H / kGroup) + (c >> 1));
-          }
-        }
+        skip = __shfl_sync(0xFFFFFFFFu, ab, 0) != 0;
       }
-      np = un.n <= 1 ? 1 : un.n <= 2 ? 2 : 4;
-      passes = un.n > 4 ? 2 : 1;
-      if (passes == 1) load_pass_any(x, 0, np, un.n);
+      np = un.n <= 1 ? 1 : 2;
+      passes = (un.n + np - 1) / np;
+      if (passes == 1 && !skip) {
+        if (np == 1) load_pass<1>(x, 0, un.n, row_q, row_s);
+        else load_pass<2>(x, 0, un.n, row_q, row_s);
+      }
     }
-    // ---- this stage: dot products and warp reductions
+    // ---- this stage: dot products and warp reductions, posted to red[stage]
     if (!skip) {
       for (int p = 0; p < passes; ++p) {
-        if (passes > 1) load_pass_any(x, p, np, un.n);
-        if (un.down) stage_pass_any<S::I>(sm, st, par, p, np, x);
-        else stage_pass_any<S::H>(sm, st, par, p, np, x);
+        if (np == 1) {
+          if (un.down) stage_pass<S::I, 1>(sm, st, stage, p, x);
+          else stage_pass<S::H, 1>(sm, st, stage, p, x);
+        } else {
+          if (passes > 1) load_pass<2>(x, p, un.n, row_q, row_s);
+          if (un.down) stage_pass<S::I, 2>(sm, st, stage, p, x);
+          else stage_pass<S::H, 2>(sm, st, stage, p, x);
+        }
       }
     }
     __syncwarp();
-    if ((tid & 31) == 0) mbar_arrive(&sm.empty[stage]);
-    consumer_sync();
-    // ---- cross-warp sums and outputs
-    if (!skip) {
-      if (un.down) {
-        const int64_t hrow0 = int64_t(un.block) * S::DB + int64_t(s) * S::RS_D;
-        stage_outputs<S::I>(sm, par, passes, np, un.n, [&](int r, int tok, float v) {
-          a.o[int64_t(pick8(pairs, tok)) * S::H + hrow0 + r] = v;
-        });
-      } else {
-        constexpr int HALF = S::RS_G / 2;
-        stage_outputs<S::H>(sm, par, passes, np, un.n, [&](int r, int tok, float v) {
-          const int which = r < HALF ? 0 : 1;
-          const int i = s * HALF + (r < HALF ? r : r - HALF);
-          sm.gu[tok][which][i] = v;
-        });
-      }
+    const bool reducer = int(seq % kConsumerWarps) == warp;
+    if (lane == 0) {
+      mbar_arrive(&sm.red_full[stage]);
+      if (!reducer) mbar_arrive(&sm.empty[stage]);
     }
-    const bool last = s == (un.down ? S::SPU_D : S::SPU_G) - 1;
-    if (last && !un.down && !skip) {
-      // ---- gate/up epilogue: h = bf16(silu(bf16 g) * bf16 u), MXFP8 along I
-      consumer_sync();
-      const int w = tid >> 5, lane = tid & 31;
-      if (w < un.n) {
-        const float gb = bf16_bits_to_float(float_to_bf16_bits(sm.gu[w][0][lane]));
-        const float ub = bf16_bits_to_float(float_to_bf16_bits(sm.gu[w][1][lane]));
-        const float silu = gb / (1.0f + expf(-gb));
-        const uint16_t hb = float_to_bf16_bits(silu * ub);
-        const float hv = bf16_bits_to_float(hb);
-        float amax = fabsf(hv);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-        const uint32_t code = mx_scale_code(amax);
-        const int64_t p = pick8(pairs, w);
-        a.hq[p * S::I + int64_t(un.block) * 32 + lane] = float_to_e4m3(mx_unscale(hv, code));
-        if (lane == 0) a.hs[p * (S::I / kGroup) + un.block] = uint8_t(code);
-        if (a.h_bf16) a.h_bf16[p * S::I + int64_t(un.block) * 32 + lane] = hb;
-        __threadfence();
+    if (reducer) {
+      // ---- cross-warp sums of this stage, then outputs
+      if (!mbar_wait(&sm.red_full[stage], phase, 16 * a.timeout_ns, &waited)) {
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, u, stage, phase, -2, waited, 0);
+        atomicExch(a.work + 1, 1u);
+      } else if (!skip) {
+        if (un.down) {
+          const int64_t hrow0 = int64_t(un.block) * S::DB + int64_t(s) * S::RS_D;
+          reduce_stage<S::I>(sm, stage, passes, np, un.n, lane, [&](int r, int tok, float v) {
+            a.o[int64_t(pick8(pairs, tok)) * S::H + hrow0 + r] = v;
+          });
+        } else {
+          constexpr int HALF = S::RS_G / 2;
+          reduce_stage<S::H>(sm, stage, passes, np, un.n, lane, [&](int r, int tok, float v) {
+            const int which = r < HALF ? 0 : 1;
+            const int i = s * HALF + (r < HALF ? r : r - HALF);
+            sm.gu[uslot][tok][which][i] = v;
+          });
+          // the warp that reduces the unit's last outstanding stage runs the epilogue
+          __threadfence_block();
+          __syncwarp();
+          uint32_t before = 0;
+          if (lane == 0) before = atomicAdd(&sm.unit_done[uslot], 1u);
+          before = __shfl_sync(0xFFFFFFFFu, before, 0);
+          if (before == uint32_t(S::SPU_G - 1)) {
+            __threadfence_block();
+            gate_up_epilogue<S>(a, sm, uslot, un, pairs, lane);
+          }
+        }
       }
-      consumer_sync();
-      if (tid == 0 && un.tile != a.skip_ready_tile) red_release_gpu_add(a.ready + un.tile, 1u);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[stage]);
     }
+    ++seq;
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1u;
     }
-    par ^= 1;
   }
 }
 
@@ -501,7 +530,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], kConsumerWarps);
+      mbar_init(&sm.red_full[i], kConsumerWarps);
     }
+    for (int i = 0; i < kUnitSlots; ++i) sm.unit_done[i] = 0;
     fence_mbar_init();
   }
   __syncthreads();
