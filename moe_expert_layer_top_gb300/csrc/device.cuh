@@ -103,7 +103,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // timeout_ns (see WaitClock) and returns false; the caller reports MOE_ERR_TIMEOUT.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int64_t timeout_ns,
                                          int64_t *waited_ns = nullptr) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // try_wait suspends the thread for a while on its own; poll it a few times
+  // before reading the clocks.
+#pragma unroll 1
+  for (int i = 0; i < 16; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const WaitClock wc;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -57,17 +57,32 @@ constexpr int kMaxSlots = kConsumers / 16;        // reduction slots (K = 256 us
 constexpr int kRedValues = 32;                    // per slot: passes x 4 rows x NP tokens
 constexpr int kUnitSlots = 8;                     // gate/up units in flight per block
 
+// A work unit as the producer publishes it (decoded once, read by every consumer warp).
+struct UnitMeta {
+  int32_t valid;     // 0: past the end of this block's schedule
+  int32_t down;      // 0: gate/up, 1: down
+  int32_t tile;      // index into tile_list
+  int32_t block;     // b
+  int32_t expert;    // e (E = shared)
+  int32_t n;         // rows in this tile (1..8)
+  int32_t cnt;       // rows of the expert (all tiles)
+  int32_t pairs[kTileRows];
+};
+
 struct __align__(16) ExpertSmem {
   unsigned char stage[kStages][kStageStride];
   float red[kStages][kMaxSlots][kRedValues];      // per-warp partial sums of a stage
   float gu[kUnitSlots][kTileRows][2][32];         // gate/up results of a unit, [token][gate|up][i]
+  UnitMeta meta[kUnitSlots];                      // unit i of this block lives in slot i % kUnitSlots
   uint64_t full[kStages];                         // weights landed (producer arrive + tx bytes)
   uint64_t empty[kStages];                        // stage free again (16 consumer warps)
   uint64_t red_full[kStages];                     // partial sums posted (16 consumer warps)
-  uint32_t meta_unit[kStages];
-  uint32_t meta_step[kStages];
+  uint32_t meta_unit[kStages];                    // unit sequence number of the stage, or kDone
+  uint32_t meta_step[kStages];                    // stage index within the unit
   uint32_t unit_done[kUnitSlots];                 // stages of a gate/up unit already reduced
+  uint4 pf_q[2][kConsumers];                      // per-thread prefetch of the next unit's columns
 };
+static_assert(sizeof(ExpertSmem) <= 227 * 1024, "shared memory budget");
 
 template <int KG, int KD>
 struct Shape {
@@ -202,116 +217,166 @@ struct Butterfly {
   }
 };
 
-__device__ __forceinline__ int32_t pick8(const int32_t (&v)[kTileRows], int i) {
-  int32_t r = v[0];
-#pragma unroll
-  for (int j = 1; j < kTileRows; ++j) r = (i == j) ? v[j] : r;
-  return r;
-}
 
-// ------------------------------------------------------------------ unit decoding
-
-struct Unit {
-  int down;     // 0: gate/up, 1: down
-  int tile;     // index into tile_list
-  int block;    // b
-  int expert;   // e (E = shared)
-  int tile_in;  // j within the expert
-  int n;        // rows in this tile (1..8)
-};
+// ------------------------------------------------------------------ unit schedule
+// Static round-robin: block b runs units b, b + G, b + 2G, ... (G = grid size) in
+// increasing order. Every gate/up unit precedes every down unit in that order,
+// so a down unit only ever waits on lower-numbered units. Each block runs its
+// units in increasing order, so the waits cannot form a cycle.
 
 template <class S>
-__device__ __forceinline__ Unit decode_unit(const ExpertArgs &a, uint32_t u, int n_tiles) {
-  Unit r;
+__device__ __forceinline__ void unit_coords(uint32_t u, int n_tiles, int &down, int &tile, int &block) {
   const uint32_t ngu = uint32_t(n_tiles) * S::NBG;
   if (u < ngu) {
-    r.down = 0;
-    r.tile = int(u / S::NBG);
-    r.block = int(u % S::NBG);
+    down = 0;
+    tile = int(u / S::NBG);
+    block = int(u % S::NBG);
   } else {
     const uint32_t v = u - ngu;
-    r.down = 1;
-    r.tile = int(v / S::NBD);
-    r.block = int(v % S::NBD);
+    down = 1;
+    tile = int(v / S::NBD);
+    block = int(v % S::NBD);
   }
-  const int32_t te = __ldcg(a.tile_list + r.tile);
-  r.expert = te >> 16;
-  r.tile_in = te & 0xFFFF;
-  const int cnt = __ldcg(a.counts + r.expert);
-  const int n = cnt - kTileRows * r.tile_in;
-  r.n = n < kTileRows ? n : kTileRows;
-  return r;
 }
 
-// ------------------------------------------------------------------ producer
+// ------------------------------------------------------------------ producer (one warp)
+// A three-step fetch pipeline keeps the decode loads off the critical path.
+// Iteration i:
+//   1. lane 0 loads the tile_list entry of unit i+3;
+//   2. using unit i+2's tile_list entry (loaded one iteration earlier), load
+//      its expert row count (lane 0) and its <= 8 pair ids (lanes 0..7);
+//   3. issue the weight stages of unit i;
+//   4. publish unit i+2's metadata. The loads of step 2 have landed during step 3.
+// Units i and i+1 were published before unit i's first stage, so consumers can
+// prefetch unit i+1's token rows while they work on unit i.
 
 template <class S>
 __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
+  const int lane = threadIdx.x & 31;
   const uint64_t pol = l2_evict_first_policy();
-  const uint32_t total = uint32_t(n_tiles) * (S::NBG + S::NBD);
   const uint64_t pol_reuse = l2_evict_normal_policy();
+  const uint32_t total = uint32_t(n_tiles) * (S::NBG + S::NBD);
+  const uint32_t G = gridDim.x;
   // The producer's waits outlast the consumers' bounded ready wait, so a
   // consumer that gives up on a tile always drains the ring first.
   const int64_t wait_ns = 4 * a.timeout_ns;
+  auto unit_of = [&](uint32_t i) -> uint32_t { return blockIdx.x + i * G; };
+  auto load_te = [&](uint32_t i) -> int32_t {
+    const uint32_t u = unit_of(i);
+    if (u >= total) return -1;
+    int down, tile, block;
+    unit_coords<S>(u, n_tiles, down, tile, block);
+    return __ldcg(a.tile_list + tile);
+  };
+  struct Fetch {
+    int32_t te, cnt, pair;
+  };
+  // step 2: counts and pair ids (one pair per lane 0..7) of the unit whose tile entry is te
+  auto load_rows = [&](int32_t te) -> Fetch {
+    Fetch f{te, 0, 0};
+    if (te < 0) return f;
+    const int expert = te >> 16, tile_in = te & 0xFFFF;
+    f.cnt = __ldcg(a.counts + expert);
+    const int row = min(kTileRows * tile_in + (lane & 7), a.Tmax - 1);
+    f.pair = __ldcg(a.rows_of + int64_t(expert) * a.Tmax + row);
+    return f;
+  };
+  auto publish = [&](uint32_t i, const Fetch &f) {
+    UnitMeta &m = sm.meta[i & (kUnitSlots - 1)];
+    const uint32_t u = unit_of(i);
+    if (lane < kTileRows) m.pairs[lane] = f.pair;
+    if (lane == 0) {
+      m.valid = u < total && f.te >= 0;
+      int down = 0, tile = 0, block = 0;
+      if (m.valid) unit_coords<S>(u, n_tiles, down, tile, block);
+      m.down = down;
+      m.tile = tile;
+      m.block = block;
+      m.expert = f.te >> 16;
+      const int n = f.cnt - kTileRows * (f.te & 0xFFFF);
+      m.n = n < kTileRows ? n : kTileRows;
+      m.cnt = f.cnt;
+    }
+    __syncwarp();
+  };
+
+  // prologue: units 0 and 1 published, unit 2's rows in flight, unit 3's tile entry in flight
+  publish(0, load_rows(__shfl_sync(0xFFFFFFFFu, load_te(0), 0)));
+  publish(1, load_rows(__shfl_sync(0xFFFFFFFFu, load_te(1), 0)));
+  int32_t te_next = __shfl_sync(0xFFFFFFFFu, load_te(2), 0);  // unit i+2's entry at iteration i
+
   int stage = 0;
   uint32_t phase = 0;  // flips each time the ring wraps; empty-barrier parity is phase ^ 1
-  while (true) {
-    uint32_t u = atomicAdd(a.work, 1u);
-    if (ld_volatile(a.work + 1) != 0) u = total;  // abort: stop claiming
-    if (u >= total) {
+  for (uint32_t i = 0;; ++i) {
+    const UnitMeta &m = sm.meta[i & (kUnitSlots - 1)];
+    const bool stop = !m.valid || ld_volatile(a.work + 1) != 0;  // end of schedule, or abort
+    if (stop) {
       int64_t waited = 0;
       if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns, &waited)) {
-        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagEmptyWait, u, stage, phase, -1, waited, 0);
+        if (lane == 0) report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagEmptyWait, i, stage, phase, -1, waited, 0);
         return;
       }
-      sm.meta_unit[stage] = kDone;
-      sm.meta_step[stage] = 0;
-      mbar_arrive(&sm.full[stage]);
+      if (lane == 0) {
+        sm.meta_unit[stage] = kDone;
+        sm.meta_step[stage] = 0;
+        mbar_arrive(&sm.full[stage]);
+      }
       return;
     }
-    const Unit un = decode_unit<S>(a, u, n_tiles);
-    const bool sh = un.expert == a.E;
-    const int e = sh ? 0 : un.expert;
+    // steps 1 and 2 (loads in flight while the stages are issued)
+    const int32_t te_far = load_te(i + 3);
+    const Fetch f2 = load_rows(te_next);
+    const bool sh = m.expert == a.E;
+    const int e = sh ? 0 : m.expert;
+    const int down = m.down, block = m.block;
     // Weights of a single-tile expert are read once per step: evict first.
     // A multi-tile expert's weights are read once per tile: keep them in L2.
-    const uint64_t pol_u = __ldcg(a.counts + un.expert) > kTileRows ? pol_reuse : pol;
-    const int steps = un.down ? S::SPU_D : S::SPU_G;
+    const uint64_t pol_u = m.cnt > kTileRows ? pol_reuse : pol;
+    const int steps = down ? S::SPU_D : S::SPU_G;
     for (int s = 0; s < steps; ++s) {
       int64_t waited = 0;
       if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns, &waited)) {
-        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagEmptyWait, u, stage, phase, s, waited, 0);
-        atomicExch(a.work + 1, 1u);
+        if (lane == 0) {
+          report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagEmptyWait, i, stage, phase, s, waited, 0);
+          atomicExch(a.work + 1, 1u);
+        }
         return;
       }
-      sm.meta_unit[stage] = u;
-      sm.meta_step[stage] = uint32_t(s);
-      unsigned char *dst = sm.stage[stage];
-      mbar_arrive_expect_tx(&sm.full[stage], uint32_t(kStageStride));
-      if (!un.down) {
-        // gate rows i0 .. i0 + RS/2, then up rows i0 .. i0 + RS/2
-        constexpr int HALF = S::RS_G / 2;
-        const int64_t i0 = int64_t(un.block) * 32 + int64_t(s) * HALF;
-        const uint8_t *wg = sh ? a.sh_w_gate : a.w_gate + int64_t(e) * S::I * S::H;
-        const uint8_t *wu = sh ? a.sh_w_up : a.w_up + int64_t(e) * S::I * S::H;
-        const uint8_t *sg = sh ? a.sh_s_gate : a.s_gate + int64_t(e) * S::I * (S::H / kGroup);
-        const uint8_t *su = sh ? a.sh_s_up : a.s_up + int64_t(e) * S::I * (S::H / kGroup);
-        bulk_g2s(dst, wg + i0 * S::H, HALF * S::H, &sm.full[stage], pol_u);
-        bulk_g2s(dst + kStageBytes / 2, wu + i0 * S::H, HALF * S::H, &sm.full[stage], pol_u);
-        bulk_g2s(dst + kStageBytes, sg + i0 * (S::H / kGroup), HALF * (S::H / kGroup), &sm.full[stage], pol_u);
-        bulk_g2s(dst + kStageBytes + kStageScaleBytes / 2, su + i0 * (S::H / kGroup), HALF * (S::H / kGroup),
-                 &sm.full[stage], pol_u);
-      } else {
-        const int64_t r0 = int64_t(un.block) * S::DB + int64_t(s) * S::RS_D;
-        const uint8_t *wd = sh ? a.sh_w_down : a.w_down + int64_t(e) * S::H * S::I;
-        const uint8_t *sd = sh ? a.sh_s_down : a.s_down + int64_t(e) * S::H * (S::I / kGroup);
-        bulk_g2s(dst, wd + r0 * S::I, kStageBytes, &sm.full[stage], pol_u);
-        bulk_g2s(dst + kStageBytes, sd + r0 * (S::I / kGroup), kStageScaleBytes, &sm.full[stage], pol_u);
+      if (lane == 0) {
+        sm.meta_unit[stage] = i;
+        sm.meta_step[stage] = uint32_t(s);
+        unsigned char *dst = sm.stage[stage];
+        mbar_arrive_expect_tx(&sm.full[stage], uint32_t(kStageStride));
+        if (!down) {
+          // gate rows i0 .. i0 + RS/2, then up rows i0 .. i0 + RS/2
+          constexpr int HALF = S::RS_G / 2;
+          const int64_t i0 = int64_t(block) * 32 + int64_t(s) * HALF;
+          const uint8_t *wg = sh ? a.sh_w_gate : a.w_gate + int64_t(e) * S::I * S::H;
+          const uint8_t *wu = sh ? a.sh_w_up : a.w_up + int64_t(e) * S::I * S::H;
+          const uint8_t *sg = sh ? a.sh_s_gate : a.s_gate + int64_t(e) * S::I * (S::H / kGroup);
+          const uint8_t *su = sh ? a.sh_s_up : a.s_up + int64_t(e) * S::I * (S::H / kGroup);
+          bulk_g2s(dst, wg + i0 * S::H, HALF * S::H, &sm.full[stage], pol_u);
+          bulk_g2s(dst + kStageBytes / 2, wu + i0 * S::H, HALF * S::H, &sm.full[stage], pol_u);
+          bulk_g2s(dst + kStageBytes, sg + i0 * (S::H / kGroup), HALF * (S::H / kGroup), &sm.full[stage], pol_u);
+          bulk_g2s(dst + kStageBytes + kStageScaleBytes / 2, su + i0 * (S::H / kGroup), HALF * (S::H / kGroup),
+                   &sm.full[stage], pol_u);
+        } else {
+          const int64_t r0 = int64_t(block) * S::DB + int64_t(s) * S::RS_D;
+          const uint8_t *wd = sh ? a.sh_w_down : a.w_down + int64_t(e) * S::H * S::I;
+          const uint8_t *sd = sh ? a.sh_s_down : a.s_down + int64_t(e) * S::H * (S::I / kGroup);
+          bulk_g2s(dst, wd + r0 * S::I, kStageBytes, &sm.full[stage], pol_u);
+          bulk_g2s(dst + kStageBytes, sd + r0 * (S::I / kGroup), kStageScaleBytes, &sm.full[stage], pol_u);
+        }
       }
+      __syncwarp();
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
+    // step 4: publish unit i+2 (its slot last held unit i-6, long finished)
+    publish(i + 2, f2);
+    te_next = __shfl_sync(0xFFFFFFFFu, te_far, 0);
   }
 }
 
@@ -364,9 +429,9 @@ __device__ __forceinline__ void reduce_stage(const ExpertSmem &sm, int stage, in
 
 // gate/up epilogue, one warp: h = bf16(silu(bf16 g) * bf16 u), MXFP8 along I; then publish.
 template <class S>
-__device__ __forceinline__ void gate_up_epilogue(const ExpertArgs &a, ExpertSmem &sm, int uslot, const Unit &un,
-                                                 const int32_t (&pairs)[kTileRows], int lane) {
-  for (int t = 0; t < un.n; ++t) {
+__device__ __forceinline__ void gate_up_epilogue(const ExpertArgs &a, ExpertSmem &sm, int uslot, const UnitMeta &m,
+                                                 int lane) {
+  for (int t = 0; t < m.n; ++t) {
     const float gb = bf16_bits_to_float(float_to_bf16_bits(sm.gu[uslot][t][0][lane]));
     const float ub = bf16_bits_to_float(float_to_bf16_bits(sm.gu[uslot][t][1][lane]));
     const float silu = gb / (1.0f + expf(-gb));
@@ -376,102 +441,201 @@ __device__ __forceinline__ void gate_up_epilogue(const ExpertArgs &a, ExpertSmem
 #pragma unroll
     for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
     const uint32_t code = mx_scale_code(amax);
-    const int64_t p = pick8(pairs, t);
-    a.hq[p * S::I + int64_t(un.block) * 32 + lane] = float_to_e4m3(mx_unscale(hv, code));
-    if (lane == 0) a.hs[p * (S::I / kGroup) + un.block] = uint8_t(code);
-    if (a.h_bf16) a.h_bf16[p * S::I + int64_t(un.block) * 32 + lane] = hb;
+    const int64_t p = m.pairs[t];
+    a.hq[p * S::I + int64_t(m.block) * 32 + lane] = float_to_e4m3(mx_unscale(hv, code));
+    if (lane == 0) a.hs[p * (S::I / kGroup) + m.block] = uint8_t(code);
+    if (a.h_bf16) a.h_bf16[p * S::I + int64_t(m.block) * 32 + lane] = hb;
   }
   __threadfence();
   __syncwarp();
   if (lane == 0) {
-    if (un.tile != a.skip_ready_tile) red_release_gpu_add(a.ready + un.tile, 1u);
+    if (m.tile != a.skip_ready_tile) red_release_gpu_add(a.ready + m.tile, 1u);
     sm.unit_done[uslot] = 0;
   }
   __syncwarp();
 }
 
+// ------------------------------------------------------------------ activation prefetch
+// Each compute thread owns 16 columns of a tile row. For units with <= 2 rows
+// it copies its columns of the next unit's rows (and the group scales) into its
+// own shared-memory slot with cp.async while it works on the current unit.
+// Only that thread reads the slot, so the copy needs no block synchronisation
+// (cp.async.wait_group covers it). A down unit's h is prefetched only after its
+// tile's ready count has been observed complete.
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// This thread's 16 columns (codes) and scale byte address of tile row `tok` of unit m.
+template <class S>
+__device__ __forceinline__ const uint8_t *row_codes(const ExpertArgs &a, const UnitMeta &m, int tok, int tid) {
+  const int64_t p = m.pairs[tok];
+  if (m.down) return a.hq + p * S::I + 16 * (tid % (S::I / 16));
+  const int64_t t = m.expert == a.E ? p - int64_t(a.T) * a.k : p / a.k;
+  return a.xq + t * S::H + 16 * (tid % (S::H / 16));
+}
+template <class S>
+__device__ __forceinline__ const uint8_t *row_scale(const ExpertArgs &a, const UnitMeta &m, int tok, int tid) {
+  const int64_t p = m.pairs[tok];
+  if (m.down) return a.hs + p * (S::I / kGroup) + ((tid % (S::I / 16)) >> 1);
+  const int64_t t = m.expert == a.E ? p - int64_t(a.T) * a.k : p / a.k;
+  return a.xs + t * (S::H / kGroup) + ((tid % (S::H / 16)) >> 1);
+}
+
+// The 16 code bytes go to shared memory by cp.async (L2 path). The scale byte
+// goes to a register with an L2 load; neither is waited for until the unit starts.
+template <class S>
+__device__ __forceinline__ void prefetch_rows(const ExpertArgs &a, ExpertSmem &sm, const UnitMeta &m, int tid,
+                                              uint32_t (&pf_sc)[2]) {
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    if (t < m.n) {
+      cp_async16(&sm.pf_q[t][tid], row_codes<S>(a, m, t, tid));
+      pf_sc[t] = __ldcg(row_scale<S>(a, m, t, tid));
+    }
+  }
+  cp_async_commit();
+}
+
+// x.f for tokens 0..n-1 (n <= 2) from this thread's prefetch slot.
+__device__ __forceinline__ void load_prefetched(XRegs &x, const ExpertSmem &sm, const UnitMeta &m, int tid,
+                                                const uint32_t (&pf_sc)[2]) {
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    float2 v[8];
+    if (t < m.n) {
+      decode16(sm.pf_q[t][tid], v);
+      const float sc = ue8m0_to_float(pf_sc[t]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = make_float2(v[i].x * sc, v[i].y * sc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x.f[t][i] = v[i];
+  }
+}
+
+// Bounded wait until every gate/up unit of `tile` has published (lane 0 polls,
+// the warp agrees). Returns false after a timeout.
+template <class S>
+__device__ __forceinline__ bool wait_tile_ready(const ExpertArgs &a, int tile, uint32_t i, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    const WaitClock wc;
+    uint32_t seen;
+    while ((seen = ld_acquire_gpu(a.ready + tile)) < uint32_t(S::NBG)) {
+      if (wc.expired(a.timeout_ns)) {
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagReadyWait, i, tile, seen, S::NBG, wc.ns(), wc.cycles());
+        atomicExch(a.work + 1, 1u);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;  // the shuffle also orders lane 0's acquire before the warp's loads
+}
+
 template <class S>
 __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
+  (void)n_tiles;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int stage = 0;
   uint32_t phase = 0;   // barrier parity of the current ring pass
   uint32_t seq = 0;     // stages processed by this block: the reducer of stage seq is warp seq % 16
-  int uslot = -1;       // unit sequence number mod kUnitSlots
-  Unit un{};
-  int32_t pairs[kTileRows];
+  uint32_t unit = 0;    // this block's unit sequence number of the current unit
+  int uslot = 0;
   XRegs x;
-  // this thread's columns of tile row `tok`: h rows (down) or x rows (gate/up)
-  auto row_q = [&](int tok) -> const uint8_t * {
-    const int64_t p = pick8(pairs, tok);
-    if (un.down) return a.hq + p * S::I + 16 * (tid % (S::I / 16));
-    const int64_t t = un.expert == a.E ? p - int64_t(a.T) * a.k : p / a.k;
-    return a.xq + t * S::H + 16 * (tid % (S::H / 16));
-  };
-  auto row_s = [&](int tok) -> const uint8_t * {
-    const int64_t p = pick8(pairs, tok);
-    if (un.down) return a.hs + p * (S::I / kGroup) + ((tid % (S::I / 16)) >> 1);
-    const int64_t t = un.expert == a.E ? p - int64_t(a.T) * a.k : p / a.k;
-    return a.xs + t * (S::H / kGroup) + ((tid % (S::H / 16)) >> 1);
-  };
   int np = 1, passes = 1;
   bool skip = false;
+  bool pf_ready_now = false;   // the prefetch slot holds the current unit's rows
+  bool pf_pending = false;     // the next unit's rows are being prefetched into the slot
+  bool pf_down_next = false;   // the next unit is a down unit whose rows may be prefetched late
+  uint32_t ready_seen = 0;     // lane 0: the next down unit's ready count, loaded early
+  uint32_t pf_sc[2] = {0, 0};  // scale codes of the prefetched rows
   while (true) {
     int64_t waited = 0;
     if (!mbar_wait(&sm.full[stage], phase, 16 * a.timeout_ns, &waited)) {
-      report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, -1, stage, phase, -1, waited, 0);
-      atomicExch(a.work + 1, 1u);
+      if (lane == 0) {
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, -1, stage, phase, -1, waited, 0);
+        atomicExch(a.work + 1, 1u);
+      }
       return;
     }
     const uint32_t u = sm.meta_unit[stage];
     const int s = int(sm.meta_step[stage]);
-    if (u == kDone) return;
+    if (u == kDone) {
+      cp_async_wait_all();
+      return;
+    }
     const unsigned char *st = sm.stage[stage];
     if (s == 0) {
-      // ---- unit start: rows of the tile, and this thread's x (or h) columns in registers
-      un = decode_unit<S>(a, u, n_tiles);
-      uslot = (uslot + 1) & (kUnitSlots - 1);
-      const int64_t rbase = int64_t(un.expert) * a.Tmax + int64_t(un.tile_in) * kTileRows;
-#pragma unroll
-      for (int r = 0; r < kTileRows; ++r) pairs[r] = r < un.n ? __ldcg(a.rows_of + rbase + r) : pairs[0];
+      // ---- unit start. The producer published this unit and the next one.
+      unit = u;
+      uslot = int(unit & (kUnitSlots - 1));
+      const UnitMeta &m = sm.meta[uslot];
+      cp_async_wait_all();
+      pf_ready_now = pf_pending;
+      pf_pending = false;
       skip = false;
-      if (un.down) {
-        // h of this tile must be complete: bounded wait on the tile's ready count (one lane per warp)
-        int ab = 0;
-        if (lane == 0) {
-          const WaitClock wc;
-          uint32_t seen;
-          while ((seen = ld_acquire_gpu(a.ready + un.tile)) < uint32_t(S::NBG)) {
-            if (wc.expired(a.timeout_ns)) {
-              report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagReadyWait, u, un.tile, seen, S::NBG, wc.ns(),
-                          wc.cycles());
-              atomicExch(a.work + 1, 1u);
-              ab = 1;
-              break;
-            }
-            __nanosleep(64);
-          }
+      np = m.n <= 1 ? 1 : 2;
+      passes = (m.n + np - 1) / np;
+      if (pf_ready_now) {
+        load_prefetched(x, sm, m, tid, pf_sc);
+      } else {
+        if (m.down) skip = !wait_tile_ready<S>(a, m.tile, unit, lane);
+        if (passes == 1 && !skip) {
+          auto rq = [&](int tok) { return row_codes<S>(a, m, tok, tid); };
+          auto rs = [&](int tok) { return row_scale<S>(a, m, tok, tid); };
+          if (np == 1) load_pass<1>(x, 0, m.n, rq, rs);
+          else load_pass<2>(x, 0, m.n, rq, rs);
         }
-        skip = __shfl_sync(0xFFFFFFFFu, ab, 0) != 0;
       }
-      np = un.n <= 1 ? 1 : 2;
-      passes = (un.n + np - 1) / np;
-      if (passes == 1 && !skip) {
-        if (np == 1) load_pass<1>(x, 0, un.n, row_q, row_s);
-        else load_pass<2>(x, 0, un.n, row_q, row_s);
+      // prefetch the next unit's rows (gate/up now; down once its tile is seen ready)
+      const UnitMeta &mn = sm.meta[(unit + 1) & (kUnitSlots - 1)];
+      pf_down_next = false;
+      if (mn.valid && mn.n <= 2) {
+        if (!mn.down) {
+          prefetch_rows<S>(a, sm, mn, tid, pf_sc);
+          pf_pending = true;
+        } else {
+          pf_down_next = true;
+          if (lane == 0) ready_seen = ld_acquire_gpu(a.ready + mn.tile);
+        }
       }
     }
+    const UnitMeta &m = sm.meta[uslot];
     // ---- this stage: dot products and warp reductions, posted to red[stage]
     if (!skip) {
       for (int p = 0; p < passes; ++p) {
         if (np == 1) {
-          if (un.down) stage_pass<S::I, 1>(sm, st, stage, p, x);
+          if (m.down) stage_pass<S::I, 1>(sm, st, stage, p, x);
           else stage_pass<S::H, 1>(sm, st, stage, p, x);
         } else {
-          if (passes > 1) load_pass<2>(x, p, un.n, row_q, row_s);
-          if (un.down) stage_pass<S::I, 2>(sm, st, stage, p, x);
+          if (passes > 1) {
+            auto rq = [&](int tok) { return row_codes<S>(a, m, tok, tid); };
+            auto rs = [&](int tok) { return row_scale<S>(a, m, tok, tid); };
+            load_pass<2>(x, p, m.n, rq, rs);
+          }
+          if (m.down) stage_pass<S::I, 2>(sm, st, stage, p, x);
           else stage_pass<S::H, 2>(sm, st, stage, p, x);
         }
       }
+    }
+    const int spu = m.down ? S::SPU_D : S::SPU_G;
+    if (s == spu - 1 && pf_down_next) {
+      // the next unit is a down unit: prefetch its h if its tile was already complete
+      const int ok = __shfl_sync(0xFFFFFFFFu, ready_seen >= uint32_t(S::NBG) ? 1 : 0, 0);
+      if (ok) {
+        prefetch_rows<S>(a, sm, sm.meta[(unit + 1) & (kUnitSlots - 1)], tid, pf_sc);
+        pf_pending = true;
+      }
+      pf_down_next = false;
     }
     __syncwarp();
     const bool reducer = int(seq % kConsumerWarps) == warp;
@@ -482,17 +646,19 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     if (reducer) {
       // ---- cross-warp sums of this stage, then outputs
       if (!mbar_wait(&sm.red_full[stage], phase, 16 * a.timeout_ns, &waited)) {
-        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, u, stage, phase, -2, waited, 0);
-        atomicExch(a.work + 1, 1u);
+        if (lane == 0) {
+          report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, u, stage, phase, -2, waited, 0);
+          atomicExch(a.work + 1, 1u);
+        }
       } else if (!skip) {
-        if (un.down) {
-          const int64_t hrow0 = int64_t(un.block) * S::DB + int64_t(s) * S::RS_D;
-          reduce_stage<S::I>(sm, stage, passes, np, un.n, lane, [&](int r, int tok, float v) {
-            a.o[int64_t(pick8(pairs, tok)) * S::H + hrow0 + r] = v;
+        if (m.down) {
+          const int64_t hrow0 = int64_t(m.block) * S::DB + int64_t(s) * S::RS_D;
+          reduce_stage<S::I>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
+            a.o[int64_t(m.pairs[tok]) * S::H + hrow0 + r] = v;
           });
         } else {
           constexpr int HALF = S::RS_G / 2;
-          reduce_stage<S::H>(sm, stage, passes, np, un.n, lane, [&](int r, int tok, float v) {
+          reduce_stage<S::H>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
             const int which = r < HALF ? 0 : 1;
             const int i = s * HALF + (r < HALF ? r : r - HALF);
             sm.gu[uslot][tok][which][i] = v;
@@ -505,7 +671,7 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
           before = __shfl_sync(0xFFFFFFFFu, before, 0);
           if (before == uint32_t(S::SPU_G - 1)) {
             __threadfence_block();
-            gate_up_epilogue<S>(a, sm, uslot, un, pairs, lane);
+            gate_up_epilogue<S>(a, sm, uslot, m, lane);
           }
         }
       }
