@@ -309,10 +309,12 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
   uint32_t phase = 0;  // flips each time the ring wraps; empty-barrier parity is phase ^ 1
   for (uint32_t i = 0;; ++i) {
     const UnitMeta &m = sm.meta[i & (kUnitSlots - 1)];
-    const bool stop = !m.valid || ld_volatile(a.work + 1) != 0;  // end of schedule, or abort
+    // end of schedule, or abort: lane 0 decides for the warp
+    const int stop = __shfl_sync(0xFFFFFFFFu, (!m.valid || ld_volatile(a.work + 1) != 0) ? 1 : 0, 0);
     if (stop) {
       int64_t waited = 0;
-      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns, &waited)) {
+      const int ok = __shfl_sync(0xFFFFFFFFu, mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns, &waited) ? 1 : 0, 0);
+      if (!ok) {
         if (lane == 0) report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagEmptyWait, i, stage, phase, -1, waited, 0);
         return;
       }
@@ -335,7 +337,8 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     const int steps = down ? S::SPU_D : S::SPU_G;
     for (int s = 0; s < steps; ++s) {
       int64_t waited = 0;
-      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns, &waited)) {
+      const int ok = __shfl_sync(0xFFFFFFFFu, mbar_wait(&sm.empty[stage], phase ^ 1u, wait_ns, &waited) ? 1 : 0, 0);
+      if (!ok) {
         if (lane == 0) {
           report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagEmptyWait, i, stage, phase, s, waited, 0);
           atomicExch(a.work + 1, 1u);
@@ -706,7 +709,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
   pdl_wait_primary();
   const int n_tiles = __ldcg(a.n_tiles);
   if (warp == kConsumerWarps) {
-    if ((threadIdx.x & 31) == 0) producer<S>(a, sm, n_tiles);
+    producer<S>(a, sm, n_tiles);  // the whole warp: lanes 0..7 fetch pair ids, lane 0 issues copies
     return;
   }
   consumers<S>(a, sm, n_tiles);
