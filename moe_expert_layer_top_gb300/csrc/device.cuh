@@ -179,6 +179,25 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
   return __half22float2(*reinterpret_cast<__half2 *>(&h));
 }
 
+// Two E4M3 codes (low byte first) -> f16x2 bits (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// c + a.lo * b.lo + a.hi * b.hi with f16 operands and an fp32 accumulator, two
+// fma.rn.f32.f16: each product is exact in fp32 and each step rounds once.
+__device__ __forceinline__ float fma_f16x2_f32(uint32_t a2, uint32_t b2, float c) {
+  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\t"
+      "mov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+      "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+      : "+f"(c)
+      : "r"(a2), "r"(b2));
+  return c;
+}
+
 // float -> E4M3, round to nearest even, saturating to +-448.
 __device__ __forceinline__ uint8_t float_to_e4m3(float v) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));

@@ -115,19 +115,21 @@ struct Rows {
 // ------------------------------------------------------------------ per-thread math
 
 struct XRegs {
-  float2 f[2][8];           // the pass's tokens, dequantised: 16 values as 8 pairs each
+  uint32_t h[2][8];         // the pass's tokens: 16 E4M3 values as 8 f16x2 (exact, unscaled)
+  float sc[2];              // their group scales 2^(code - 127)
 };
 
-__device__ __forceinline__ void decode16(const uint4 v, float2 (&o)[8]) {
+// 16 E4M3 codes -> 8 f16x2 (exact: every E4M3 value is an f16 normal or zero).
+__device__ __forceinline__ void decode16_h2(const uint4 v, uint32_t (&o)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    o[2 * i] = e4m3x2_to_float2(uint16_t(w[i] & 0xFFFFu));
-    o[2 * i + 1] = e4m3x2_to_float2(uint16_t(w[i] >> 16));
+    o[2 * i] = e4m3x2_to_f16x2(uint16_t(w[i] & 0xFFFFu));
+    o[2 * i + 1] = e4m3x2_to_f16x2(uint16_t(w[i] >> 16));
   }
 }
 
-// Tokens [NP*pass, NP*pass + NP) of the tile into fp32 registers, scales applied.
+// Tokens [NP*pass, NP*pass + NP) of the tile into registers (f16x2 codes + scale).
 // row_q(tok) / row_s(tok) give the thread's 16 E4M3 codes and the group's scale
 // code of a tile row. They are read through L2: an earlier grid or block wrote them.
 template <int NP, class FQ, class FS>
@@ -135,22 +137,20 @@ __device__ __forceinline__ void load_pass(XRegs &x, int pass, int n, FQ &&row_q,
 #pragma unroll
   for (int t = 0; t < NP; ++t) {
     const int tok = NP * pass + t;
-    float2 v[8];
     if (tok < n) {
-      decode16(__ldcg(reinterpret_cast<const uint4 *>(row_q(tok))), v);
-      const float sc = ue8m0_to_float(__ldcg(row_s(tok)));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = make_float2(v[i].x * sc, v[i].y * sc);
+      decode16_h2(__ldcg(reinterpret_cast<const uint4 *>(row_q(tok))), x.h[t]);
+      x.sc[t] = ue8m0_to_float(__ldcg(row_s(tok)));
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < 8; ++i) x.h[t][i] = 0u;
+      x.sc[t] = 0.f;
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x.f[t][i] = v[i];
   }
 }
 
 // This thread's partial dot products for its 4 rows of the stage and NP tokens.
+// Products of two E4M3 values are exact in fp32; fma.rn.f32.f16 accumulates
+// them in fp32 directly from the f16 operands (no separate widening).
 template <int K, int NP>
 __device__ __forceinline__ void stage_dot(const unsigned char *st, int g, int c, const XRegs &x,
                                           float (&acc)[4 * NP]) {
@@ -162,17 +162,17 @@ __device__ __forceinline__ void stage_dot(const unsigned char *st, int g, int c,
     const int r = g + R::RG * j;
     const uint4 wv = *reinterpret_cast<const uint4 *>(sw + r * K + 16 * c);
     const float ws = ue8m0_to_float(ss[r * (K / kGroup) + (c >> 1)]);
-    float2 w[8];
-    decode16(wv, w);
+    uint32_t w[8];
+    decode16_h2(wv, w);
 #pragma unroll
     for (int t = 0; t < NP; ++t) {
-      float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+      float c0 = 0.f, c1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
-        a0 = __ffma2_rn(w[i], x.f[t][i], a0);
-        a1 = __ffma2_rn(w[i + 1], x.f[t][i + 1], a1);
+        c0 = fma_f16x2_f32(w[i], x.h[t][i], c0);
+        c1 = fma_f16x2_f32(w[i + 1], x.h[t][i + 1], c1);
       }
-      acc[j * NP + t] = ws * ((a0.x + a1.x) + (a0.y + a1.y));
+      acc[j * NP + t] = (c0 + c1) * (ws * x.sc[t]);
     }
   }
 }
@@ -503,23 +503,19 @@ __device__ __forceinline__ void prefetch_rows(const ExpertArgs &a, ExpertSmem &s
   cp_async_commit();
 }
 
-// x.f for tokens 0..n-1 (n <= 2) from this thread's prefetch slot.
+// Tokens 0..n-1 (n <= 2) of the unit from this thread's prefetch slot.
 __device__ __forceinline__ void load_prefetched(XRegs &x, const ExpertSmem &sm, const UnitMeta &m, int tid,
                                                 const uint32_t (&pf_sc)[2]) {
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    float2 v[8];
     if (t < m.n) {
-      decode16(sm.pf_q[t][tid], v);
-      const float sc = ue8m0_to_float(pf_sc[t]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = make_float2(v[i].x * sc, v[i].y * sc);
+      decode16_h2(sm.pf_q[t][tid], x.h[t]);
+      x.sc[t] = ue8m0_to_float(pf_sc[t]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < 8; ++i) x.h[t][i] = 0u;
+      x.sc[t] = 0.f;
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x.f[t][i] = v[i];
   }
 }
 
