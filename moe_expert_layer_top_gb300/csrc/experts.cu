@@ -35,10 +35,10 @@
 //    against its 16 columns of the token rows (fp32 registers, 2 tokens per
 //    pass).
 // A transposing butterfly reduces 4 rows x NP tokens across the lanes. Each
-// warp then posts its partial sums to shared memory and arrives on the stage's
-// reduction barrier. One warp per stage, rotating, sums the partials across
-// warps in a fixed order and writes the outputs. No block-wide barrier runs
-// in steady state. Every output goes through the same addition tree
+// warp then posts its partial sums to shared memory and counts itself in with
+// a shared-memory atomic. The last warp to post sums the partials across warps
+// in a fixed order, writes the outputs and frees the stage. No warp waits for
+// another, and no block-wide barrier runs in steady state. Every output goes through the same addition tree
 // whatever the tile's row count, so results do not depend on tile-mates.
 #include <stdint.h>
 
@@ -76,10 +76,10 @@ struct __align__(16) ExpertSmem {
   UnitMeta meta[kUnitSlots];                      // unit i of this block lives in slot i % kUnitSlots
   uint64_t full[kStages];                         // weights landed (producer arrive + tx bytes)
   uint64_t empty[kStages];                        // stage free again (16 consumer warps)
-  uint64_t red_full[kStages];                     // partial sums posted (16 consumer warps)
   uint32_t meta_unit[kStages];                    // unit sequence number of the stage, or kDone
   uint32_t meta_step[kStages];                    // stage index within the unit
   uint32_t unit_done[kUnitSlots];                 // stages of a gate/up unit already reduced
+  uint32_t posted[kStages];                       // warps that posted their partial sums of the stage
   uint4 pf_q[2][kConsumers];                      // per-thread prefetch of the next unit's columns
 };
 static_assert(sizeof(ExpertSmem) <= 227 * 1024, "shared memory budget");
@@ -406,7 +406,7 @@ __device__ __forceinline__ void stage_pass(ExpertSmem &sm, const unsigned char *
   }
 }
 
-// The rotating reducer: sums one stage's partials across the warps of each
+// The stage's last warp to post: sums one stage's partials across the warps of each
 // row group, in slot order. Calls out(row_in_stage, token, value).
 template <int K, class F>
 __device__ __forceinline__ void reduce_stage(const ExpertSmem &sm, int stage, int passes, int np, int n, int lane,
@@ -546,7 +546,6 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int stage = 0;
   uint32_t phase = 0;   // barrier parity of the current ring pass
-  uint32_t seq = 0;     // stages processed by this block: the reducer of stage seq is warp seq % 16
   uint32_t unit = 0;    // this block's unit sequence number of the current unit
   int uslot = 0;
   XRegs x;
@@ -603,8 +602,9 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
           prefetch_rows<S>(a, sm, mn, tid, pf_sc);
           pf_pending = true;
         } else {
+          // a relaxed look now (no ordering stall); upgraded by a fence when used
           pf_down_next = true;
-          if (lane == 0) ready_seen = ld_acquire_gpu(a.ready + mn.tile);
+          if (lane == 0) ready_seen = ld_relaxed_gpu(a.ready + mn.tile);
         }
       }
     }
@@ -631,25 +631,29 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
       // the next unit is a down unit: prefetch its h if its tile was already complete
       const int ok = __shfl_sync(0xFFFFFFFFu, ready_seen >= uint32_t(S::NBG) ? 1 : 0, 0);
       if (ok) {
+        // relaxed load that saw the count complete + fence = acquire; the
+        // warp's copies below are ordered after it by the shuffle
+        if (lane == 0) __threadfence();
+        __syncwarp();
         prefetch_rows<S>(a, sm, sm.meta[(unit + 1) & (kUnitSlots - 1)], tid, pf_sc);
         pf_pending = true;
       }
       pf_down_next = false;
     }
     __syncwarp();
-    const bool reducer = int(seq % kConsumerWarps) == warp;
+    // The last warp to post its partial sums of this stage reduces it, so no
+    // warp ever waits for another; it then frees the stage.
+    uint32_t before = 0;
     if (lane == 0) {
-      mbar_arrive(&sm.red_full[stage]);
-      if (!reducer) mbar_arrive(&sm.empty[stage]);
+      __threadfence_block();
+      before = atomicAdd(&sm.posted[stage], 1u);
     }
-    if (reducer) {
-      // ---- cross-warp sums of this stage, then outputs
-      if (!mbar_wait(&sm.red_full[stage], phase, 16 * a.timeout_ns, &waited)) {
-        if (lane == 0) {
-          report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, u, stage, phase, -2, waited, 0);
-          atomicExch(a.work + 1, 1u);
-        }
-      } else if (!skip) {
+    before = __shfl_sync(0xFFFFFFFFu, before, 0);
+    if (before != uint32_t(kConsumerWarps - 1)) {
+      if (lane == 0) mbar_arrive(&sm.empty[stage]);
+    } else {
+      __threadfence_block();
+      if (!skip) {
         if (m.down) {
           const int64_t hrow0 = int64_t(m.block) * S::DB + int64_t(s) * S::RS_D;
           reduce_stage<S::I>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
@@ -665,19 +669,21 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
           // the warp that reduces the unit's last outstanding stage runs the epilogue
           __threadfence_block();
           __syncwarp();
-          uint32_t before = 0;
-          if (lane == 0) before = atomicAdd(&sm.unit_done[uslot], 1u);
-          before = __shfl_sync(0xFFFFFFFFu, before, 0);
-          if (before == uint32_t(S::SPU_G - 1)) {
+          uint32_t done = 0;
+          if (lane == 0) done = atomicAdd(&sm.unit_done[uslot], 1u);
+          done = __shfl_sync(0xFFFFFFFFu, done, 0);
+          if (done == uint32_t(S::SPU_G - 1)) {
             __threadfence_block();
             gate_up_epilogue<S>(a, sm, uslot, m, lane);
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[stage]);
+      if (lane == 0) {
+        sm.posted[stage] = 0;
+        mbar_arrive(&sm.empty[stage]);
+      }
     }
-    ++seq;
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1u;
@@ -695,7 +701,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], kConsumerWarps);
-      mbar_init(&sm.red_full[i], kConsumerWarps);
+      sm.posted[i] = 0;
     }
     for (int i = 0; i < kUnitSlots; ++i) sm.unit_done[i] = 0;
     fence_mbar_init();
