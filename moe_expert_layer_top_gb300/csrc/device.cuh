@@ -87,14 +87,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+// One try_wait. The thread sleeps in hardware until the phase completes or
+// about suspend_ns have passed, so waiting warps do not take issue slots
+// from working ones.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t suspend_ns = 20000) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
@@ -103,10 +106,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // timeout_ns (see WaitClock) and returns false; the caller reports MOE_ERR_TIMEOUT.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int64_t timeout_ns,
                                          int64_t *waited_ns = nullptr) {
-  // try_wait suspends the thread for a while on its own; poll it a few times
-  // before reading the clocks.
+  // try_wait suspends the thread on its own; poll it a few times before
+  // reading the clocks.
 #pragma unroll 1
-  for (int i = 0; i < 16; ++i)
+  for (int i = 0; i < 4; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   const WaitClock wc;
   while (true) {

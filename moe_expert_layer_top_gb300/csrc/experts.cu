@@ -24,7 +24,7 @@
 // - Same page, 3.1: SwiGLU with the original intermediate rounding. g and u are
 //   rounded to bf16, and h = bf16(silu(g) * u) is then quantised.
 //
-// Block layout: 16 compute warps + 1 producer warp. The producer's elected
+// Block layout: 16 compute warps + 1 producer warp + 1 reducer warp. The producer's elected
 // lane streams the unit's weight rows with bulk copies (TMA, no tensor map, no
 // multicast) into a 5-stage ring of 32 KB + scales.
 //
@@ -35,10 +35,11 @@
 //    against its 16 columns of the token rows (fp32 registers, 2 tokens per
 //    pass).
 // A transposing butterfly reduces 4 rows x NP tokens across the lanes. Each
-// warp then posts its partial sums to shared memory and counts itself in with
-// a shared-memory atomic. The last warp to post sums the partials across warps
-// in a fixed order, writes the outputs and frees the stage. No warp waits for
-// another, and no block-wide barrier runs in steady state. Every output goes through the same addition tree
+// compute warp then posts its partial sums to shared memory and arrives on the
+// stage's reduction barrier. The reducer warp sums the partials across warps in
+// a fixed order, writes the outputs, runs the gate/up epilogue and frees the
+// stage. Compute warps never wait for each other or for the reducer except
+// through the depth of the ring. No block-wide barrier runs in steady state. Every output goes through the same addition tree
 // whatever the tile's row count, so results do not depend on tile-mates.
 #include <stdint.h>
 
@@ -72,14 +73,13 @@ struct UnitMeta {
 struct __align__(16) ExpertSmem {
   unsigned char stage[kStages][kStageStride];
   float red[kStages][kMaxSlots][kRedValues];      // per-warp partial sums of a stage
-  float gu[kUnitSlots][kTileRows][2][32];         // gate/up results of a unit, [token][gate|up][i]
+  float gu[kTileRows][2][32];                     // gate/up results of the reducer's unit, [token][gate|up][i]
   UnitMeta meta[kUnitSlots];                      // unit i of this block lives in slot i % kUnitSlots
   uint64_t full[kStages];                         // weights landed (producer arrive + tx bytes)
-  uint64_t empty[kStages];                        // stage free again (16 consumer warps)
+  uint64_t empty[kStages];                        // stage free again (the reducer warp)
+  uint64_t red_full[kStages];                     // partial sums posted (16 compute warps)
   uint32_t meta_unit[kStages];                    // unit sequence number of the stage, or kDone
   uint32_t meta_step[kStages];                    // stage index within the unit
-  uint32_t unit_done[kUnitSlots];                 // stages of a gate/up unit already reduced
-  uint32_t posted[kStages];                       // warps that posted their partial sums of the stage
   uint4 pf_q[2][kConsumers];                      // per-thread prefetch of the next unit's columns
 };
 static_assert(sizeof(ExpertSmem) <= 227 * 1024, "shared memory budget");
@@ -432,11 +432,10 @@ __device__ __forceinline__ void reduce_stage(const ExpertSmem &sm, int stage, in
 
 // gate/up epilogue, one warp: h = bf16(silu(bf16 g) * bf16 u), MXFP8 along I; then publish.
 template <class S>
-__device__ __forceinline__ void gate_up_epilogue(const ExpertArgs &a, ExpertSmem &sm, int uslot, const UnitMeta &m,
-                                                 int lane) {
+__device__ __forceinline__ void gate_up_epilogue(const ExpertArgs &a, ExpertSmem &sm, const UnitMeta &m, int lane) {
   for (int t = 0; t < m.n; ++t) {
-    const float gb = bf16_bits_to_float(float_to_bf16_bits(sm.gu[uslot][t][0][lane]));
-    const float ub = bf16_bits_to_float(float_to_bf16_bits(sm.gu[uslot][t][1][lane]));
+    const float gb = bf16_bits_to_float(float_to_bf16_bits(sm.gu[t][0][lane]));
+    const float ub = bf16_bits_to_float(float_to_bf16_bits(sm.gu[t][1][lane]));
     const float silu = gb / (1.0f + expf(-gb));
     const uint16_t hb = float_to_bf16_bits(silu * ub);
     const float hv = bf16_bits_to_float(hb);
@@ -453,7 +452,6 @@ __device__ __forceinline__ void gate_up_epilogue(const ExpertArgs &a, ExpertSmem
   __syncwarp();
   if (lane == 0) {
     if (m.tile != a.skip_ready_tile) red_release_gpu_add(a.ready + m.tile, 1u);
-    sm.unit_done[uslot] = 0;
   }
   __syncwarp();
 }
@@ -543,7 +541,7 @@ __device__ __forceinline__ bool wait_tile_ready(const ExpertArgs &a, int tile, u
 template <class S>
 __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
   (void)n_tiles;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
   int stage = 0;
   uint32_t phase = 0;   // barrier parity of the current ring pass
   uint32_t unit = 0;    // this block's unit sequence number of the current unit
@@ -641,49 +639,65 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
       pf_down_next = false;
     }
     __syncwarp();
-    // The last warp to post its partial sums of this stage reduces it, so no
-    // warp ever waits for another; it then frees the stage.
-    uint32_t before = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      before = atomicAdd(&sm.posted[stage], 1u);
+    if (lane == 0) mbar_arrive(&sm.red_full[stage]);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
     }
-    before = __shfl_sync(0xFFFFFFFFu, before, 0);
-    if (before != uint32_t(kConsumerWarps - 1)) {
-      if (lane == 0) mbar_arrive(&sm.empty[stage]);
-    } else {
-      __threadfence_block();
-      if (!skip) {
-        if (m.down) {
-          const int64_t hrow0 = int64_t(m.block) * S::DB + int64_t(s) * S::RS_D;
-          reduce_stage<S::I>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
-            a.o[int64_t(m.pairs[tok]) * S::H + hrow0 + r] = v;
-          });
-        } else {
-          constexpr int HALF = S::RS_G / 2;
-          reduce_stage<S::H>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
-            const int which = r < HALF ? 0 : 1;
-            const int i = s * HALF + (r < HALF ? r : r - HALF);
-            sm.gu[uslot][tok][which][i] = v;
-          });
-          // the warp that reduces the unit's last outstanding stage runs the epilogue
-          __threadfence_block();
-          __syncwarp();
-          uint32_t done = 0;
-          if (lane == 0) done = atomicAdd(&sm.unit_done[uslot], 1u);
-          done = __shfl_sync(0xFFFFFFFFu, done, 0);
-          if (done == uint32_t(S::SPU_G - 1)) {
-            __threadfence_block();
-            gate_up_epilogue<S>(a, sm, uslot, m, lane);
-          }
-        }
-      }
-      __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------ reducer (one warp)
+// For every stage: waits until the 16 compute warps have posted their partial
+// sums, sums them across warps in a fixed order, writes the outputs and frees
+// the stage. At the end of a gate/up unit it runs the SwiGLU + MXFP8 epilogue
+// and publishes the tile's ready count. The compute warps never wait for it
+// except through the depth of the ring.
+template <class S>
+__device__ void reducer(const ExpertArgs &a, ExpertSmem &sm) {
+  const int lane = threadIdx.x & 31;
+  int stage = 0;
+  uint32_t phase = 0;
+  while (true) {
+    int64_t waited = 0;
+    if (!__shfl_sync(0xFFFFFFFFu, mbar_wait(&sm.full[stage], phase, 16 * a.timeout_ns, &waited) ? 1 : 0, 0)) {
       if (lane == 0) {
-        sm.posted[stage] = 0;
-        mbar_arrive(&sm.empty[stage]);
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, -1, stage, phase, -3, waited, 0);
+        atomicExch(a.work + 1, 1u);
       }
+      return;
     }
+    const uint32_t u = sm.meta_unit[stage];
+    const int s = int(sm.meta_step[stage]);
+    if (u == kDone) return;
+    if (!__shfl_sync(0xFFFFFFFFu, mbar_wait(&sm.red_full[stage], phase, 16 * a.timeout_ns, &waited) ? 1 : 0, 0)) {
+      if (lane == 0) {
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, u, stage, phase, -2, waited, 0);
+        atomicExch(a.work + 1, 1u);
+      }
+      return;
+    }
+    const int uslot = int(u & (kUnitSlots - 1));
+    const UnitMeta &m = sm.meta[uslot];
+    const int np = m.n <= 1 ? 1 : 2;
+    const int passes = (m.n + np - 1) / np;
+    if (m.down) {
+      const int64_t hrow0 = int64_t(m.block) * S::DB + int64_t(s) * S::RS_D;
+      reduce_stage<S::I>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
+        a.o[int64_t(m.pairs[tok]) * S::H + hrow0 + r] = v;
+      });
+    } else {
+      constexpr int HALF = S::RS_G / 2;
+      reduce_stage<S::H>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
+        const int which = r < HALF ? 0 : 1;
+        const int i = s * HALF + (r < HALF ? r : r - HALF);
+        sm.gu[tok][which][i] = v;
+      });
+      __syncwarp();
+      if (s == S::SPU_G - 1) gate_up_epilogue<S>(a, sm, m, lane);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1u;
@@ -700,10 +714,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], kConsumerWarps);
-      sm.posted[i] = 0;
+      mbar_init(&sm.empty[i], 1);
+      mbar_init(&sm.red_full[i], kConsumerWarps);
     }
-    for (int i = 0; i < kUnitSlots; ++i) sm.unit_done[i] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -712,6 +725,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
   const int n_tiles = __ldcg(a.n_tiles);
   if (warp == kConsumerWarps) {
     producer<S>(a, sm, n_tiles);  // the whole warp: lanes 0..7 fetch pair ids, lane 0 issues copies
+    return;
+  }
+  if (warp == kConsumerWarps + 1) {
+    reducer<S>(a, sm);
     return;
   }
   consumers<S>(a, sm, n_tiles);

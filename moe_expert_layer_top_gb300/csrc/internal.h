@@ -11,7 +11,7 @@ namespace moe {
 constexpr int kTileRows = 8;            // rows per expert tile
 constexpr int kGroup = 32;              // MXFP8 group along K
 constexpr int kConsumerWarps = 16;      // expert kernel: compute warps
-constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kExpertThreads = (kConsumerWarps + 2) * 32;  // + one producer warp + one reducer warp
 constexpr int kStageBytes = 32768;      // weight bytes per pipeline stage
 constexpr int kStages = 5;              // pipeline depth
 constexpr int kRouteThreads = 1024;     // route kernel: block 0 (router + placement)
