@@ -166,6 +166,25 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def traffic_per_launch(algorithmic_bytes):
+    """DRAM bytes per expert-kernel launch from the committed ncu capture, scaled
+    by the active weight bytes; None if the kernel source changed since then."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "experts_kernel_traffic.json")
+    src = os.path.join(ROOT, "moe_expert_layer_top_gb300", "csrc", "experts.cu")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if sha != d["source_sha256"]:
+        return None
+    ratio = (d["dram_bytes_read"] + d["dram_bytes_write"]) / d["algorithmic_bytes"]
+    return int(round(algorithmic_bytes * ratio))
+
+
 def active_experts(lg, k, shared):
     import numpy as np
     ids = np.argsort(-lg, axis=1, kind="stable")[:, :k]
@@ -377,7 +396,8 @@ def run_gpu(args):
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": None,
+            "traffic": traffic_per_launch(main["weight_bytes"]),
+            "traffic_source": "profiles/experts_kernel_traffic.json (ncu capture at 64 experts, scaled by weight bytes)",
             "algorithmic_bytes_per_launch": main["weight_bytes"],
             "kernel_us": round(exp_ms * 1e3, 3),
         },
