@@ -203,6 +203,37 @@ moe_status_t moe_plan_status(void *plan, int32_t *status_out);
  * All zero when the last step had no device-side error. Synchronises the device. */
 moe_status_t moe_plan_diagnostics(void *plan, int64_t *out8);
 
+/* Size of the fixed device array used by moe_forward_static_scratch. */
+#define MOE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* A MoE step that allocates nothing, for callers that cannot call cudaMalloc
+ * where they run the step. Examples:
+ *  - a server whose allocator has already reserved nearly all device memory;
+ *  - code that must avoid the synchronisation and latency of cudaMalloc/cudaFree;
+ *  - a plugin that is only handed its input and output buffers.
+ * It runs the same kernels as moe_forward, with every intermediate kept in a
+ * fixed device array of MOE_STATIC_SCRATCH_BYTES compiled into this library.
+ * Every GPU that loads the library holds that array until the process exits.
+ * There is no plan: the config and weights are passed on every call, as for
+ * moe_plan (max_rows is ignored; T bounds the step).
+ *   x, logits, y, d_status: as moe_forward (device memory, caller-owned).
+ * Returns MOE_ERR_UNSUPPORTED, before any device work, when the step's
+ * scratch (about T * (k*(4H + 1.03 I) + 1.03 H + 4(E+1)) bytes) exceeds
+ * MOE_STATIC_SCRATCH_BYTES. At H = 4096, I = 2048, E = 256, k = 8 that is
+ * about 50 rows. It also returns the Guard's errors, as moe_plan does.
+ * Every call uses the same array. Calls that overlap on the GPU (two streams,
+ * or two host threads) race and corrupt each other's results. Everything that
+ * must start at zero is cleared by the step itself.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and sets kernel
+ * attributes. Make that first call before any stream capture. Each call also
+ * raises the route kernel's dynamic shared-memory limit (cudaFuncSetAttribute,
+ * host-side only).
+ * The pages have no counterpart to this entry point. */
+moe_status_t moe_forward_static_scratch(const moe_config_t *config, const moe_weights_t *weights, const void *x,
+                                        const float *logits, int32_t T, void *y, int32_t *d_status,
+                                        void *cuda_stream);
+
 /* Teardown: frees the plan's device memory and events, after a device-wide
  * synchronise. NULL is a no-op. */
 moe_status_t moe_destroy(void *plan);

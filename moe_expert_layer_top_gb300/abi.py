@@ -36,8 +36,11 @@ EXPORTED = (
     "moe_kernel_times",
     "moe_plan_status",
     "moe_plan_diagnostics",
+    "moe_forward_static_scratch",
     "moe_destroy",
 )
+
+MOE_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class MoeError(RuntimeError):
@@ -107,6 +110,9 @@ def load(path: str | None = None):
     lib.moe_plan_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32)]
     lib.moe_plan_diagnostics.restype = ctypes.c_int
     lib.moe_plan_diagnostics.argtypes = [_P, ctypes.POINTER(ctypes.c_int64)]
+    lib.moe_forward_static_scratch.restype = ctypes.c_int
+    lib.moe_forward_static_scratch.argtypes = [ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeWeights), _P, _P,
+                                               ctypes.c_int32, _P, _P, _P]
     lib.moe_destroy.restype = ctypes.c_int
     lib.moe_destroy.argtypes = [_P]
     if lib.moe_abi_version() != MOE_ABI_VERSION:
@@ -202,6 +208,14 @@ def moe_plan_diagnostics(plan: int) -> list[int]:
     out = (ctypes.c_int64 * 8)()
     check("moe_plan_diagnostics", lib.moe_plan_diagnostics(plan, out))
     return list(out)
+
+
+def moe_forward_static_scratch(config: MoeConfig, weights: MoeWeights, x, logits, T: int, y, d_status=None,
+                               stream=None) -> int:
+    """One MoE step with no allocation (scratch in the library's fixed device array)."""
+    lib = load()
+    return lib.moe_forward_static_scratch(ctypes.byref(config), ctypes.byref(weights), ptr(x), ptr(logits), T, ptr(y),
+                                          ptr(d_status), stream_ptr(stream))
 
 
 def moe_destroy(plan: int | None) -> int:

@@ -116,6 +116,7 @@ cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int cols, uint8_t *
 cudaError_t launch_experts(const ExpertArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t st);
 bool experts_shape_supported(int H, int I);
+moe_status_t guard_host(const moe_config_t &c, const moe_weights_t &w);
 size_t experts_smem_bytes();
 
 }  // namespace moe

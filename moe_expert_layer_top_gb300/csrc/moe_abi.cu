@@ -119,6 +119,14 @@ moe_status_t copy_taps(Plan *p, const moe_taps_t *t, int T, cudaStream_t st) {
 
 }  // namespace
 
+namespace moe {
+// The Guard's host-only checks, for the other entry points of the library.
+moe_status_t guard_host(const moe_config_t &c, const moe_weights_t &w) {
+  const moe_status_t g = guard_config(c);
+  return g != MOE_OK ? g : guard_weights(c, w);
+}
+}  // namespace moe
+
 extern "C" {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
