@@ -1,7 +1,7 @@
 """Benchmark of the small-batch MXFP8 MoE step on GB300.
 
 One step is one pass of the whole hot path over one batch of synthetic input:
-route + place + quantise x, expert SwiGLU MLPs (gate/up, then down), combine.
+route + place + quantise x, expert SwiGLU MLPs (gate/up, then down) with the combine fused into the expert kernel.
 
 Default workload: the bs1 speculative-verify shape. That is T=6 token rows,
 H=4096, E=256 routed experts, top-8, I=2048, MXFP8 weights (group-32 UE8M0
@@ -402,7 +402,7 @@ def run_gpu(args):
             "kernel_us": round(exp_ms * 1e3, 3),
         },
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": summarise_clocks(clock_rows),
     }
     if cpu is not None:

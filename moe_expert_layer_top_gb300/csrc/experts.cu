@@ -647,6 +647,49 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
   }
 }
 
+// ------------------------------------------------------------------ fused combine
+// y[t][h] for h in down block b: ((w_0*o_0 + w_1*o_1) + ...) + o_shared in
+// binary32, rank order, no contraction, then bf16. One warp runs it: the one
+// whose down unit was the last of token row t's k (+ shared) pairs to finish
+// block b. The o values of the other pairs were written by other blocks; the
+// counter atomics and the fences on both sides order them before these reads.
+// Source: "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", 2.1. The
+// weighted reduction of expert outputs is fused with the shared-expert addition.
+template <class S>
+__device__ __forceinline__ void fused_combine(const ExpertArgs &a, int t, int b, int lane) {
+  const int64_t h0 = int64_t(b) * S::DB;
+  for (int h = lane; h < S::DB; h += 32) {
+    float acc = 0.0f;
+    for (int j = 0; j < a.k; ++j) {
+      const float w = __ldcg(a.topk_w + int64_t(t) * a.k + j);
+      const float v = __ldcg(a.o + (int64_t(t) * a.k + j) * S::H + h0 + h);
+      acc = j == 0 ? __fmul_rn(w, v) : __fadd_rn(acc, __fmul_rn(w, v));
+    }
+    if (a.shared) acc = __fadd_rn(acc, __ldcg(a.o + (int64_t(a.T) * a.k + t) * S::H + h0 + h));
+    a.y[int64_t(t) * S::H + h0 + h] = float_to_bf16_bits(acc);
+  }
+}
+
+// After a down unit's last stage: count each of its pairs in for (token row,
+// block) and run the combine for the rows this unit completes.
+template <class S>
+__device__ __forceinline__ void down_unit_done(const ExpertArgs &a, const UnitMeta &m, int lane) {
+  __threadfence();  // this unit's o stores, before the counts
+  __syncwarp();
+  const uint32_t target = uint32_t(a.k + a.shared);
+  for (int r = 0; r < m.n; ++r) {
+    const int64_t p = m.pairs[r];
+    const int t = p < int64_t(a.T) * a.k ? int(p / a.k) : int(p - int64_t(a.T) * a.k);
+    uint32_t before = 0;
+    if (lane == 0) before = atomicAdd(a.comb_cnt + int64_t(t) * S::NBD + m.block, 1u);
+    before = __shfl_sync(0xFFFFFFFFu, before, 0);
+    if (before == target - 1) {
+      __threadfence();  // the other pairs' o stores, before the reads below
+      fused_combine<S>(a, t, m.block, lane);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ reducer (one warp)
 // For every stage: waits until the 16 compute warps have posted their partial
 // sums, sums them across warps in a fixed order, writes the outputs and frees
@@ -686,6 +729,8 @@ __device__ void reducer(const ExpertArgs &a, ExpertSmem &sm) {
       reduce_stage<S::I>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
         a.o[int64_t(m.pairs[tok]) * S::H + hrow0 + r] = v;
       });
+      __syncwarp();
+      if (s == S::SPU_D - 1) down_unit_done<S>(a, m, lane);
     } else {
       constexpr int HALF = S::RS_G / 2;
       reduce_stage<S::H>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
@@ -759,6 +804,13 @@ cudaError_t launch_shape(const ExpertArgs &a, int grid, cudaStream_t st) {
 }  // namespace
 
 size_t experts_smem_bytes() { return sizeof(ExpertSmem); }
+
+int experts_down_blocks(int H, int I) {
+  if (H == 4096 && I == 2048) return Shape<4096, 2048>::NBD;
+  if (H == 1024 && I == 512) return Shape<1024, 512>::NBD;
+  if (H == 512 && I == 256) return Shape<512, 256>::NBD;
+  return 0;
+}
 
 // Shapes compiled into the library: (H, I) = (4096, 2048), (1024, 512), (512, 256).
 bool experts_shape_supported(int H, int I) {

@@ -29,6 +29,7 @@ struct Scratch {
   int32_t *tile_list;   // [n_tiles_max] (expert << 16) | tile
   int32_t *n_tiles;     // [1]
   uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile
+  uint32_t *comb_cnt;   // [Tmax][H / DB] down blocks of a token row finished (fused combine)
   uint32_t *work;       // [2] unit counter, abort flag
   int32_t *status;      // [1] plan-owned status word
   int64_t *diag;        // [8] first device-side error of the last step (site, unit, tile, ...)
@@ -75,6 +76,8 @@ struct RouteArgs {
   int32_t *n_tiles;
   uint32_t *ready;
   int n_tiles_max;
+  uint32_t *comb_cnt;
+  int n_comb;
   uint32_t *work;
   int32_t *status;
   int64_t *diag;
@@ -94,18 +97,15 @@ struct ExpertArgs {
   uint16_t *h_bf16;  // NULL unless the h tap is requested
   float *o;
   uint32_t *ready;
+  uint32_t *comb_cnt;       // per (token row, down block): arrivals of the row's k (+ shared) pairs
+  const float *topk_w;      // combine weights [T][k]
+  uint16_t *y;              // bf16 [T][H] output
+  int shared;
   uint32_t *work;
   int32_t *status;
   int64_t *diag;
   int64_t timeout_ns;
   int skip_ready_tile;  // fault injection: tile index whose ready count is never published, or -1
-};
-
-struct CombineArgs {
-  const float *o;
-  const float *topk_w;
-  int T, H, k, shared;
-  uint16_t *y;
 };
 
 size_t route_smem_bytes(int E, int words);
@@ -114,7 +114,7 @@ cudaError_t prepare_experts(int H, int I);
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
 cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int cols, uint8_t *q, uint8_t *s, cudaStream_t st);
 cudaError_t launch_experts(const ExpertArgs &a, int grid, cudaStream_t st);
-cudaError_t launch_combine(const CombineArgs &a, cudaStream_t st);
+int experts_down_blocks(int H, int I);  // H / DB: down units per tile
 bool experts_shape_supported(int H, int I);
 moe_status_t guard_host(const moe_config_t &c, const moe_weights_t &w);
 size_t experts_smem_bytes();

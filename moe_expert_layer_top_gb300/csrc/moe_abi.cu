@@ -8,11 +8,10 @@
 // - Build allocates every scratch buffer once for max_rows. "Beyond Day-0:
 //   Optimizing DeepSeek-V4.1 Flash in SGLang" 2.1 reuses scratch buffers
 //   across calls to avoid re-initialisation.
-// - Runtime enqueues three kernels:
+// - Runtime enqueues two kernels:
 //     1. route + place + quantise x;
-//     2. the persistent expert kernel, launched with Programmatic Dependent
-//        Launch;
-//     3. the combine.
+//     2. the persistent expert kernel (gate/up, down and the fused combine),
+//        launched with Programmatic Dependent Launch.
 //   It allocates nothing and does not synchronise.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -192,6 +191,7 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   const size_t o_slot = take(pairs_routed * 4), o_rows = take(size_t(E + 1) * Tm * 4);
   const size_t o_tl = take(size_t(p->n_tiles_max) * 4), o_nt = take(4);
   const size_t o_ready = take(size_t(p->n_tiles_max) * 4), o_work = take(8), o_status = take(4);
+  const size_t o_comb = take(size_t(Tm) * experts_down_blocks(H, I) * 4);
   const size_t o_diag = take(8 * 8);
   const size_t o_xq = take(size_t(Tm) * H), o_xs = take(size_t(Tm) * (H / 32));
   const size_t o_hq = take(size_t(p->pairs_max) * I), o_hs = take(size_t(p->pairs_max) * (I / 32));
@@ -214,6 +214,7 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   s.tile_list = reinterpret_cast<int32_t *>(base + o_tl);
   s.n_tiles = reinterpret_cast<int32_t *>(base + o_nt);
   s.ready = reinterpret_cast<uint32_t *>(base + o_ready);
+  s.comb_cnt = reinterpret_cast<uint32_t *>(base + o_comb);
   s.work = reinterpret_cast<uint32_t *>(base + o_work);
   s.status = reinterpret_cast<int32_t *>(base + o_status);
   s.diag = reinterpret_cast<int64_t *>(base + o_diag);
@@ -288,6 +289,8 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ra.n_tiles = s.n_tiles;
   ra.ready = s.ready;
   ra.n_tiles_max = p->n_tiles_max;
+  ra.comb_cnt = s.comb_cnt;
+  ra.n_comb = T * experts_down_blocks(c.hidden, c.intermediate);
   ra.work = s.work;
   ra.status = status;
   ra.diag = s.diag;
@@ -325,6 +328,10 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ea.h_bf16 = (taps && taps->h_bf16) ? s.h_bf16 : nullptr;
   ea.o = s.o;
   ea.ready = s.ready;
+  ea.comb_cnt = s.comb_cnt;
+  ea.topk_w = s.topk_w;
+  ea.y = static_cast<uint16_t *>(y);
+  ea.shared = c.num_shared;
   ea.work = s.work;
   ea.status = status;
   ea.diag = s.diag;
@@ -338,15 +345,6 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
     ++p->timed_calls;
   }
 
-  CombineArgs ca;
-  ca.o = s.o;
-  ca.topk_w = s.topk_w;
-  ca.T = T;
-  ca.H = c.hidden;
-  ca.k = c.top_k;
-  ca.shared = c.num_shared;
-  ca.y = static_cast<uint16_t *>(y);
-  if (launch_combine(ca, st) != cudaSuccess) return MOE_ERR_CUDA;
   return copy_taps(p, taps, T, st);
 }
 

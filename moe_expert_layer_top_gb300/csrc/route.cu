@@ -84,55 +84,47 @@ struct RouteSmem {
   int32_t warp_sums[kRouteThreads / 32];
 };
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-
-__device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
+// Top-k and combine weights, one warp per token row. Each lane keeps its NC
+// candidates (lane, lane + 32, ...) in registers as 64-bit keys: the
+// order-preserving bits of the logit, then the complemented expert id. So the
+// largest key is the largest logit and, among equal logits, the lower id.
+template <int NC>
+__device__ __forceinline__ void route_topk(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, k = a.k, T = a.T, W = a.words;
-
-  if (tid < 8) a.diag[tid] = 0;
-  if (tid == 0) {
-    *a.status = MOE_OK;  // start of the step
-    a.work[0] = 0;       // unit counter
-    a.work[1] = 0;       // abort flag
-  }
-  for (int i = tid; i < a.n_tiles_max; i += blockDim.x) a.ready[i] = 0;
-  for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0;
-  __syncthreads();
-
-  // --- top-k + combine weights: one warp per token row
   for (int t = warp; t < T; t += kRouteThreads / 32) {
     const float *row = a.logits + int64_t(t) * E;
-    uint32_t taken = 0;  // bit j: this lane's candidate lane + 32*j already selected
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7FFFFFFF;
-      for (int j = 0; j * 32 + lane < E; ++j) {
-        if (taken & (1u << j)) continue;
-        const int i = j * 32 + lane;
-        const float v = __ldg(row + i);
-        if (better(v, i, bv, bi)) { bv = v; bi = i; }
+    uint64_t key[NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const int i = j * 32 + lane;
+      key[j] = 0;
+      if (i < E) {
+        const uint32_t b = __float_as_uint(__ldg(row + i));
+        const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        key[j] = (uint64_t(ord) << 32) | uint32_t(0xFFFFFFFFu - uint32_t(i));
       }
+    }
+    for (int r = 0; r < k; ++r) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int j = 0; j < NC; ++j) best = key[j] > best ? key[j] : best;
 #pragma unroll
       for (int off = 16; off; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+        best = o > best ? o : best;
       }
-      if (bi >= E) {  // only possible with NaN logits: take the lowest unselected id
-        report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
-        int cand = 0x7FFFFFFF;
-        for (int j = 0; j * 32 + lane < E; ++j)
-          if (!(taken & (1u << j))) { cand = j * 32 + lane; break; }
+      const int id = int(0xFFFFFFFFu - uint32_t(best));
+      if (id >= E) report_error(a.status, MOE_ERR_DEVICE_BOUNDS);  // cannot happen for k <= E
 #pragma unroll
-        for (int off = 16; off; off >>= 1) cand = min(cand, __shfl_xor_sync(0xFFFFFFFFu, cand, off));
-        bi = cand;
-        bv = __ldg(row + bi);
+      for (int j = 0; j < NC; ++j)
+        if (key[j] == best) key[j] = 0;  // taken (only the owning lane matches)
+      if (lane == 0) {
+        const uint32_t ord = uint32_t(best >> 32);
+        const uint32_t bits = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
+        sm.sel_i[warp][r] = id < E ? id : 0;
+        sm.sel_v[warp][r] = __uint_as_float(bits);
       }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == 0) { sm.sel_i[warp][r] = bi; sm.sel_v[warp][r] = bv; }
     }
     __syncwarp();
     // weights: e_j = exp_rn(l_j - l_0); s = ((e_0 + e_1) + ...) ; w_j = e_j / s
@@ -151,6 +143,31 @@ __device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
     }
     __syncwarp();
   }
+}
+
+__device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E, k = a.k, T = a.T, W = a.words;
+
+  if (tid < 8) a.diag[tid] = 0;
+  if (tid == 0) {
+    *a.status = MOE_OK;  // start of the step
+    a.work[0] = 0;       // unit counter
+    a.work[1] = 0;       // abort flag
+  }
+  for (int i = tid; i < a.n_tiles_max; i += blockDim.x) a.ready[i] = 0;
+  for (int i = tid; i < a.n_comb; i += blockDim.x) a.comb_cnt[i] = 0;
+  for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0;
+  __syncthreads();
+
+  // --- top-k + combine weights: one warp per token row
+  const int nc = (E + 31) / 32;
+  if (nc <= 1) route_topk<1>(a, sm, bm);
+  else if (nc <= 2) route_topk<2>(a, sm, bm);
+  else if (nc <= 4) route_topk<4>(a, sm, bm);
+  else if (nc <= 8) route_topk<8>(a, sm, bm);
+  else if (nc <= 16) route_topk<16>(a, sm, bm);
+  else route_topk<32>(a, sm, bm);
   __syncthreads();
 
   // --- counts and tiles per expert (index E: the shared expert, every row)

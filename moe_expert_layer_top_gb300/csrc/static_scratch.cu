@@ -9,8 +9,8 @@
 //    spikes cudaMalloc/cudaFree can cause;
 //  - code loaded as a plugin that is only handed input and output buffers.
 // moe_plan allocates its scratch once (cudaMalloc), which such callers cannot
-// do. moe_forward_static_scratch runs the same three kernels (route, experts,
-// combine) on the fixed array below instead. It allocates nothing, and it
+// do. moe_forward_static_scratch runs the same kernels (route, and experts with the
+// fused combine) on the fixed array below instead. It allocates nothing, and it
 // calls no allocating library routine.
 //
 // Cost and limits:
@@ -81,7 +81,7 @@ moe_status_t setup_device(int dev, DeviceSetup *&out) {
 }
 
 struct Layout {
-  size_t ids, w, bm, cnt, slot, rows, tl, nt, ready, work, status, diag, xq, xs, hq, hs, o, total;
+  size_t ids, w, bm, cnt, slot, rows, tl, nt, ready, comb, work, status, diag, xq, xs, hq, hs, o, total;
 };
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
@@ -106,6 +106,7 @@ Layout layout_for(const moe_config_t &c, int T, int words, int n_tiles_max) {
   L.tl = take(size_t(n_tiles_max) * 4);
   L.nt = take(4);
   L.ready = take(size_t(n_tiles_max) * 4);
+  L.comb = take(size_t(T) * experts_down_blocks(c.hidden, c.intermediate) * 4);
   L.work = take(8);
   L.status = take(4);
   L.diag = take(64);
@@ -178,6 +179,8 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ra.n_tiles = reinterpret_cast<int32_t *>(base + L.nt);
   ra.ready = reinterpret_cast<uint32_t *>(base + L.ready);
   ra.n_tiles_max = n_tiles_max;
+  ra.comb_cnt = reinterpret_cast<uint32_t *>(base + L.comb);
+  ra.n_comb = T * experts_down_blocks(c.hidden, c.intermediate);
   ra.work = reinterpret_cast<uint32_t *>(base + L.work);
   ra.status = status;
   ra.diag = reinterpret_cast<int64_t *>(base + L.diag);
@@ -215,6 +218,10 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ea.h_bf16 = nullptr;
   ea.o = reinterpret_cast<float *>(base + L.o);
   ea.ready = ra.ready;
+  ea.comb_cnt = ra.comb_cnt;
+  ea.topk_w = ra.topk_w;
+  ea.y = static_cast<uint16_t *>(y);
+  ea.shared = c.num_shared;
   ea.work = ra.work;
   ea.status = status;
   ea.diag = ra.diag;
@@ -222,14 +229,5 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ea.skip_ready_tile = -1;
   if (launch_experts(ea, d->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
 
-  CombineArgs ca;
-  ca.o = ea.o;
-  ca.topk_w = ra.topk_w;
-  ca.T = T;
-  ca.H = c.hidden;
-  ca.k = c.top_k;
-  ca.shared = c.num_shared;
-  ca.y = static_cast<uint16_t *>(y);
-  if (launch_combine(ca, st) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
