@@ -56,8 +56,7 @@ constexpr int kStageScaleBytes = kStageBytes / kGroup;
 constexpr int kStageStride = kStageBytes + kStageScaleBytes;
 constexpr int kMaxSlots = kConsumers / 16;        // reduction slots (K = 256 uses half-warps)
 constexpr int kRedValues = 32;                    // per slot: passes x 4 rows x NP tokens
-constexpr int kUnitSlots = 16;                    // units whose metadata may still be read (ring lags)
-constexpr int kRedStages = 8;                     // ring of posted partial sums (compute warps -> reducer)
+constexpr int kUnitSlots = 8;                     // gate/up units in flight per block
 
 // A work unit as the producer publishes it (decoded once, read by every consumer warp).
 struct UnitMeta {
@@ -73,15 +72,12 @@ struct UnitMeta {
 
 struct __align__(16) ExpertSmem {
   unsigned char stage[kStages][kStageStride];
-  float red[kRedStages][kMaxSlots][kRedValues];   // per-warp partial sums of a stage
+  float red[kStages][kMaxSlots][kRedValues];      // per-warp partial sums of a stage
   float gu[kTileRows][2][32];                     // gate/up results of the reducer's unit, [token][gate|up][i]
   UnitMeta meta[kUnitSlots];                      // unit i of this block lives in slot i % kUnitSlots
   uint64_t full[kStages];                         // weights landed (producer arrive + tx bytes)
-  uint64_t empty[kStages];                        // weight stage free again (16 compute warps)
-  uint64_t red_full[kRedStages];                  // partial sums posted (16 compute warps)
-  uint64_t red_empty[kRedStages];                 // partial sums consumed (the reducer warp)
-  uint32_t red_unit[kRedStages];                  // unit sequence number of the posted stage, or kDone
-  uint32_t red_step[kRedStages];                  // its stage index within the unit
+  uint64_t empty[kStages];                        // stage free again (the reducer warp)
+  uint64_t red_full[kStages];                     // partial sums posted (16 compute warps)
   uint32_t meta_unit[kStages];                    // unit sequence number of the stage, or kDone
   uint32_t meta_step[kStages];                    // stage index within the unit
   uint4 pf_q[2][kConsumers];                      // per-thread prefetch of the next unit's columns
@@ -381,8 +377,7 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
         phase ^= 1u;
       }
     }
-    // step 4: publish unit i+2. Its slot last held unit i-14; compute warps lag
-    // the producer by at most 5 stages and the reducer by at most 8 more.
+    // step 4: publish unit i+2 (its slot last held unit i-6, long finished)
     publish(i + 2, f2);
     te_next = __shfl_sync(0xFFFFFFFFu, te_far, 0);
   }
@@ -393,7 +388,7 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
 // One pass (NP tokens) over this thread's 4 rows of the stage: dot products,
 // warp reduction, and the per-slot partial sums into red[stage].
 template <int K, int NP>
-__device__ __forceinline__ void stage_pass(ExpertSmem &sm, const unsigned char *st, int rslot, int pass,
+__device__ __forceinline__ void stage_pass(ExpertSmem &sm, const unsigned char *st, int stage, int pass,
                                            const XRegs &x) {
   using R = Rows<K>;
   constexpr int V = 4 * NP;
@@ -407,7 +402,7 @@ __device__ __forceinline__ void stage_pass(ExpertSmem &sm, const unsigned char *
   BF::run(acc, l);
   if ((l & BF::TAILMASK) == 0) {
 #pragma unroll
-    for (int i = 0; i < BF::CNT; ++i) sm.red[rslot][slot][pass * V + BF::index(l, i)] = acc[i];
+    for (int i = 0; i < BF::CNT; ++i) sm.red[stage][slot][pass * V + BF::index(l, i)] = acc[i];
   }
 }
 
@@ -559,19 +554,6 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
   bool pf_down_next = false;   // the next unit is a down unit whose rows may be prefetched late
   uint32_t ready_seen = 0;     // lane 0: the next down unit's ready count, loaded early
   uint32_t pf_sc[2] = {0, 0};  // scale codes of the prefetched rows
-  int rslot = 0;               // slot of the partial-sum ring
-  uint32_t rphase = 0;
-  // posts the end of work to the reducer through the partial-sum ring
-  auto post_done = [&]() {
-    int64_t w = 0;
-    mbar_wait(&sm.red_empty[rslot], rphase ^ 1u, 16 * a.timeout_ns, &w);
-    if (tid == 0) {
-      sm.red_unit[rslot] = kDone;
-      sm.red_step[rslot] = 0;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.red_full[rslot]);
-  };
   while (true) {
     int64_t waited = 0;
     if (!mbar_wait(&sm.full[stage], phase, 16 * a.timeout_ns, &waited)) {
@@ -585,18 +567,9 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     const int s = int(sm.meta_step[stage]);
     if (u == kDone) {
       cp_async_wait_all();
-      post_done();
       return;
     }
     const unsigned char *st = sm.stage[stage];
-    // the partial-sum slot must have been consumed by the reducer
-    if (!mbar_wait(&sm.red_empty[rslot], rphase ^ 1u, 16 * a.timeout_ns, &waited)) {
-      if (lane == 0) {
-        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, u, rslot, rphase, -4, waited, 0);
-        atomicExch(a.work + 1, 1u);
-      }
-      return;
-    }
     if (s == 0) {
       // ---- unit start. The producer published this unit and the next one.
       unit = u;
@@ -638,16 +611,16 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     if (!skip) {
       for (int p = 0; p < passes; ++p) {
         if (np == 1) {
-          if (m.down) stage_pass<S::I, 1>(sm, st, rslot, p, x);
-          else stage_pass<S::H, 1>(sm, st, rslot, p, x);
+          if (m.down) stage_pass<S::I, 1>(sm, st, stage, p, x);
+          else stage_pass<S::H, 1>(sm, st, stage, p, x);
         } else {
           if (passes > 1) {
             auto rq = [&](int tok) { return row_codes<S>(a, m, tok, tid); };
             auto rs = [&](int tok) { return row_scale<S>(a, m, tok, tid); };
             load_pass<2>(x, p, m.n, rq, rs);
           }
-          if (m.down) stage_pass<S::I, 2>(sm, st, rslot, p, x);
-          else stage_pass<S::H, 2>(sm, st, rslot, p, x);
+          if (m.down) stage_pass<S::I, 2>(sm, st, stage, p, x);
+          else stage_pass<S::H, 2>(sm, st, stage, p, x);
         }
       }
     }
@@ -665,23 +638,11 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
       }
       pf_down_next = false;
     }
-    // done with the weights of this stage: the producer may refill it
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[stage]);
-    // post this stage's partial sums
-    if (tid == 0) {
-      sm.red_unit[rslot] = u;
-      sm.red_step[rslot] = uint32_t(s);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.red_full[rslot]);
+    if (lane == 0) mbar_arrive(&sm.red_full[stage]);
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1u;
-    }
-    if (++rslot == kRedStages) {
-      rslot = 0;
-      rphase ^= 1u;
     }
   }
 }
@@ -696,37 +657,17 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
 // weighted reduction of expert outputs is fused with the shared-expert addition.
 template <class S>
 __device__ __forceinline__ void fused_combine(const ExpertArgs &a, int t, int b, int lane) {
-  constexpr int Q = S::DB / 32;  // outputs per lane
-  const int64_t h0 = int64_t(b) * S::DB + lane;
-  float acc[Q];
-#pragma unroll
-  for (int q = 0; q < Q; ++q) acc[q] = 0.0f;
-  // pairs in chunks of 4: all loads of a chunk are in flight together
-  for (int j0 = 0; j0 < a.k; j0 += 4) {
-    float w[4], v[4][Q];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int j = j0 + jj < a.k ? j0 + jj : a.k - 1;
-      w[jj] = __ldcg(a.topk_w + int64_t(t) * a.k + j);
-      const float *src = a.o + (int64_t(t) * a.k + j) * S::H + h0;
-#pragma unroll
-      for (int q = 0; q < Q; ++q) v[jj][q] = __ldcg(src + 32 * q);
+  const int64_t h0 = int64_t(b) * S::DB;
+  for (int h = lane; h < S::DB; h += 32) {
+    float acc = 0.0f;
+    for (int j = 0; j < a.k; ++j) {
+      const float w = __ldcg(a.topk_w + int64_t(t) * a.k + j);
+      const float v = __ldcg(a.o + (int64_t(t) * a.k + j) * S::H + h0 + h);
+      acc = j == 0 ? __fmul_rn(w, v) : __fadd_rn(acc, __fmul_rn(w, v));
     }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      if (j0 + jj >= a.k) break;
-#pragma unroll
-      for (int q = 0; q < Q; ++q)
-        acc[q] = (j0 + jj == 0) ? __fmul_rn(w[jj], v[jj][q]) : __fadd_rn(acc[q], __fmul_rn(w[jj], v[jj][q]));
-    }
+    if (a.shared) acc = __fadd_rn(acc, __ldcg(a.o + (int64_t(a.T) * a.k + t) * S::H + h0 + h));
+    a.y[int64_t(t) * S::H + h0 + h] = float_to_bf16_bits(acc);
   }
-  if (a.shared) {
-    const float *src = a.o + (int64_t(a.T) * a.k + t) * S::H + h0;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) acc[q] = __fadd_rn(acc[q], __ldcg(src + 32 * q));
-  }
-#pragma unroll
-  for (int q = 0; q < Q; ++q) a.y[int64_t(t) * S::H + h0 + 32 * q] = float_to_bf16_bits(acc[q]);
 }
 
 // After a down unit's last stage: count each of its pairs in for (token row,
@@ -750,56 +691,61 @@ __device__ __forceinline__ void down_unit_done(const ExpertArgs &a, const UnitMe
 }
 
 // ------------------------------------------------------------------ reducer (one warp)
-// For every posted stage: waits until the 16 compute warps have posted their
-// partial sums, sums them across warps in a fixed order, writes the outputs
-// and frees the partial-sum slot. At the end of a gate/up unit it runs the
-// SwiGLU + MXFP8 epilogue and publishes the tile's ready count. At the end of
-// a down unit it counts the unit in for the fused combine. The weight ring
-// never waits for it: compute warps free each weight stage themselves, and
-// they wait for the reducer only if it falls 8 stages behind.
+// For every stage: waits until the 16 compute warps have posted their partial
+// sums, sums them across warps in a fixed order, writes the outputs and frees
+// the stage. At the end of a gate/up unit it runs the SwiGLU + MXFP8 epilogue
+// and publishes the tile's ready count. The compute warps never wait for it
+// except through the depth of the ring.
 template <class S>
 __device__ void reducer(const ExpertArgs &a, ExpertSmem &sm) {
   const int lane = threadIdx.x & 31;
-  int rslot = 0;
-  uint32_t rphase = 0;
+  int stage = 0;
+  uint32_t phase = 0;
   while (true) {
     int64_t waited = 0;
-    if (!__shfl_sync(0xFFFFFFFFu, mbar_wait(&sm.red_full[rslot], rphase, 16 * a.timeout_ns, &waited) ? 1 : 0, 0)) {
+    if (!__shfl_sync(0xFFFFFFFFu, mbar_wait(&sm.full[stage], phase, 16 * a.timeout_ns, &waited) ? 1 : 0, 0)) {
       if (lane == 0) {
-        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, -1, rslot, rphase, -2, waited, 0);
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, -1, stage, phase, -3, waited, 0);
         atomicExch(a.work + 1, 1u);
       }
       return;
     }
-    const uint32_t u = sm.red_unit[rslot];
-    const int s = int(sm.red_step[rslot]);
+    const uint32_t u = sm.meta_unit[stage];
+    const int s = int(sm.meta_step[stage]);
     if (u == kDone) return;
+    if (!__shfl_sync(0xFFFFFFFFu, mbar_wait(&sm.red_full[stage], phase, 16 * a.timeout_ns, &waited) ? 1 : 0, 0)) {
+      if (lane == 0) {
+        report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, u, stage, phase, -2, waited, 0);
+        atomicExch(a.work + 1, 1u);
+      }
+      return;
+    }
     const int uslot = int(u & (kUnitSlots - 1));
     const UnitMeta &m = sm.meta[uslot];
     const int np = m.n <= 1 ? 1 : 2;
     const int passes = (m.n + np - 1) / np;
     if (m.down) {
       const int64_t hrow0 = int64_t(m.block) * S::DB + int64_t(s) * S::RS_D;
-      reduce_stage<S::I>(sm, rslot, passes, np, m.n, lane, [&](int r, int tok, float v) {
+      reduce_stage<S::I>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
         a.o[int64_t(m.pairs[tok]) * S::H + hrow0 + r] = v;
       });
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.red_empty[rslot]);  // partials consumed
       if (s == S::SPU_D - 1) down_unit_done<S>(a, m, lane);
     } else {
       constexpr int HALF = S::RS_G / 2;
-      reduce_stage<S::H>(sm, rslot, passes, np, m.n, lane, [&](int r, int tok, float v) {
+      reduce_stage<S::H>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
         const int which = r < HALF ? 0 : 1;
         const int i = s * HALF + (r < HALF ? r : r - HALF);
         sm.gu[tok][which][i] = v;
       });
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.red_empty[rslot]);  // partials consumed
       if (s == S::SPU_G - 1) gate_up_epilogue<S>(a, sm, m, lane);
     }
-    if (++rslot == kRedStages) {
-      rslot = 0;
-      rphase ^= 1u;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
 }
@@ -813,11 +759,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], kConsumerWarps);
-    }
-    for (int i = 0; i < kRedStages; ++i) {
+      mbar_init(&sm.empty[i], 1);
       mbar_init(&sm.red_full[i], kConsumerWarps);
-      mbar_init(&sm.red_empty[i], 1);
     }
     fence_mbar_init();
   }
