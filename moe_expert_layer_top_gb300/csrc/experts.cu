@@ -657,17 +657,37 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
 // weighted reduction of expert outputs is fused with the shared-expert addition.
 template <class S>
 __device__ __forceinline__ void fused_combine(const ExpertArgs &a, int t, int b, int lane) {
-  const int64_t h0 = int64_t(b) * S::DB;
-  for (int h = lane; h < S::DB; h += 32) {
-    float acc = 0.0f;
-    for (int j = 0; j < a.k; ++j) {
-      const float w = __ldcg(a.topk_w + int64_t(t) * a.k + j);
-      const float v = __ldcg(a.o + (int64_t(t) * a.k + j) * S::H + h0 + h);
-      acc = j == 0 ? __fmul_rn(w, v) : __fadd_rn(acc, __fmul_rn(w, v));
+  constexpr int Q = S::DB / 32;  // outputs per lane
+  const int64_t h0 = int64_t(b) * S::DB + lane;
+  float acc[Q];
+#pragma unroll
+  for (int q = 0; q < Q; ++q) acc[q] = 0.0f;
+  // pairs in chunks of 4: all loads of a chunk are in flight together
+  for (int j0 = 0; j0 < a.k; j0 += 4) {
+    float w[4], v[4][Q];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = j0 + jj < a.k ? j0 + jj : a.k - 1;
+      w[jj] = __ldcg(a.topk_w + int64_t(t) * a.k + j);
+      const float *src = a.o + (int64_t(t) * a.k + j) * S::H + h0;
+#pragma unroll
+      for (int q = 0; q < Q; ++q) v[jj][q] = __ldcg(src + 32 * q);
     }
-    if (a.shared) acc = __fadd_rn(acc, __ldcg(a.o + (int64_t(a.T) * a.k + t) * S::H + h0 + h));
-    a.y[int64_t(t) * S::H + h0 + h] = float_to_bf16_bits(acc);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      if (j0 + jj >= a.k) break;
+#pragma unroll
+      for (int q = 0; q < Q; ++q)
+        acc[q] = (j0 + jj == 0) ? __fmul_rn(w[jj], v[jj][q]) : __fadd_rn(acc[q], __fmul_rn(w[jj], v[jj][q]));
+    }
   }
+  if (a.shared) {
+    const float *src = a.o + (int64_t(a.T) * a.k + t) * S::H + h0;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) acc[q] = __fadd_rn(acc[q], __ldcg(src + 32 * q));
+  }
+#pragma unroll
+  for (int q = 0; q < Q; ++q) a.y[int64_t(t) * S::H + h0 + 32 * q] = float_to_bf16_bits(acc[q]);
 }
 
 // After a down unit's last stage: count each of its pairs in for (token row,
