@@ -192,14 +192,18 @@ def active_experts(lg, k, shared):
 
 
 def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
-    """Times `steps` steps (L2 flushed before each, outside the events). Returns a dict."""
+    """Times `steps` steps (L2 flushed before each, outside the events), then,
+    in a second pass with the plan's kernel timing on, the expert kernel alone.
+    Kernel timing records events between the two launches, which would break
+    their programmatic-dependent-launch overlap, so the step times come from a
+    plan without it."""
     import torch
     from moe_expert_layer_top_gb300 import abi, synthetic
     from moe_expert_layer_top_gb300.layer import MoEStep, MoEWeightsMXFP8
     w = weights if wl.shared else MoEWeightsMXFP8(weights.w_gate, weights.s_gate, weights.w_up, weights.s_up,
                                                   weights.w_down, weights.s_down)
     x, lg, _, lg_np = synthetic.make_inputs(seed, wl.T, wl.H, wl.E, wl.k, wl.routing)
-    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING)
+    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     # one device status word per step: every step must finish with MOE_OK
@@ -208,7 +212,6 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
         flush_buf.zero_()
         step.forward(x, lg, y=y, d_status=st_words[i:i + 1])
     torch.cuda.synchronize()
-    step.kernel_times()  # reset the expert-kernel event log
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
@@ -218,13 +221,24 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
         ends[i].record(stream)
     torch.cuda.synchronize()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    expert_ms, launches = step.kernel_times()
     words = st_words.cpu().tolist()
     bad = [(i, w) for i, w in enumerate(words) if w != abi.MOE_OK]
     status = 0 if not bad else bad[0][1]
     if bad:
         print(f"warning: {len(bad)} of {len(words)} steps reported a device status: first {bad[0]}, "
               f"diagnostics {step.diagnostics()}", file=sys.stderr)
+    # second pass: the expert kernel's own duration (CUDA events on the launch stream)
+    kstep = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING)
+    for _ in range(max(3, warmup // 2)):
+        flush_buf.zero_()
+        kstep.forward(x, lg, y=y)
+    torch.cuda.synchronize()
+    kstep.kernel_times()
+    for _ in range(steps):
+        flush_buf.zero_()
+        kstep.forward(x, lg, y=y)
+    expert_ms, launches = kstep.kernel_times()
+    kstep.close()
     A = active_experts(lg_np, wl.k, wl.shared)
     weight_bytes = A * wl.expert_bytes
     step_bytes = weight_bytes + wl.T * wl.H * 2 + wl.T * wl.E * 4 + wl.T * wl.H * 2

@@ -336,7 +336,7 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
       if (lane == 0 && mn.valid) {
         const bool shn = mn.expert == a.E;
         const int en = shn ? 0 : mn.expert;
-        const uint64_t pn = mn.cnt > kTileRows ? pol_reuse : pol;
+        const uint64_t pn = pol_reuse;  // keep prefetched lines until the stage copies read them
         if (!mn.down) {
           const int64_t i0 = int64_t(mn.block) * 32;
           const uint8_t *wg = shn ? a.sh_w_gate : a.w_gate + int64_t(en) * S::I * S::H;
