@@ -148,12 +148,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
-// global -> L2 prefetch of `bytes` (a multiple of 16) at a 16-byte aligned address.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy) {
-  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
-               : "memory");
-}
-
 // ------------------------------------------------------------------ acquire / release on global counters
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {

@@ -328,34 +328,6 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     // steps 1 and 2 (loads in flight while the stages are issued)
     const int32_t te_far = load_te(i + 3);
     const Fetch f2 = load_rows(te_next);
-    // Weights of the next unit: start their DRAM reads into L2 now, so its
-    // stages' bulk copies hit L2. This adds bytes in flight without using
-    // shared memory.
-    {
-      const UnitMeta &mn = sm.meta[(i + 1) & (kUnitSlots - 1)];
-      if (lane == 0 && mn.valid) {
-        const bool shn = mn.expert == a.E;
-        const int en = shn ? 0 : mn.expert;
-        const uint64_t pn = pol_reuse;  // keep prefetched lines until the stage copies read them
-        if (!mn.down) {
-          const int64_t i0 = int64_t(mn.block) * 32;
-          const uint8_t *wg = shn ? a.sh_w_gate : a.w_gate + int64_t(en) * S::I * S::H;
-          const uint8_t *wu = shn ? a.sh_w_up : a.w_up + int64_t(en) * S::I * S::H;
-          const uint8_t *sg = shn ? a.sh_s_gate : a.s_gate + int64_t(en) * S::I * (S::H / kGroup);
-          const uint8_t *su = shn ? a.sh_s_up : a.s_up + int64_t(en) * S::I * (S::H / kGroup);
-          bulk_prefetch_l2(wg + i0 * S::H, 32 * S::H, pn);
-          bulk_prefetch_l2(wu + i0 * S::H, 32 * S::H, pn);
-          bulk_prefetch_l2(sg + i0 * (S::H / kGroup), 32 * (S::H / kGroup), pn);
-          bulk_prefetch_l2(su + i0 * (S::H / kGroup), 32 * (S::H / kGroup), pn);
-        } else {
-          const int64_t r0 = int64_t(mn.block) * S::DB;
-          const uint8_t *wd = shn ? a.sh_w_down : a.w_down + int64_t(en) * S::H * S::I;
-          const uint8_t *sd = shn ? a.sh_s_down : a.s_down + int64_t(en) * S::H * (S::I / kGroup);
-          bulk_prefetch_l2(wd + r0 * S::I, S::DB * S::I, pn);
-          bulk_prefetch_l2(sd + r0 * (S::I / kGroup), S::DB * (S::I / kGroup), pn);
-        }
-      }
-    }
     const bool sh = m.expert == a.E;
     const int e = sh ? 0 : m.expert;
     const int down = m.down, block = m.block;
