@@ -57,6 +57,7 @@ constexpr int kStageStride = kStageBytes + kStageScaleBytes;
 constexpr int kMaxSlots = kConsumers / 16;        // reduction slots (K = 256 uses half-warps)
 constexpr int kRedValues = 32;                    // per slot: passes x 4 rows x NP tokens
 constexpr int kUnitSlots = 8;                     // gate/up units in flight per block
+constexpr int kCombineQueue = 256;                // combine jobs a block can defer to its end
 
 // A work unit as the producer publishes it (decoded once, read by every consumer warp).
 struct UnitMeta {
@@ -81,6 +82,10 @@ struct __align__(16) ExpertSmem {
   uint32_t meta_unit[kStages];                    // unit sequence number of the stage, or kDone
   uint32_t meta_step[kStages];                    // stage index within the unit
   uint4 pf_q[2][kConsumers];                      // per-thread prefetch of the next unit's columns
+  uint32_t cq[kCombineQueue];                     // deferred combine jobs (token row << 16 | down block)
+  uint32_t cq_head;                               // jobs queued by the reducer
+  uint32_t cq_tail;                               // jobs taken by compute warps at the end
+  uint32_t cq_done;                               // the reducer has finished
 };
 static_assert(sizeof(ExpertSmem) <= 227 * 1024, "shared memory budget");
 
@@ -539,6 +544,9 @@ __device__ __forceinline__ bool wait_tile_ready(const ExpertArgs &a, int tile, u
 }
 
 template <class S>
+__device__ __forceinline__ void run_deferred_combines(const ExpertArgs &a, ExpertSmem &sm, int lane);
+
+template <class S>
 __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
   (void)n_tiles;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -567,6 +575,7 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     const int s = int(sm.meta_step[stage]);
     if (u == kDone) {
       cp_async_wait_all();
+      run_deferred_combines<S>(a, sm, lane);
       return;
     }
     const unsigned char *st = sm.stage[stage];
@@ -691,9 +700,12 @@ __device__ __forceinline__ void fused_combine(const ExpertArgs &a, int t, int b,
 }
 
 // After a down unit's last stage: count each of its pairs in for (token row,
-// block) and run the combine for the rows this unit completes.
+// block). For each row this unit completes, a combine job is queued. The 16
+// compute warps run the queue in parallel once their stream of stages ends, so
+// the combine stays off the reducer's path. If the queue is full, the reducer
+// combines the row itself.
 template <class S>
-__device__ __forceinline__ void down_unit_done(const ExpertArgs &a, const UnitMeta &m, int lane) {
+__device__ __forceinline__ void down_unit_done(const ExpertArgs &a, ExpertSmem &sm, const UnitMeta &m, int lane) {
   __threadfence();  // this unit's o stores, before the counts
   __syncwarp();
   const uint32_t target = uint32_t(a.k + a.shared);
@@ -703,10 +715,47 @@ __device__ __forceinline__ void down_unit_done(const ExpertArgs &a, const UnitMe
     uint32_t before = 0;
     if (lane == 0) before = atomicAdd(a.comb_cnt + int64_t(t) * S::NBD + m.block, 1u);
     before = __shfl_sync(0xFFFFFFFFu, before, 0);
-    if (before == target - 1) {
-      __threadfence();  // the other pairs' o stores, before the reads below
+    if (before != target - 1) continue;
+    __threadfence();  // the other pairs' o stores, before anyone reads them
+    const uint32_t head = sm.cq_head;  // only this warp writes it
+    if (head < uint32_t(kCombineQueue)) {
+      if (lane == 0) {
+        sm.cq[head] = (uint32_t(t) << 16) | uint32_t(m.block);
+        sm.cq_head = head + 1;
+      }
+      __syncwarp();
+    } else {
       fused_combine<S>(a, t, m.block, lane);
     }
+  }
+  __syncwarp();
+}
+
+// Compute warps, after their last stage: wait (bounded) for the reducer to
+// finish, then take the queued combine jobs one by one.
+template <class S>
+__device__ __forceinline__ void run_deferred_combines(const ExpertArgs &a, ExpertSmem &sm, int lane) {
+  int done = 0;
+  if (lane == 0) {
+    const WaitClock wc;
+    while (!(done = *reinterpret_cast<volatile uint32_t *>(&sm.cq_done) != 0)) {
+      if (wc.expired(16 * a.timeout_ns)) {
+        report_error(a.status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(128);
+    }
+  }
+  if (!__shfl_sync(0xFFFFFFFFu, done, 0)) return;
+  __threadfence_block();
+  const uint32_t head = *reinterpret_cast<volatile uint32_t *>(&sm.cq_head);
+  while (true) {
+    uint32_t j = 0;
+    if (lane == 0) j = atomicAdd(&sm.cq_tail, 1u);
+    j = __shfl_sync(0xFFFFFFFFu, j, 0);
+    if (j >= head) return;
+    const uint32_t job = sm.cq[j];
+    fused_combine<S>(a, int(job >> 16), int(job & 0xFFFFu), lane);
   }
 }
 
@@ -727,16 +776,25 @@ __device__ void reducer(const ExpertArgs &a, ExpertSmem &sm) {
       if (lane == 0) {
         report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, -1, stage, phase, -3, waited, 0);
         atomicExch(a.work + 1, 1u);
+        *reinterpret_cast<volatile uint32_t *>(&sm.cq_done) = 1u;
       }
       return;
     }
     const uint32_t u = sm.meta_unit[stage];
     const int s = int(sm.meta_step[stage]);
-    if (u == kDone) return;
+    if (u == kDone) {
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        *reinterpret_cast<volatile uint32_t *>(&sm.cq_done) = 1u;
+      }
+      return;
+    }
     if (!__shfl_sync(0xFFFFFFFFu, mbar_wait(&sm.red_full[stage], phase, 16 * a.timeout_ns, &waited) ? 1 : 0, 0)) {
       if (lane == 0) {
         report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagFullWait, u, stage, phase, -2, waited, 0);
         atomicExch(a.work + 1, 1u);
+        *reinterpret_cast<volatile uint32_t *>(&sm.cq_done) = 1u;
       }
       return;
     }
@@ -750,7 +808,7 @@ __device__ void reducer(const ExpertArgs &a, ExpertSmem &sm) {
         a.o[int64_t(m.pairs[tok]) * S::H + hrow0 + r] = v;
       });
       __syncwarp();
-      if (s == S::SPU_D - 1) down_unit_done<S>(a, m, lane);
+      if (s == S::SPU_D - 1) down_unit_done<S>(a, sm, m, lane);
     } else {
       constexpr int HALF = S::RS_G / 2;
       reduce_stage<S::H>(sm, stage, passes, np, m.n, lane, [&](int r, int tok, float v) {
@@ -782,6 +840,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
       mbar_init(&sm.empty[i], 1);
       mbar_init(&sm.red_full[i], kConsumerWarps);
     }
+    sm.cq_head = sm.cq_tail = sm.cq_done = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -796,6 +855,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) experts_kernel(const Expert
     reducer<S>(a, sm);
     return;
   }
+
   consumers<S>(a, sm, n_tiles);
 }
 
