@@ -166,12 +166,30 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def traffic_per_launch(algorithmic_bytes):
+EXPERT_KERNELS = {
+    # path -> (kernel, source file, committed ncu traffic summary)
+    "gemv": ("experts_kernel (persistent CUDA-core gate/up + down GEMV)", "experts.cu",
+             "experts_kernel_traffic.json"),
+    "mma": ("experts_mma_kernel (persistent tcgen05 block-scaled MXFP8 MMA)", "experts_mma.cu",
+            "experts_mma_kernel_traffic.json"),
+}
+PATH_FLAGS = {"auto": 0, "gemv": 1 << 1, "mma": 1 << 2}
+MMA_MIN_ROWS = 32  # the library's default switch between the two expert kernels
+
+
+def kernel_path(path, T):
+    if path != "auto":
+        return path
+    return "mma" if T >= MMA_MIN_ROWS else "gemv"
+
+
+def traffic_per_launch(algorithmic_bytes, path="gemv"):
     """DRAM bytes per expert-kernel launch from the committed ncu capture, scaled
     by the active weight bytes; None if the kernel source changed since then."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "experts_kernel_traffic.json")
-    src = os.path.join(ROOT, "moe_expert_layer_top_gb300", "csrc", "experts.cu")
+    _, src_name, summary = EXPERT_KERNELS[path]
+    p = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "moe_expert_layer_top_gb300", "csrc", src_name)
     try:
         with open(p) as f:
             d = json.load(f)
@@ -191,7 +209,7 @@ def active_experts(lg, k, shared):
     return len(set(ids.ravel().tolist())) + (1 if shared else 0)
 
 
-def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
+def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed, flags=0):
     """Times `steps` steps (L2 flushed before each, outside the events), then,
     in a second pass with the plan's kernel timing on, the expert kernel alone.
     Kernel timing records events between the two launches, which would break
@@ -203,7 +221,7 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
     w = weights if wl.shared else MoEWeightsMXFP8(weights.w_gate, weights.s_gate, weights.w_up, weights.s_up,
                                                   weights.w_down, weights.s_down)
     x, lg, _, lg_np = synthetic.make_inputs(seed, wl.T, wl.H, wl.E, wl.k, wl.routing)
-    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared)
+    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=flags)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     # one device status word per step: every step must finish with MOE_OK
@@ -228,7 +246,7 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed):
         print(f"warning: {len(bad)} of {len(words)} steps reported a device status: first {bad[0]}, "
               f"diagnostics {step.diagnostics()}", file=sys.stderr)
     # second pass: the expert kernel's own duration (CUDA events on the launch stream)
-    kstep = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING)
+    kstep = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING | flags)
     for _ in range(max(3, warmup // 2)):
         flush_buf.zero_()
         kstep.forward(x, lg, y=y)
@@ -329,7 +347,8 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    main = time_gpu_workload(wl, weights, args.steps, args.warmup, flush_buf, seed)
+    flags = PATH_FLAGS[args.path]
+    main = time_gpu_workload(wl, weights, args.steps, args.warmup, flush_buf, seed, flags)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -350,9 +369,10 @@ def run_gpu(args):
             if name == wl.name:
                 continue
             o = synth.WORKLOADS[name]
-            r = time_gpu_workload(o, weights, max(args.steps // 2, 5), max(args.warmup, 3), flush_buf, seed)
+            r = time_gpu_workload(o, weights, max(args.steps // 2, 5), max(args.warmup, 3), flush_buf, seed, flags)
             peak, _ = measured_peaks()
-            also[name] = {"T": o.T, "us_per_step": round(r["ms_mean"] * 1e3, 2),
+            also[name] = {"T": o.T, "expert_kernel": kernel_path(args.path, o.T),
+                          "us_per_step": round(r["ms_mean"] * 1e3, 2),
                           "us_median": round(r["ms_median"] * 1e3, 2),
                           "expert_kernel_us": round(r["expert_ms_mean"] * 1e3, 2),
                           "active_experts": r["active_experts"],
@@ -374,6 +394,7 @@ def run_gpu(args):
 
     peak, peak_kind = measured_peaks()
     achieved = main["weight_bytes"] / (exp_ms * 1e-3) / 1e9
+    path = kernel_path(args.path, wl.T)
     line = {
         "metric": "MoE step us & achieved HBM GB/s (% of roofline) at 6/24/96/384 token rows",
         "value": round(ms * 1e3, 3),
@@ -391,6 +412,7 @@ def run_gpu(args):
             "workload": f"{wl.name}: T={wl.T} token rows, H={wl.H}, E={wl.E}, top-{wl.k}, I={wl.I}, "
                         f"shared={wl.shared}, routing={wl.routing}",
             "T": wl.T, "H": wl.H, "E": wl.E, "top_k": wl.k, "I": wl.I, "shared": wl.shared,
+            "expert_kernel": path,
             "active_experts": main["active_experts"],
             "step_bytes": main["step_bytes"],
             "step_gbs": round(main["step_bytes"] / (ms * 1e-3) / 1e9, 1),
@@ -404,14 +426,14 @@ def run_gpu(args):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "experts_kernel (persistent gate/up + down)",
+            "kernel": EXPERT_KERNELS[path][0],
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic_per_launch(main["weight_bytes"]),
-            "traffic_source": "profiles/experts_kernel_traffic.json (ncu capture at 64 experts, scaled by weight bytes)",
+            "traffic": traffic_per_launch(main["weight_bytes"], path),
+            "traffic_source": f"profiles/{EXPERT_KERNELS[path][2]} (ncu capture, scaled by weight bytes)",
             "algorithmic_bytes_per_launch": main["weight_bytes"],
             "kernel_us": round(exp_ms * 1e3, 3),
         },
@@ -471,6 +493,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=["tiny", "bs1", "bs4", "bs16", "bs64"])
+    ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
+                    help="expert kernel: auto (GEMV below 32 rows, MMA from 32), or pin gemv / mma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -80,9 +80,22 @@ typedef enum {
 /* Record CUDA events around the expert kernel of every moe_forward. Read the
  * times back with moe_kernel_times. Events are recorded on the launch stream. */
 
+#define MOE_FLAG_PATH_GEMV (1u << 1)
+#define MOE_FLAG_PATH_MMA (1u << 2)
+/* Expert kernel selection. By default a step with T >= 32 rows runs the
+ * tensor-core expert kernel (block-scaled MXFP8 tcgen05 MMA: one MMA covers
+ * up to 128 token rows of an expert, so multi-tile experts stream their
+ * weights once), and a smaller step runs the CUDA-core GEMV expert kernel
+ * (8-row tiles; no tensor-core work for one or two rows). PATH_GEMV and
+ * PATH_MMA pin one kernel for every step; setting both is
+ * MOE_ERR_INVALID_ARG. Both kernels compute the same result within the fp32
+ * summation-order tolerance; routing, placement and every MXFP8 quantisation
+ * of a given input are identical. */
+
 #define MOE_FLAG_TEST_SKIP_READY (1u << 8)
 /* Host-side fault injection for tests. The gate/up units of the first placed
- * tile never publish their ready count. The down units of that tile then give
+ * tile (on the tensor-core kernel: chunk) never publish their ready count.
+ * The down units of that tile then give
  * up after wait_timeout_ns, and MOE_ERR_TIMEOUT appears in *d_status; y is
  * undefined for that step. The GPU does not fault or hang, and the next
  * moe_forward on a plan without this flag is unaffected. */
@@ -211,7 +224,8 @@ moe_status_t moe_plan_diagnostics(void *plan, int64_t *out8);
  *  - a server whose allocator has already reserved nearly all device memory;
  *  - code that must avoid the synchronisation and latency of cudaMalloc/cudaFree;
  *  - a plugin that is only handed its input and output buffers.
- * It runs the same kernels as moe_forward, with every intermediate kept in a
+ * It runs the same kernels as moe_forward (always the CUDA-core GEMV expert
+ * kernel; the path flags are ignored), with every intermediate kept in a
  * fixed device array of MOE_STATIC_SCRATCH_BYTES compiled into this library.
  * Every GPU that loads the library holds that array until the process exits.
  * There is no plan: the config and weights are passed on every call, as for

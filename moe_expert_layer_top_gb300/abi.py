@@ -23,6 +23,8 @@ MOE_ERR_TIMEOUT = 5
 MOE_ERR_DEVICE_BOUNDS = 6
 
 MOE_FLAG_TIMING = 1 << 0
+MOE_FLAG_PATH_GEMV = 1 << 1
+MOE_FLAG_PATH_MMA = 1 << 2
 MOE_FLAG_TEST_SKIP_READY = 1 << 8
 
 # Every function declared in include/moe.h.

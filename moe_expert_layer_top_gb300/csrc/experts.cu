@@ -43,6 +43,7 @@
 // whatever the tile's row count, so results do not depend on tile-mates.
 #include <stdint.h>
 
+#include "combine.cuh"
 #include "device.cuh"
 #include "internal.h"
 
@@ -657,46 +658,11 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
 }
 
 // ------------------------------------------------------------------ fused combine
-// y[t][h] for h in down block b: ((w_0*o_0 + w_1*o_1) + ...) + o_shared in
-// binary32, rank order, no contraction, then bf16. One warp runs it: the one
-// whose down unit was the last of token row t's k (+ shared) pairs to finish
-// block b. The o values of the other pairs were written by other blocks; the
-// counter atomics and the fences on both sides order them before these reads.
-// Source: "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", 2.1. The
-// weighted reduction of expert outputs is fused with the shared-expert addition.
+// y[t][h] for h in down block b, one warp: the warp whose down unit was the
+// last of token row t's k (+ shared) pairs to finish block b (combine.cuh).
 template <class S>
 __device__ __forceinline__ void fused_combine(const ExpertArgs &a, int t, int b, int lane) {
-  constexpr int Q = S::DB / 32;  // outputs per lane
-  const int64_t h0 = int64_t(b) * S::DB + lane;
-  float acc[Q];
-#pragma unroll
-  for (int q = 0; q < Q; ++q) acc[q] = 0.0f;
-  // pairs in chunks of 4: all loads of a chunk are in flight together
-  for (int j0 = 0; j0 < a.k; j0 += 4) {
-    float w[4], v[4][Q];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int j = j0 + jj < a.k ? j0 + jj : a.k - 1;
-      w[jj] = __ldcg(a.topk_w + int64_t(t) * a.k + j);
-      const float *src = a.o + (int64_t(t) * a.k + j) * S::H + h0;
-#pragma unroll
-      for (int q = 0; q < Q; ++q) v[jj][q] = __ldcg(src + 32 * q);
-    }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      if (j0 + jj >= a.k) break;
-#pragma unroll
-      for (int q = 0; q < Q; ++q)
-        acc[q] = (j0 + jj == 0) ? __fmul_rn(w[jj], v[jj][q]) : __fadd_rn(acc[q], __fmul_rn(w[jj], v[jj][q]));
-    }
-  }
-  if (a.shared) {
-    const float *src = a.o + (int64_t(a.T) * a.k + t) * S::H + h0;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) acc[q] = __fadd_rn(acc[q], __ldcg(src + 32 * q));
-  }
-#pragma unroll
-  for (int q = 0; q < Q; ++q) a.y[int64_t(t) * S::H + h0 + 32 * q] = float_to_bf16_bits(acc[q]);
+  combine_row_block<S::DB / 32>(a.o, a.topk_w, a.y, a.T, a.k, a.shared, S::H, t, int64_t(b) * S::DB, lane);
 }
 
 // After a down unit's last stage: count each of its pairs in for (token row,

@@ -1,0 +1,748 @@
+// experts_mma.cu — tensor-core expert kernel: block-scaled MXFP8 MMA (tcgen05)
+// for steps whose experts hold many token rows.
+//
+// The CUDA-core expert kernel streams an expert's weights once per 8-row tile,
+// so an expert with hundreds of rows re-reads them and spends CUDA-core FMAs
+// on every tile. Here each expert's rows are split into chunks of <= 128 rows,
+// and one MMA per 32 K columns covers a whole chunk. The weights are streamed
+// once per chunk (chunks of one expert run side by side and share the lines
+// in L2). Tensor time is small next to the weight stream, so the kernel stays
+// bound by HBM.
+//
+// Work units, in each block's order:
+//   gate/up unit (chunk c, block b): rows [64b, 64b + 64) of W_gate and of W_up
+//       as the MMA's A operand (M = 128: 64 gate rows, then 64 up rows); the
+//       chunk's token rows of x (MXFP8) as B (N = rows rounded up to 16).
+//       Epilogue: g, u -> bf16, h = bf16(silu(g) * u), h -> MXFP8 along I,
+//       one 32-group per warp. Then ready[c] is bumped.
+//   down unit (chunk c, block b): rows [128b, 128b + 128) of W_down as A; the
+//       chunk's rows of h (MXFP8) as B. It waits (bounded) until ready[c]
+//       counts every gate/up unit of c. Epilogue: o[pair][h] in fp32, then the
+//       fused combine of every (token row, block) this unit completes.
+// Static schedule: block b runs gate/up units b, b + G, ... and then down
+// units G-1-b, 2G-1-b, ... (G blocks; the reversed order evens out the
+// per-block unit counts). Every gate/up unit precedes every down unit in each
+// block's order, so a down unit only waits on gate/up units, which never
+// wait. The waits cannot form a cycle, and every wait is bounded anyway.
+//
+// Warp roles (10 warps):
+//   warp 0      TMA producer: one lane loads the A tiles (128 bytes of K x 64
+//               or 128 rows per box, 128-byte swizzle) into a 6-stage ring.
+//   warp 1      MMA issuer: one lane issues tcgen05.mma.kind::mxf8f6f4
+//               .block_scale (4 per stage, K = 32 each) into one of two TMEM
+//               accumulators and commits each stage back to the ring.
+//   warps 2-5   loaders: gather the chunk's token rows into the B ring slot
+//               with cp.async in the 128-byte swizzled K-major layout, and
+//               write the stage's UE8M0 scales of A and B into TMEM.
+//   warps 6-9   epilogue: read the accumulator (tcgen05.ld), run the unit's
+//               epilogue, and hand the accumulator back to the MMA issuer.
+//
+// Pages followed:
+// - "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", 2.1: group-32
+//   FP8 weights and scales reorganised for Blackwell MXFP8 (here the canonical
+//   K-major layout feeds the block-scaled MMA directly, with no copy), and
+//   the reduction fused with the MXFP8 quantisation of its output.
+// - Same page, 3.1: SwiGLU with the original intermediate rounding.
+// - "FlyDSL Mono Kernels for High-Interactivity LLM Serving in ATOM",
+//   "MiniMax-M3: Connecting Attention and Experts": persistent blocks, the
+//   down weights loaded before h is ready, and tagged ready counters.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "combine.cuh"
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kMStages = 6;                 // ring depth
+constexpr int kKC = 128;                    // bytes (E4M3 values) of K per stage: 4 MMAs of K = 32
+constexpr int kBM = 128;                    // MMA M (weight rows per unit)
+constexpr int kABytes = kBM * kKC;          // 16 KB
+constexpr int kBBytes = kChunkRows * kKC;   // 16 KB
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpLoad = 2, kWarpEpi = 6, kMWarps = 10;
+constexpr int kMThreads = kMWarps * 32;
+constexpr int kLoaders = 128;               // threads of the loader warps
+constexpr int kEpiThreads = 128;            // threads of the epilogue warps
+constexpr int kLag = 3;                     // loader: stages of copies kept in flight
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 128;          // one fp32 accumulator: N <= 128 columns
+constexpr uint32_t kScaleCol0 = 2 * kAccCols;
+constexpr uint32_t kScaleSlotCols = 32;     // per stage: SFA at +0 (4 columns), SFB at +16 (4 columns)
+constexpr int kBarLoad = 1, kBarEpi = 2, kBarGate = 3;  // named barriers (0 is __syncthreads)
+static_assert(kScaleCol0 + kMStages * kScaleSlotCols <= kTmemCols, "TMEM budget");
+static_assert(kLag < kMStages, "loader lag below the ring depth");
+static_assert(kChunkRows == 128 && kMmaDownRows == kBM, "unit geometry");
+
+struct MmaSmem {
+  uint8_t a[kMStages][kABytes];       // weight tiles, 128-byte swizzled K-major (TMA)
+  uint8_t b[kMStages][kBBytes];       // token-row tiles, same layout (cp.async)
+  uint32_t sfa[kMStages][kBM];        // per weight row: the stage's 4 UE8M0 codes (one per 32 K)
+  uint32_t sfb[kMStages][kChunkRows]; // per token row: the same
+  uint16_t xchg[2][16][64];           // bf16 u of one 16-column slice, [column][i]
+  uint32_t jobs[kChunkRows];          // token rows whose combine a down unit completed
+  uint64_t full_a[kMStages];          // A landed (TMA bytes)
+  uint64_t full_b[kMStages];          // B and the scales in place (128 loader arrivals)
+  uint64_t empty[kMStages];           // the stage's MMAs are done (tcgen05.commit)
+  uint64_t acc_full[2];               // accumulator complete (tcgen05.commit)
+  uint64_t acc_empty[2];              // accumulator read out (128 epilogue arrivals)
+  uint64_t mma_done;                  // every MMA of the block finished (before TMEM is freed)
+  uint32_t tmem_base;
+  uint32_t n_jobs;
+};
+constexpr size_t kMmaSmemBytes = sizeof(MmaSmem) + 1024;  // + alignment of the ring to 1024 bytes
+static_assert(kMmaSmemBytes <= 227 * 1024, "shared memory budget");
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// 16-byte copy global -> shared through L2; src_bytes = 0 writes 16 zero bytes.
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// 4-byte copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async4_zfill(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Generic-proxy writes of this thread (cp.async) before later async-proxy reads (tcgen05.mma).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Barrier over n threads that also returns the AND of v over them. Every
+// control decision taken by a group of warps goes through one, so the group
+// always takes the same path through its barriers.
+__device__ __forceinline__ int bar_and(int id, int n, int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v), "r"(id), "r"(n)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart, start address 16-byte granular.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);  // start address
+  d |= uint64_t(1) << 16;                 // leading byte offset (unused with a 128-byte swizzle)
+  d |= uint64_t(1024 >> 4) << 32;         // stride byte offset: 8 rows x 128 bytes
+  d |= uint64_t(1) << 46;                 // descriptor version
+  d |= uint64_t(2) << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// D (+)= (A * SFA) x (B * SFB)^T for K = 32; sf_id picks the byte of the scale words.
+__device__ __forceinline__ void mma_mxf8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of the warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ units and schedule
+
+struct MUnit {
+  int down;    // 0: gate/up, 1: down
+  int chunk;   // index into chunk_list
+  int blk;     // 64-row block of I (gate/up) or 128-row block of H (down)
+  int e;       // expert (E: the shared expert)
+  int start;   // first rank of the chunk within the expert's rows
+  int n;       // token rows of the chunk (1..128)
+  int npad;    // n rounded up to 16 (the MMA's N)
+  int nch;     // chunks of the expert
+};
+
+// An expert with cnt rows is split into ceil(cnt/128) chunks of nearly equal size.
+__device__ __forceinline__ MUnit decode_unit(const ExpertArgs &a, int u, int n_chunks, int mbg, int hbd) {
+  MUnit m;
+  const int ng = n_chunks * mbg;
+  if (u < ng) {
+    m.down = 0;
+    m.chunk = u / mbg;
+    m.blk = u % mbg;
+  } else {
+    u -= ng;
+    m.down = 1;
+    m.chunk = u / hbd;
+    m.blk = u % hbd;
+  }
+  const int ent = __ldcg(a.chunk_list + m.chunk);
+  m.e = ent >> 16;
+  const int c = ent & 0xFFFF;
+  const int cnt = __ldcg(a.counts + m.e);
+  m.nch = (cnt + kChunkRows - 1) / kChunkRows;
+  const int cs = (cnt + m.nch - 1) / m.nch;
+  m.start = c * cs;
+  m.n = min(cs, cnt - m.start);
+  m.npad = (m.n + 15) & ~15;
+  return m;
+}
+
+struct Sched {
+  int b, G, NG, ND, ng;
+  __device__ Sched(int n_chunks, int mbg, int hbd)
+      : b(blockIdx.x), G(gridDim.x), NG(n_chunks * mbg), ND(n_chunks * hbd) {
+    ng = b < NG ? (NG - 1 - b) / G + 1 : 0;
+  }
+  // The i-th unit of this block, or -1 past its end.
+  __device__ __forceinline__ int unit(int i) const {
+    if (i < ng) return b + i * G;
+    const int d = (G - 1 - b) + (i - ng) * G;
+    return d < ND ? NG + d : -1;
+  }
+};
+
+__device__ __forceinline__ bool aborted(const ExpertArgs &a) { return ld_volatile(a.work + 1) != 0; }
+
+__device__ __forceinline__ void fail(const ExpertArgs &a, int64_t site, int64_t unit, int64_t where, int64_t seen,
+                                     int64_t expected, int64_t ns) {
+  report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, site, unit, where, seen, expected, ns, 0);
+  atomicExch(a.work + 1, 1u);
+}
+
+// ------------------------------------------------------------------ TMA producer (one lane)
+
+__device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, MmaSmem &sm, const Sched &sc, int n_chunks,
+                             int mbg, int hbd) {
+  const uint64_t pol_first = l2_evict_first_policy(), pol_normal = l2_evict_normal_policy();
+  uint32_t g = 0;  // stages issued
+  for (int i = 0;; ++i) {
+    const int u = sc.unit(i);
+    if (u < 0 || aborted(a)) break;
+    const MUnit m = decode_unit(a, u, n_chunks, mbg, hbd);
+    const bool sh = m.e == a.E;
+    // the chunks of a multi-chunk expert read the same weights at about the same time
+    const uint64_t pol = m.nch > 1 ? pol_normal : pol_first;
+    const int kcs = (m.down ? a.I : a.H) / kKC;
+    bool ok = true;
+    for (int kc = 0; kc < kcs; ++kc) {
+      const int s = int(g % kMStages);
+      const uint32_t ph = (g / kMStages) & 1u;
+      int64_t waited = 0;
+      if (!mbar_wait(&sm.empty[s], ph ^ 1u, a.timeout_ns, &waited)) {
+        fail(a, kDiagEmptyWait, u, s, kc, -10, waited);
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&sm.full_a[s], kABytes);
+      if (!m.down) {
+        const int y = (sh ? 0 : m.e * a.I) + m.blk * 64;
+        tma_load_2d(sm.a[s], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full_a[s], pol);
+        tma_load_2d(sm.a[s] + kABytes / 2, sh ? &maps.sh_up : &maps.up, kc * kKC, y, &sm.full_a[s], pol);
+      } else {
+        const int y = (sh ? 0 : m.e * a.H) + m.blk * kBM;
+        tma_load_2d(sm.a[s], sh ? &maps.sh_down : &maps.down, kc * kKC, y, &sm.full_a[s], pol);
+      }
+      ++g;
+    }
+    if (!ok) break;
+  }
+  // No copy may still be in flight when the block exits: wait for the last
+  // load of every slot (already complete unless the MMA side stopped early).
+  const uint32_t last = g < uint32_t(kMStages) ? g : uint32_t(kMStages);
+  for (uint32_t j = 1; j <= last; ++j) {
+    const uint32_t gg = g - j;
+    mbar_wait(&sm.full_a[gg % kMStages], (gg / kMStages) & 1u, a.timeout_ns);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer (one lane)
+
+__device__ void mma_issuer(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, const Sched &sc, int n_chunks, int mbg,
+                           int hbd) {
+  uint32_t g = 0, nu = 0;  // stages consumed, units done
+  for (int i = 0;; ++i) {
+    const int u = sc.unit(i);
+    if (u < 0 || aborted(a)) break;
+    const MUnit m = decode_unit(a, u, n_chunks, mbg, hbd);
+    const int acc = int(nu & 1u);
+    const uint32_t aph = (nu >> 1) & 1u;
+    int64_t waited = 0;
+    if (!mbar_wait(&sm.acc_empty[acc], aph ^ 1u, a.timeout_ns, &waited)) {
+      fail(a, kDiagEmptyWait, u, acc, -1, -11, waited);
+      break;
+    }
+    tmem_fence_after();
+    const uint32_t d = tmem + uint32_t(acc) * kAccCols;
+    // kind::mxf8f6f4, A and B E4M3, K-major, UE8M0 scales, N = npad, M = 128
+    const uint32_t idesc = (1u << 23) | (uint32_t(m.npad >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+    const int kcs = (m.down ? a.I : a.H) / kKC;
+    bool ok = true;
+    for (int kc = 0; kc < kcs; ++kc) {
+      const int s = int(g % kMStages);
+      const uint32_t ph = (g / kMStages) & 1u;
+      if (!mbar_wait(&sm.full_a[s], ph, a.timeout_ns, &waited)) {
+        fail(a, kDiagFullWait, u, s, kc, -12, waited);
+        ok = false;
+        break;
+      }
+      if (!mbar_wait(&sm.full_b[s], ph, a.timeout_ns, &waited)) {
+        fail(a, kDiagFullWait, u, s, kc, -13, waited);
+        ok = false;
+        break;
+      }
+      tmem_fence_after();
+      const uint32_t sfa = tmem + kScaleCol0 + uint32_t(s) * kScaleSlotCols, sfb = sfa + 16;
+      const uint64_t adesc = sw128_desc(smem_u32(sm.a[s])), bdesc = sw128_desc(smem_u32(sm.b[s]));
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        // +32 bytes of K per step: +2 in the descriptor's 16-byte start-address field
+        mma_mxf8(d, adesc + uint64_t(2 * k4), bdesc + uint64_t(2 * k4),
+                 idesc | (uint32_t(k4) << 4) | (uint32_t(k4) << 29), sfa, sfb, (kc | k4) != 0 ? 1u : 0u);
+      }
+      mma_commit(&sm.empty[s]);
+      ++g;
+    }
+    if (!ok) break;
+    mma_commit(&sm.acc_full[acc]);
+    ++nu;
+  }
+  // every MMA issued must finish before TMEM is freed
+  mma_commit(&sm.mma_done);
+  mbar_wait(&sm.mma_done, 0, a.timeout_ns);
+}
+
+// ------------------------------------------------------------------ loaders (warps 2-5)
+// Thread tau (0..127) copies 16-byte column c8 = tau % 8 of rows tau/8 + 16 i of
+// the B tile, the scale word of weight row tau and that of token row tau. Then,
+// for its warp's TMEM lane quadrant, it writes the stage's scale words: lane l
+// of column c holds row l + 32 c (the same words in each quadrant).
+
+struct LoaderRows {
+  const uint8_t *b[8];  // row i: token (pair) row r = tau/8 + 16 i of the chunk, its K-major codes
+  const uint8_t *sfa;   // scale row of weight row tau
+  const uint8_t *sfb;   // scale row of token row tau (or NULL past the chunk)
+};
+
+__device__ __forceinline__ LoaderRows loader_rows(const ExpertArgs &a, const MUnit &m, int tau) {
+  LoaderRows lr;
+  const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
+  const int64_t tk = int64_t(a.T) * a.k;
+  const int r0 = tau >> 3;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0 + 16 * i;
+    lr.b[i] = nullptr;
+    if (r < m.n) {
+      const int64_t p = __ldcg(rows + r);
+      lr.b[i] = m.down ? a.hq + p * a.I : a.xq + (p < tk ? p / a.k : p - tk) * a.H;
+    }
+  }
+  lr.sfb = nullptr;
+  if (tau < m.n) {
+    const int64_t p = __ldcg(rows + tau);
+    lr.sfb = m.down ? a.hs + p * (a.I / kGroup) : a.xs + (p < tk ? p / a.k : p - tk) * (a.H / kGroup);
+  }
+  const bool sh = m.e == a.E;
+  if (!m.down) {
+    const int64_t row = int64_t(m.blk) * 64 + (tau & 63);
+    const uint8_t *base = tau < 64 ? (sh ? a.sh_s_gate : a.s_gate) : (sh ? a.sh_s_up : a.s_up);
+    lr.sfa = base + ((sh ? 0 : int64_t(m.e) * a.I) + row) * (a.H / kGroup);
+  } else {
+    const int64_t row = int64_t(m.blk) * kBM + tau;
+    lr.sfa = (sh ? a.sh_s_down : a.s_down) + ((sh ? 0 : int64_t(m.e) * a.H) + row) * (a.I / kGroup);
+  }
+  return lr;
+}
+
+// Issue the copies of stage slot s for K chunk kc.
+__device__ __forceinline__ void loader_issue(MmaSmem &sm, const MUnit &m, const LoaderRows &lr, int s, int kc,
+                                             int tau, const void *zero_src) {
+  const int c8 = tau & 7, r0 = tau >> 3;
+  uint8_t *bs = sm.b[s];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0 + 16 * i;
+    if (r < m.npad) {
+      const bool v = lr.b[i] != nullptr;
+      cp_async16_zfill(bs + r * kKC + ((c8 ^ (r & 7)) << 4), v ? lr.b[i] + kc * kKC + c8 * 16 : zero_src,
+                       v ? 16u : 0u);
+    }
+  }
+  cp_async4_zfill(&sm.sfa[s][tau], lr.sfa + kc * 4, 4u);
+  if (tau < m.npad) cp_async4_zfill(&sm.sfb[s][tau], lr.sfb ? lr.sfb + kc * 4 : zero_src, lr.sfb ? 4u : 0u);
+}
+
+// After a loader barrier: the scale words of stage slot s into TMEM, then this
+// thread's arrival on full_b[s].
+__device__ __forceinline__ void loader_signal(MmaSmem &sm, uint32_t tmem, int s, int q, int lane) {
+  uint32_t va[4], vb[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    va[c] = sm.sfa[s][lane + 32 * c];
+    vb[c] = sm.sfb[s][lane + 32 * c];
+  }
+  const uint32_t t = tmem + (uint32_t(32 * q) << 16) + kScaleCol0 + uint32_t(s) * kScaleSlotCols;
+  tmem_st4(t, va);
+  tmem_st4(t + 16, vb);
+  tmem_wait_st();
+  tmem_fence_before();
+  mbar_arrive(&sm.full_b[s]);
+}
+
+__device__ __forceinline__ int wait_chunk_ready(const ExpertArgs &a, int chunk, uint32_t target, int u) {
+  const WaitClock wc;
+  uint32_t seen;
+  while ((seen = ld_acquire_gpu(a.ready + chunk)) < target) {
+    if (wc.expired(a.timeout_ns)) {
+      report_diag(a.status, a.diag, MOE_ERR_TIMEOUT, kDiagReadyWait, u, chunk, seen, target, wc.ns(), wc.cycles());
+      atomicExch(a.work + 1, 1u);
+      return 0;
+    }
+    __nanosleep(128);
+  }
+  return 1;
+}
+
+__device__ void mma_loaders(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, const Sched &sc, int n_chunks, int mbg,
+                            int hbd) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3;
+  const int tau = (warp - kWarpLoad) * 32 + lane;
+  const void *zero_src = a.xq;  // any valid address: zero-byte copies read nothing
+  uint32_t g = 0, gc = 0;       // stages issued, stages signalled
+  bool alive = true;
+  for (int i = 0; alive; ++i) {
+    const int u = sc.unit(i);
+    if (u < 0) break;
+    const MUnit m = decode_unit(a, u, n_chunks, mbg, hbd);
+    int ok = !aborted(a);
+    if (m.down && !bar_and(kBarLoad, kLoaders, ld_acquire_gpu(a.ready + m.chunk) >= uint32_t(mbg))) {
+      // h of the chunk is not complete yet. Every issued stage reaches the MMA
+      // before this block waits on others.
+      cp_async_wait<0>();
+      fence_proxy_async();
+      named_bar(kBarLoad, kLoaders);
+      for (; gc < g; ++gc) loader_signal(sm, tmem, int(gc % kMStages), q, lane);
+      if (ok) ok = wait_chunk_ready(a, m.chunk, uint32_t(mbg), u);
+    }
+    if (!bar_and(kBarLoad, kLoaders, ok)) {
+      alive = false;
+      break;
+    }
+    const LoaderRows lr = loader_rows(a, m, tau);
+    const int kcs = (m.down ? a.I : a.H) / kKC;
+    for (int kc = 0; kc < kcs; ++kc) {
+      const int s = int(g % kMStages);
+      const uint32_t ph = (g / kMStages) & 1u;
+      int64_t waited = 0;
+      int ok2 = mbar_wait(&sm.empty[s], ph ^ 1u, a.timeout_ns, &waited) ? 1 : 0;
+      if (ok2) loader_issue(sm, m, lr, s, kc, tau, zero_src);
+      else fail(a, kDiagEmptyWait, u, s, kc, -14, waited);
+      cp_async_commit();
+      ++g;
+      const bool due = g - gc > uint32_t(kLag);
+      if (due) {
+        cp_async_wait<kLag>();  // this thread's copies of stage gc have landed
+        fence_proxy_async();
+      }
+      if (!bar_and(kBarLoad, kLoaders, ok2)) {
+        alive = false;
+        break;
+      }
+      if (due) {
+        loader_signal(sm, tmem, int(gc % kMStages), q, lane);
+        ++gc;
+      }
+    }
+  }
+  cp_async_wait<0>();
+  fence_proxy_async();
+  named_bar(kBarLoad, kLoaders);
+  if (alive)
+    for (; gc < g; ++gc) loader_signal(sm, tmem, int(gc % kMStages), q, lane);
+}
+
+// ------------------------------------------------------------------ epilogue (warps 6-9)
+
+__device__ void mma_epilogue(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, const Sched &sc, int n_chunks, int mbg,
+                             int hbd) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ew = warp - kWarpEpi;
+  const int et = ew * 32 + lane;
+  const int64_t tk = int64_t(a.T) * a.k;
+  const uint32_t target = uint32_t(a.k + a.shared);
+  uint32_t nu = 0, xc = 0;  // units done, gate/up column slices done
+  for (int i = 0;; ++i) {
+    const int u = sc.unit(i);
+    if (u < 0) break;
+    const MUnit m = decode_unit(a, u, n_chunks, mbg, hbd);
+    const int acc = int(nu & 1u);
+    const uint32_t aph = (nu >> 1) & 1u;
+    int ok = !aborted(a);
+    if (ok) {
+      int64_t waited = 0;
+      ok = mbar_wait(&sm.acc_full[acc], aph, a.timeout_ns, &waited) ? 1 : 0;
+      if (!ok) fail(a, kDiagFullWait, u, acc, -1, -15, waited);
+    }
+    if (!bar_and(kBarEpi, kEpiThreads, ok)) break;
+    tmem_fence_after();
+    const uint32_t ta = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc) * kAccCols;
+    const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
+    const int slices = m.npad / 16;
+    if (!m.down) {
+      // lanes of quadrants 0, 1 hold gate rows 64b + 32q + lane; quadrants 2, 3 the up rows
+      for (int j = 0; j < slices; ++j, ++xc) {
+        float v[16];
+        tmem_ld16(ta + uint32_t(16 * j), v);
+        int pr = -1;
+        if (lane < 16 && 16 * j + lane < m.n) pr = __ldcg(rows + 16 * j + lane);
+        uint16_t(*xb)[64] = sm.xchg[xc & 1u];
+        if (q >= 2) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) xb[c][32 * (q - 2) + lane] = float_to_bf16_bits(v[c]);
+        }
+        named_bar(kBarEpi, kEpiThreads);
+        if (q < 2) {
+          const int64_t col = int64_t(m.blk) * 64 + 32 * q + lane;
+#pragma unroll 4
+          for (int c = 0; c < 16; ++c) {
+            const int p = __shfl_sync(0xFFFFFFFFu, pr, c);
+            if (p < 0) continue;  // the same for the whole warp
+            const float gb = bf16_bits_to_float(float_to_bf16_bits(v[c]));
+            const float ub = bf16_bits_to_float(xb[c][32 * q + lane]);
+            const float silu = gb / (1.0f + expf(-gb));
+            const uint16_t hb = float_to_bf16_bits(silu * ub);
+            const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, uint32_t(hb) & 0x7FFFu);
+            const uint32_t code = mx_scale_code(bf16_bits_to_float(uint16_t(amax)));
+            a.hq[int64_t(p) * a.I + col] = float_to_e4m3(mx_unscale(bf16_bits_to_float(hb), code));
+            if (lane == 0) a.hs[int64_t(p) * (a.I / kGroup) + m.blk * 2 + q] = uint8_t(code);
+            if (a.h_bf16) a.h_bf16[int64_t(p) * a.I + col] = hb;
+          }
+        }
+      }
+      tmem_fence_before();
+      mbar_arrive(&sm.acc_empty[acc]);
+      if (q < 2) {
+        __threadfence();  // this unit's h stores, before the ready count
+        named_bar(kBarGate, 64);
+        if (q == 0 && lane == 0 && m.chunk != a.skip_ready_tile) red_release_gpu_add(a.ready + m.chunk, 1u);
+      }
+    } else {
+      const int64_t h = int64_t(m.blk) * kBM + 32 * q + lane;
+      for (int j = 0; j < slices; ++j) {
+        float v[16];
+        tmem_ld16(ta + uint32_t(16 * j), v);
+        int pr = -1;
+        if (lane < 16 && 16 * j + lane < m.n) pr = __ldcg(rows + 16 * j + lane);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int p = __shfl_sync(0xFFFFFFFFu, pr, c);
+          if (p >= 0) a.o[int64_t(p) * a.H + h] = v[c];
+        }
+      }
+      tmem_fence_before();
+      mbar_arrive(&sm.acc_empty[acc]);
+      // Count each pair in for (token row, block); the last of a row's k (+ shared)
+      // pairs queues the row's combine (threadfence pattern: stores, fence, barrier, count).
+      __threadfence();
+      named_bar(kBarEpi, kEpiThreads);
+      if (et < m.n) {
+        const int64_t p = __ldcg(rows + et);
+        const int t = int(p < tk ? p / a.k : p - tk);
+        if (atomicAdd(a.comb_cnt + int64_t(t) * hbd + m.blk, 1u) == target - 1u) {
+          const uint32_t idx = atomicAdd(&sm.n_jobs, 1u);
+          sm.jobs[idx] = uint32_t(t);
+        }
+      }
+      named_bar(kBarEpi, kEpiThreads);
+      const uint32_t nj = *reinterpret_cast<volatile uint32_t *>(&sm.n_jobs);
+      if (nj) {
+        __threadfence();  // the other pairs' o stores, before these reads
+        for (uint32_t jj = uint32_t(ew); jj < nj; jj += 4)
+          combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, a.T, a.k, a.shared, a.H, int(sm.jobs[jj]),
+                                      int64_t(m.blk) * kBM, lane);
+      }
+      named_bar(kBarEpi, kEpiThreads);
+      if (et == 0) sm.n_jobs = 0;
+    }
+    ++nu;
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_constant__ MmaMaps maps,
+                                                                   const ExpertArgs a) {
+  extern __shared__ unsigned char mma_smem_raw[];
+  MmaSmem &sm = *reinterpret_cast<MmaSmem *>((reinterpret_cast<uintptr_t>(mma_smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMStages; ++i) {
+      mbar_init(&sm.full_a[i], 1);
+      mbar_init(&sm.full_b[i], kLoaders);
+      mbar_init(&sm.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.acc_full[i], 1);
+      mbar_init(&sm.acc_empty[i], kEpiThreads);
+    }
+    mbar_init(&sm.mma_done, 1);
+    sm.n_jobs = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  // Everything below reads the router's outputs.
+  pdl_wait_primary();
+  const int n_chunks = __ldcg(a.n_chunks);
+  const int mbg = a.I / 64, hbd = a.H / kBM;
+  const Sched sc(n_chunks, mbg, hbd);
+  if (warp == kWarpTma) {
+    if (lane == 0) mma_producer(maps, a, sm, sc, n_chunks, mbg, hbd);
+  } else if (warp == kWarpMma) {
+    if (lane == 0) mma_issuer(a, sm, tmem, sc, n_chunks, mbg, hbd);
+  } else if (warp < kWarpEpi) {
+    mma_loaders(a, sm, tmem, sc, n_chunks, mbg, hbd);
+  } else {
+    mma_epilogue(a, sm, tmem, sc, n_chunks, mbg, hbd);
+  }
+  __syncwarp();
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  if (warp == kWarpMma)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// rows x k_bytes uint8 matrix, row-major; boxes of 128 bytes x box_rows, 128-byte swizzle.
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map, const void *base, uint64_t k_bytes,
+                 uint64_t rows, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {k_bytes, rows};
+  const cuuint64_t strides[1] = {k_bytes};
+  const cuuint32_t box[2] = {uint32_t(kKC), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// K chunks of 128 bytes, 64-row gate/up blocks, 128-row down blocks.
+bool experts_mma_shape_supported(int H, int I) {
+  return H >= 128 && I >= 128 && H % 128 == 0 && I % 128 == 0 && H <= 65535 * 32 && I <= 65535 * 32;
+}
+
+bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *maps) {
+  memset(maps, 0, sizeof(MmaMaps));
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const uint64_t H = uint64_t(c.hidden), I = uint64_t(c.intermediate), E = uint64_t(c.num_experts);
+  bool ok = encode_rows(enc, &maps->gate, w.w_gate, H, E * I, 64) && encode_rows(enc, &maps->up, w.w_up, H, E * I, 64) &&
+            encode_rows(enc, &maps->down, w.w_down, I, E * H, kBM);
+  if (ok && c.num_shared)
+    ok = encode_rows(enc, &maps->sh_gate, w.sh_w_gate, H, I, 64) && encode_rows(enc, &maps->sh_up, w.sh_w_up, H, I, 64) &&
+         encode_rows(enc, &maps->sh_down, w.sh_w_down, I, H, kBM);
+  return ok;
+}
+
+size_t experts_mma_smem_bytes() { return kMmaSmemBytes; }
+
+cudaError_t prepare_experts_mma() {
+  return cudaFuncSetAttribute(experts_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMmaSmemBytes));
+}
+
+cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMThreads);
+  cfg.dynamicSmemBytes = kMmaSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, experts_mma_kernel, maps, a);
+}
+
+}  // namespace moe

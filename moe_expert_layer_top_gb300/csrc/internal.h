@@ -1,6 +1,7 @@
 // internal.h — plan layout and kernel launchers shared by the .cu files of the library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,6 +18,9 @@ constexpr int kStages = 5;              // pipeline depth
 constexpr int kRouteThreads = 1024;     // route kernel: block 0 (router + placement)
 constexpr int kQuantThreads = 256;      // route kernel: x-quantisation blocks (one group per thread)
 constexpr int kMaxTimedCalls = 4096;
+constexpr int kChunkRows = 128;         // tensor-core expert kernel: token rows per chunk (MMA N <= 128)
+constexpr int kMmaDownRows = 128;       // tensor-core expert kernel: W_down rows per down unit
+constexpr int kMmaMinRowsDefault = 32;  // steps with at least this many rows take the tensor-core kernel
 
 // Device scratch and schedule of one plan (all sized for max_rows).
 struct Scratch {
@@ -28,8 +32,10 @@ struct Scratch {
   int32_t *rows_of;     // [E + 1][Tmax] pair ids in rank order
   int32_t *tile_list;   // [n_tiles_max] (expert << 16) | tile
   int32_t *n_tiles;     // [1]
-  uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile
-  uint32_t *comb_cnt;   // [Tmax][H / DB] down blocks of a token row finished (fused combine)
+  int32_t *chunk_list;  // [n_tiles_max] (expert << 16) | chunk, chunks of <= kChunkRows rows
+  int32_t *n_chunks;    // [1]
+  uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile (per chunk on the tensor-core path)
+  uint32_t *comb_cnt;   // [Tmax][down blocks] down blocks of a token row finished (fused combine)
   uint32_t *work;       // [2] unit counter, abort flag
   int32_t *status;      // [1] plan-owned status word
   int64_t *diag;        // [8] first device-side error of the last step (site, unit, tile, ...)
@@ -43,6 +49,14 @@ struct Scratch {
   void *y_dev;
 };
 
+// TMA tensor maps over the caller's weights (canonical layout, 128-byte swizzle),
+// for the tensor-core expert kernel. Boxes: 128 bytes of K x 64 rows (gate, up)
+// or x 128 rows (down).
+struct MmaMaps {
+  CUtensorMap gate, up, down;           // rows: E*I, E*I, E*H
+  CUtensorMap sh_gate, sh_up, sh_down;  // shared expert (zero when absent)
+};
+
 struct Plan {
   moe_config_t cfg;
   moe_weights_t w;
@@ -52,6 +66,8 @@ struct Plan {
   int n_tiles_max;       // upper bound on tiles in a step
   int64_t pairs_max;     // P for T = max_rows
   int64_t timeout_ns;
+  int mma_min_rows;      // steps with T >= this take the tensor-core expert kernel
+  MmaMaps maps;
   Scratch s;
   void *arena;           // single device allocation backing Scratch
   size_t arena_bytes;
@@ -74,6 +90,8 @@ struct RouteArgs {
   int32_t *rows_of;
   int32_t *tile_list;
   int32_t *n_tiles;
+  int32_t *chunk_list;  // NULL: no chunk list (the GEMV expert kernel only)
+  int32_t *n_chunks;
   uint32_t *ready;
   int n_tiles_max;
   uint32_t *comb_cnt;
@@ -92,6 +110,8 @@ struct ExpertArgs {
   const int32_t *rows_of;
   const int32_t *tile_list;
   const int32_t *n_tiles;
+  const int32_t *chunk_list;  // tensor-core kernel: chunks of <= kChunkRows rows per expert
+  const int32_t *n_chunks;
   const uint8_t *xq, *xs;
   uint8_t *hq, *hs;
   uint16_t *h_bf16;  // NULL unless the h tap is requested
@@ -118,5 +138,11 @@ int experts_down_blocks(int H, int I);  // H / DB: down units per tile
 bool experts_shape_supported(int H, int I);
 moe_status_t guard_host(const moe_config_t &c, const moe_weights_t &w);
 size_t experts_smem_bytes();
+// Tensor-core expert kernel (tcgen05 block-scaled MXFP8 MMA).
+bool experts_mma_shape_supported(int H, int I);
+bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *maps);
+cudaError_t prepare_experts_mma();
+cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaStream_t st);
+size_t experts_mma_smem_bytes();
 
 }  // namespace moe

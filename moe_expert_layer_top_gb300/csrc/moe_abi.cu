@@ -10,8 +10,11 @@
 //   across calls to avoid re-initialisation.
 // - Runtime enqueues two kernels:
 //     1. route + place + quantise x;
-//     2. the persistent expert kernel (gate/up, down and the fused combine),
-//        launched with Programmatic Dependent Launch.
+//     2. a persistent expert kernel (gate/up, down and the fused combine),
+//        launched with Programmatic Dependent Launch. Steps with fewer rows
+//        than plan->mma_min_rows take the CUDA-core GEMV kernel
+//        (experts.cu); larger ones take the tensor-core kernel
+//        (experts_mma.cu). MOE_FLAG_PATH_GEMV / MOE_FLAG_PATH_MMA pin one.
 //   It allocates nothing and does not synchronise.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -39,10 +42,12 @@ moe_status_t guard_config(const moe_config_t &c) {
   if (c.hidden <= 0 || c.intermediate <= 0 || c.num_experts <= 0 || c.top_k <= 0 || c.max_rows <= 0)
     return MOE_ERR_INVALID_ARG;
   if (c.num_shared != 0 && c.num_shared != 1) return MOE_ERR_INVALID_ARG;
+  if ((c.flags & MOE_FLAG_PATH_GEMV) && (c.flags & MOE_FLAG_PATH_MMA)) return MOE_ERR_INVALID_ARG;
   if (c.top_k > c.num_experts) return MOE_ERR_INVALID_ARG;
   if (c.hidden % 32 || c.intermediate % 32) return MOE_ERR_UNSUPPORTED;
   if (!is_pow2(c.hidden) || !is_pow2(c.intermediate)) return MOE_ERR_UNSUPPORTED;
   if (!experts_shape_supported(c.hidden, c.intermediate)) return MOE_ERR_UNSUPPORTED;
+  if (!experts_mma_shape_supported(c.hidden, c.intermediate)) return MOE_ERR_UNSUPPORTED;
   if (c.num_experts + c.num_shared > kRouteThreads) return MOE_ERR_UNSUPPORTED;
   if (c.top_k > 32) return MOE_ERR_UNSUPPORTED;
   if (c.max_rows > 4096) return MOE_ERR_UNSUPPORTED;
@@ -173,6 +178,7 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   p->device = dev;
   p->num_sms = sms;
   p->timeout_ns = c.wait_timeout_ns > 0 ? c.wait_timeout_ns : 200000000LL;
+  p->mma_min_rows = (c.flags & MOE_FLAG_PATH_GEMV) ? 0x7FFFFFFF : (c.flags & MOE_FLAG_PATH_MMA) ? 1 : kMmaMinRowsDefault;
   const int Tm = c.max_rows, E = c.num_experts, k = c.top_k, H = c.hidden, I = c.intermediate;
   p->words = (Tm + 31) / 32;
   const int64_t pairs_routed = int64_t(Tm) * k;
@@ -190,8 +196,10 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   const size_t o_bm = take(size_t(E) * p->words * 4), o_cnt = take(size_t(E + 1) * 4);
   const size_t o_slot = take(pairs_routed * 4), o_rows = take(size_t(E + 1) * Tm * 4);
   const size_t o_tl = take(size_t(p->n_tiles_max) * 4), o_nt = take(4);
+  const size_t o_cl = take(size_t(p->n_tiles_max) * 4), o_nc = take(4);
   const size_t o_ready = take(size_t(p->n_tiles_max) * 4), o_work = take(8), o_status = take(4);
-  const size_t o_comb = take(size_t(Tm) * experts_down_blocks(H, I) * 4);
+  const int down_blocks = experts_down_blocks(H, I) > H / kMmaDownRows ? experts_down_blocks(H, I) : H / kMmaDownRows;
+  const size_t o_comb = take(size_t(Tm) * down_blocks * 4);
   const size_t o_diag = take(8 * 8);
   const size_t o_xq = take(size_t(Tm) * H), o_xs = take(size_t(Tm) * (H / 32));
   const size_t o_hq = take(size_t(p->pairs_max) * I), o_hs = take(size_t(p->pairs_max) * (I / 32));
@@ -213,6 +221,8 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   s.rows_of = reinterpret_cast<int32_t *>(base + o_rows);
   s.tile_list = reinterpret_cast<int32_t *>(base + o_tl);
   s.n_tiles = reinterpret_cast<int32_t *>(base + o_nt);
+  s.chunk_list = reinterpret_cast<int32_t *>(base + o_cl);
+  s.n_chunks = reinterpret_cast<int32_t *>(base + o_nc);
   s.ready = reinterpret_cast<uint32_t *>(base + o_ready);
   s.comb_cnt = reinterpret_cast<uint32_t *>(base + o_comb);
   s.work = reinterpret_cast<uint32_t *>(base + o_work);
@@ -231,7 +241,12 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
     destroy_plan(p);
     return MOE_ERR_CUDA;
   }
-  if (prepare_route(route_smem_bytes(E, p->words)) != cudaSuccess || prepare_experts(H, I) != cudaSuccess) {
+  if (prepare_route(route_smem_bytes(E, p->words)) != cudaSuccess || prepare_experts(H, I) != cudaSuccess ||
+      prepare_experts_mma() != cudaSuccess) {
+    destroy_plan(p);
+    return MOE_ERR_CUDA;
+  }
+  if (!encode_mma_maps(c, *weights, &p->maps)) {
     destroy_plan(p);
     return MOE_ERR_CUDA;
   }
@@ -268,6 +283,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   const moe_config_t &c = p->cfg;
   Scratch &s = p->s;
   int32_t *status = d_status ? d_status : s.status;
+  const bool mma = T >= p->mma_min_rows;
 
   RouteArgs ra;
   ra.logits = logits;
@@ -287,10 +303,12 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ra.rows_of = s.rows_of;
   ra.tile_list = s.tile_list;
   ra.n_tiles = s.n_tiles;
+  ra.chunk_list = mma ? s.chunk_list : nullptr;
+  ra.n_chunks = s.n_chunks;
   ra.ready = s.ready;
   ra.n_tiles_max = p->n_tiles_max;
   ra.comb_cnt = s.comb_cnt;
-  ra.n_comb = T * experts_down_blocks(c.hidden, c.intermediate);
+  ra.n_comb = T * (mma ? c.hidden / kMmaDownRows : experts_down_blocks(c.hidden, c.intermediate));
   ra.work = s.work;
   ra.status = status;
   ra.diag = s.diag;
@@ -321,6 +339,8 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ea.rows_of = s.rows_of;
   ea.tile_list = s.tile_list;
   ea.n_tiles = s.n_tiles;
+  ea.chunk_list = s.chunk_list;
+  ea.n_chunks = s.n_chunks;
   ea.xq = s.xq;
   ea.xs = s.xs;
   ea.hq = s.hq;
@@ -339,7 +359,8 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ea.skip_ready_tile = (c.flags & MOE_FLAG_TEST_SKIP_READY) ? 0 : -1;
   const bool timed = (c.flags & MOE_FLAG_TIMING) && p->timed_calls < kMaxTimedCalls;
   if (timed && cudaEventRecord(p->ev_start[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_experts(ea, p->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+  const cudaError_t le = mma ? launch_experts_mma(p->maps, ea, p->num_sms, st) : launch_experts(ea, p->num_sms, st);
+  if (le != cudaSuccess) return MOE_ERR_CUDA;
   if (timed) {
     if (cudaEventRecord(p->ev_stop[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
     ++p->timed_calls;

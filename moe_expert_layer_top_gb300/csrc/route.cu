@@ -15,9 +15,11 @@
 // Optimizing DeepSeek-V4.1 Flash in SGLang" 2.1: the router writes the layout
 // the expert kernel consumes. That layout is:
 //   rows_of[e][rank]   pair ids (t*k + j), in token order;
-//   tile_list[]        (expert, tile) work items for the expert kernel.
-// The tile list's per-expert offsets come from one block-wide prefix over
-// the E+1 tile counts. That is work enumeration, not row placement.
+//   tile_list[]        (expert, tile) work items for the expert kernel;
+//   chunk_list[]       (expert, chunk) items of <= 128 rows for the tensor-core
+//                      expert kernel.
+// The lists' per-expert offsets come from block-wide prefixes over the E+1
+// tile (chunk) counts. That is work enumeration, not row placement.
 //
 // Blocks 1.. quantise x to MXFP8 (one 32-group per thread). "Beyond Day-0"
 // 2.1 fuses activation quantisation into the producer, and here it shares
@@ -145,8 +147,35 @@ __device__ __forceinline__ void route_topk(const RouteArgs &a, RouteSmem &sm, ui
   }
 }
 
-__device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
+// Exclusive prefix of v over the block's kRouteThreads threads, in thread
+// order; *total gets the sum. Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_scan(RouteSmem &sm, int v, int &total) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += u;
+  }
+  __syncthreads();  // an earlier scan's readers are done with warp_sums
+  if (lane == 31) sm.warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = sm.warp_sums[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, ws, off);
+      if (lane >= off) ws += u;
+    }
+    sm.warp_sums[lane] = ws;  // inclusive
+  }
+  __syncthreads();
+  total = sm.warp_sums[kRouteThreads / 32 - 1];
+  return x - v + (warp ? sm.warp_sums[warp - 1] : 0);
+}
+
+__device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
+  const int tid = threadIdx.x;
   const int E = a.E, k = a.k, T = a.T, W = a.words;
 
   if (tid < 8) a.diag[tid] = 0;
@@ -172,8 +201,8 @@ __device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
 
   // --- counts and tiles per expert (index E: the shared expert, every row)
   const int nexp = E + a.shared;
+  int cnt = 0;
   if (tid < nexp) {
-    int cnt;
     if (tid < E) {
       cnt = 0;
       for (int w = 0; w < W; ++w) cnt += __popc(bm[tid * W + w]);
@@ -186,25 +215,8 @@ __device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
     sm.tiles[tid] = 0;
   }
   // block-wide exclusive prefix of tiles[] (work enumeration for the expert kernel)
-  int v = sm.tiles[tid];
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int u = __shfl_up_sync(0xFFFFFFFFu, v, off);
-    if (lane >= off) v += u;
-  }
-  if (lane == 31) sm.warp_sums[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    int ws = sm.warp_sums[lane];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int u = __shfl_up_sync(0xFFFFFFFFu, ws, off);
-      if (lane >= off) ws += u;
-    }
-    sm.warp_sums[lane] = ws;  // inclusive
-  }
-  __syncthreads();
-  const int excl = v - sm.tiles[tid] + (warp ? sm.warp_sums[warp - 1] : 0);
+  int total = 0;
+  const int excl = block_exclusive_scan(sm, sm.tiles[tid], total);
   if (tid < nexp) {
     for (int j = 0; j < sm.tiles[tid]; ++j) {
       const int idx = excl + j;
@@ -212,7 +224,20 @@ __device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
       else report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
     }
   }
-  if (tid == kRouteThreads - 1) *a.n_tiles = min(excl + sm.tiles[tid], a.n_tiles_max);
+  if (tid == 0) *a.n_tiles = min(total, a.n_tiles_max);
+
+  // chunks of <= kChunkRows rows per expert, for the tensor-core expert kernel
+  if (a.chunk_list) {
+    const int nch = tid < nexp ? (cnt + kChunkRows - 1) / kChunkRows : 0;
+    int nch_total = 0;
+    const int cexcl = block_exclusive_scan(sm, nch, nch_total);
+    for (int j = 0; j < nch; ++j) {
+      const int idx = cexcl + j;
+      if (idx < a.n_tiles_max) a.chunk_list[idx] = (tid << 16) | j;
+      else report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
+    }
+    if (tid == 0) *a.n_chunks = min(nch_total, a.n_tiles_max);
+  }
 
   // --- placement: rank by population count of lower token bits
   for (int p = tid; p < T * k; p += blockDim.x) {

@@ -177,6 +177,8 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ra.rows_of = reinterpret_cast<int32_t *>(base + L.rows);
   ra.tile_list = reinterpret_cast<int32_t *>(base + L.tl);
   ra.n_tiles = reinterpret_cast<int32_t *>(base + L.nt);
+  ra.chunk_list = nullptr;  // this entry point always runs the CUDA-core expert kernel
+  ra.n_chunks = nullptr;
   ra.ready = reinterpret_cast<uint32_t *>(base + L.ready);
   ra.n_tiles_max = n_tiles_max;
   ra.comb_cnt = reinterpret_cast<uint32_t *>(base + L.comb);
@@ -211,6 +213,8 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ea.rows_of = ra.rows_of;
   ea.tile_list = ra.tile_list;
   ea.n_tiles = ra.n_tiles;
+  ea.chunk_list = nullptr;
+  ea.n_chunks = nullptr;
   ea.xq = ra.xq;
   ea.xs = ra.xs;
   ea.hq = base + L.hq;

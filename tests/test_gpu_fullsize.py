@@ -42,11 +42,18 @@ def routed_only(w: MoEWeightsMXFP8) -> MoEWeightsMXFP8:
     return MoEWeightsMXFP8(w.w_gate, w.s_gate, w.w_up, w.s_up, w.w_down, w.s_down)
 
 
-@pytest.mark.parametrize("name", ["bs1", "bs4", "bs16", "bs64"])
-def test_fullsize_parity(name, weights):
+# flags 0: the expert kernel the benchmark times (GEMV below 32 rows, MMA from
+# 32 rows); the pinned cases run the other kernel on the same workload.
+FULL = [("bs1", 0), ("bs4", 0), ("bs16", 0), ("bs64", 0),
+        ("bs1", abi.MOE_FLAG_PATH_MMA), ("bs4", abi.MOE_FLAG_PATH_MMA), ("bs16", abi.MOE_FLAG_PATH_GEMV)]
+
+
+@pytest.mark.parametrize("name,flags", FULL, ids=[f"{n}_{'default' if f == 0 else 'mma' if f == abi.MOE_FLAG_PATH_MMA else 'gemv'}"
+                                                  for n, f in FULL])
+def test_fullsize_parity(name, flags, weights):
     wl = synth.WORKLOADS[name]
     w = weights if wl.shared else routed_only(weights)
-    g = GpuRun(wl.T, wl.H, wl.E, wl.k, wl.I, wl.routing, wl.shared, seed=SEED, weights=w).run()
+    g = GpuRun(wl.T, wl.H, wl.E, wl.k, wl.I, wl.routing, wl.shared, seed=SEED, weights=w, flags=flags).run()
     assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     # sampled rows: the first and the last token row
     rows = [0, wl.T - 1]

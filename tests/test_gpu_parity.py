@@ -91,13 +91,19 @@ SMALL = [
     (24, 512, 16, 4, 256, "zipf", 1),         # shared expert
     (20, 1024, 16, 4, 512, "uniform", 0),     # second compiled shape
     (70, 512, 8, 3, 256, "zipf", 1),          # > 64 rows: several bitmap words, hot expert with 9 tiles
+    (300, 512, 8, 2, 256, "zipf", 1),         # experts with > 128 rows: several MMA chunks each
 ]
 
+# Both expert kernels, pinned by flag: the CUDA-core GEMV kernel and the
+# tensor-core (block-scaled MXFP8 MMA) kernel.
+PATHS = {"gemv": abi.MOE_FLAG_PATH_GEMV, "mma": abi.MOE_FLAG_PATH_MMA}
 
+
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("case", SMALL, ids=[f"T{c[0]}_H{c[1]}_E{c[2]}_k{c[3]}_sh{c[6]}" for c in SMALL])
-def test_small_case_parity(case):
+def test_small_case_parity(case, path):
     T, H, E, k, I, routing, shared = case
-    g = GpuRun(T, H, E, k, I, routing, shared, seed=42 + T).run()
+    g = GpuRun(T, H, E, k, I, routing, shared, seed=42 + T, flags=PATHS[path]).run()
     assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     get = oracle_experts(42 + T, E, H, I)
     sh = oracle.expert_weights_from_synth(42 + T, "shared", H, I) if shared else None
@@ -142,14 +148,15 @@ def test_routing_tie_break_on_device():
 
 # ----------------------------------------------------------------- properties
 
-def test_deterministic_and_token_permutation_invariant():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_deterministic_and_token_permutation_invariant(path):
     T, H, E, k, I = 40, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I, "zipf").run()
+    g = GpuRun(T, H, E, k, I, "zipf", flags=PATHS[path]).run()
     y1 = g.y_bits.copy()
     g.run()
     np.testing.assert_array_equal(g.y_bits, y1)             # same input twice -> same bits
     perm = np.random.default_rng(5).permutation(T)
-    g2 = GpuRun(T, H, E, k, I, weights=g.weights, x_lg=(g.x_bits[perm], g.lg[perm])).run()
+    g2 = GpuRun(T, H, E, k, I, weights=g.weights, x_lg=(g.x_bits[perm], g.lg[perm]), flags=PATHS[path]).run()
     # each row's arithmetic does not depend on its tile-mates
     np.testing.assert_array_equal(g2.y_bits, y1[perm])
     g.close()
@@ -171,21 +178,23 @@ def test_empty_step_and_argument_errors():
     g.close()
 
 
-def test_fewer_rows_than_planned():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_fewer_rows_than_planned(path):
     T, H, E, k, I = 9, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I, max_rows=64).run()
+    g = GpuRun(T, H, E, k, I, max_rows=64, flags=PATHS[path]).run()
     r = oracle.moe_step(g.x_bits, g.lg, k, oracle_experts(42, E, H, I))
     check_routing_bit_exact(g, r)
     check_y(g.y_bits, r["y"])
     g.close()
 
 
-def test_bounded_wait_timeout_is_reported_and_recoverable():
-    """Host-injected fault: one tile never publishes its ready count. The down
-    units' bounded wait gives up, the step reports MOE_ERR_TIMEOUT, and the GPU
-    stays usable: a normal plan afterwards matches the oracle."""
+@pytest.mark.parametrize("path", list(PATHS))
+def test_bounded_wait_timeout_is_reported_and_recoverable(path):
+    """Host-injected fault: one tile (chunk) never publishes its ready count. The
+    down units' bounded wait gives up, the step reports MOE_ERR_TIMEOUT, and the
+    GPU stays usable: a normal plan afterwards matches the oracle."""
     T, H, E, k, I = 6, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I, flags=abi.MOE_FLAG_TEST_SKIP_READY, timeout_ns=20_000_000).run()
+    g = GpuRun(T, H, E, k, I, flags=abi.MOE_FLAG_TEST_SKIP_READY | PATHS[path], timeout_ns=20_000_000).run()
     assert g.status_code == abi.MOE_ERR_TIMEOUT
     g.close()
     ok = GpuRun(T, H, E, k, I).run()
@@ -204,6 +213,25 @@ def test_forward_host_matches_device_forward():
     assert g.step.forward_host(xh, lh, yh) == abi.MOE_OK
     np.testing.assert_array_equal(yh.numpy().view(np.uint16), g.y_bits)
     g.close()
+
+
+def test_path_flags_are_exclusive():
+    T, H, E, k, I = 6, 512, 8, 2, 256
+    w = synthetic.make_weights(1, E, H, I, 0, torch.device("cuda", 0))
+    with pytest.raises(abi.MoeError):
+        MoEStep(H, I, E, k, w, T, 0, abi.MOE_FLAG_PATH_GEMV | abi.MOE_FLAG_PATH_MMA)
+
+
+def test_default_path_switches_at_32_rows():
+    """Without a path flag, 31 rows run the GEMV kernel and 32 rows the MMA
+    kernel. Both results match the oracle."""
+    H, E, k, I = 512, 8, 2, 256
+    for T in (31, 32):
+        g = GpuRun(T, H, E, k, I, "zipf", seed=5).run()
+        assert g.status_code == abi.MOE_OK
+        r = oracle.moe_step(g.x_bits, g.lg, k, oracle_experts(5, E, H, I))
+        check_y(g.y_bits, r["y"])
+        g.close()
 
 
 def test_timing_flag_records_expert_kernel():
