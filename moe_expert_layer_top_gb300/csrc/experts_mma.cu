@@ -32,8 +32,9 @@
 //               .block_scale (4 per stage, K = 32 each) into one of two TMEM
 //               accumulators and commits each stage back to the ring.
 //   warps 2-5   loaders: gather the chunk's token rows into the B ring slot
-//               with cp.async in the 128-byte swizzled K-major layout, and
-//               write the stage's UE8M0 scales of A and B into TMEM.
+//               with cp.async in the 128-byte swizzled K-major layout, with
+//               the stage's UE8M0 scale words of A and B (the MMA issuer
+//               moves those into TMEM with tcgen05.cp).
 //   warps 6-9   epilogue: read the accumulator (tcgen05.ld), run the unit's
 //               epilogue, and hand the accumulator back to the MMA issuer.
 //
@@ -68,25 +69,23 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpLoad = 2, kWarpEpi = 6, kMWarps =
 constexpr int kMThreads = kMWarps * 32;
 constexpr int kLoaders = 128;               // threads of the loader warps
 constexpr int kEpiThreads = 128;            // threads of the epilogue warps
-constexpr int kLag = 3;                     // loader: stages of copies kept in flight
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 128;          // one fp32 accumulator: N <= 128 columns
 constexpr uint32_t kScaleCol0 = 2 * kAccCols;
 constexpr uint32_t kScaleSlotCols = 32;     // per stage: SFA at +0 (4 columns), SFB at +16 (4 columns)
-constexpr int kBarLoad = 1, kBarEpi = 2, kBarGate = 3;  // named barriers (0 is __syncthreads)
+constexpr int kBarEpi = 2, kBarGate = 3;   // named barriers (0 is __syncthreads)
 static_assert(kScaleCol0 + kMStages * kScaleSlotCols <= kTmemCols, "TMEM budget");
-static_assert(kLag < kMStages, "loader lag below the ring depth");
 static_assert(kChunkRows == 128 && kMmaDownRows == kBM, "unit geometry");
 
 struct MmaSmem {
   uint8_t a[kMStages][kABytes];       // weight tiles, 128-byte swizzled K-major (TMA)
   uint8_t b[kMStages][kBBytes];       // token-row tiles, same layout (cp.async)
-  uint32_t sfa[kMStages][kBM];        // per weight row: the stage's 4 UE8M0 codes (one per 32 K)
-  uint32_t sfb[kMStages][kChunkRows]; // per token row: the same
+  uint32_t sfa[kMStages][kBM];        // the stage's 4 UE8M0 codes (one per 32 K) per weight row, TMEM image order
+  uint32_t sfb[kMStages][kChunkRows]; // the same per token row
   uint16_t xchg[2][16][64];           // bf16 u of one 16-column slice, [column][i]
   uint32_t jobs[kChunkRows];          // token rows whose combine a down unit completed
   uint64_t full_a[kMStages];          // A landed (TMA bytes)
-  uint64_t full_b[kMStages];          // B and the scales in place (128 loader arrivals)
+  uint64_t full_b[kMStages];          // B and the scale words in place (128 loader arrivals)
   uint64_t empty[kMStages];           // the stage's MMAs are done (tcgen05.commit)
   uint64_t acc_full[2];               // accumulator complete (tcgen05.commit)
   uint64_t acc_empty[2];              // accumulator read out (128 epilogue arrivals)
@@ -181,13 +180,22 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
-               "r"(v[2]), "r"(v[3])
-               : "memory");
+// Shared-memory descriptor of a 32-row x 16-byte matrix, no swizzle: 8-row
+// core matrices of 128 bytes, 128 bytes apart.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);  // start address
+  d |= uint64_t(1) << 16;                 // leading byte offset: 16 bytes
+  d |= uint64_t(128 >> 4) << 32;          // stride byte offset: 8 rows x 16 bytes
+  d |= uint64_t(1) << 46;                 // descriptor version
+  return d;                               // no swizzle
 }
 
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 32 TMEM lanes x 4 columns from shared memory (16 bytes per lane), the same
+// in each of the four 32-lane quadrants.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 
 // 16 consecutive fp32 columns of the warp's 32 TMEM lanes (one lane per thread).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -216,25 +224,33 @@ struct MUnit {
   int nch;     // chunks of the expert
 };
 
-// An expert with cnt rows is split into ceil(cnt/128) chunks of nearly equal size.
+// An expert with cnt rows is split into ceil(cnt/128) chunks of nearly equal
+// size. The units of one expert are consecutive: for each of its blocks in
+// order, every chunk of the expert. Neighbouring units run at about the same
+// time on neighbouring blocks, so the chunks of a multi-chunk expert read
+// each weight block from HBM once and from L2 after that.
 __device__ __forceinline__ MUnit decode_unit(const ExpertArgs &a, int u, int n_chunks, int mbg, int hbd) {
   MUnit m;
   const int ng = n_chunks * mbg;
+  int nb;  // blocks per chunk
   if (u < ng) {
     m.down = 0;
-    m.chunk = u / mbg;
-    m.blk = u % mbg;
+    nb = mbg;
   } else {
     u -= ng;
     m.down = 1;
-    m.chunk = u / hbd;
-    m.blk = u % hbd;
+    nb = hbd;
   }
-  const int ent = __ldcg(a.chunk_list + m.chunk);
+  const int ci0 = u / nb;  // a chunk of the unit's expert
+  const int ent = __ldcg(a.chunk_list + ci0);
   m.e = ent >> 16;
-  const int c = ent & 0xFFFF;
+  const int cbase = ci0 - (ent & 0xFFFF);  // the expert's first chunk
   const int cnt = __ldcg(a.counts + m.e);
   m.nch = (cnt + kChunkRows - 1) / kChunkRows;
+  const int w = u - cbase * nb;  // unit within the expert's span of nch * nb units
+  m.blk = w / m.nch;
+  const int c = w - m.blk * m.nch;
+  m.chunk = cbase + c;
   const int cs = (cnt + m.nch - 1) / m.nch;
   m.start = c * cs;
   m.n = min(cs, cnt - m.start);
@@ -347,6 +363,9 @@ __device__ void mma_issuer(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, cons
       }
       tmem_fence_after();
       const uint32_t sfa = tmem + kScaleCol0 + uint32_t(s) * kScaleSlotCols, sfb = sfa + 16;
+      // the stage's scale words into TMEM (in issue order before the MMAs that read them)
+      tmem_cp_32x128b_x4(sfa, sf_desc(smem_u32(sm.sfa[s])));
+      tmem_cp_32x128b_x4(sfb, sf_desc(smem_u32(sm.sfb[s])));
       const uint64_t adesc = sw128_desc(smem_u32(sm.a[s])), bdesc = sw128_desc(smem_u32(sm.b[s]));
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
@@ -367,10 +386,15 @@ __device__ void mma_issuer(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, cons
 }
 
 // ------------------------------------------------------------------ loaders (warps 2-5)
-// Thread tau (0..127) copies 16-byte column c8 = tau % 8 of rows tau/8 + 16 i of
-// the B tile, the scale word of weight row tau and that of token row tau. Then,
-// for its warp's TMEM lane quadrant, it writes the stage's scale words: lane l
-// of column c holds row l + 32 c (the same words in each quadrant).
+// Thread tau (0..127) copies 16-byte column tau % 8 of rows tau/8 + 16 i of the
+// B tile, and the stage's scale word (4 UE8M0 codes, one per 32 K) of weight
+// row tau and of token row tau. The scale words go to shared memory in the
+// order of their TMEM image (word 4 l + c holds row l + 32 c; the MMA issuer
+// copies them with tcgen05.cp). Each thread runs its own pipeline and meets
+// no other thread: it issues a stage as soon as the ring slot is free, and
+// when it cannot issue, it waits for its oldest stage in flight and arrives
+// on that stage's full_b (fence.proxy.async first: the copies were written
+// through the generic proxy, the MMA reads through the async proxy).
 
 struct LoaderRows {
   const uint8_t *b[8];  // row i: token (pair) row r = tau/8 + 16 i of the chunk, its K-major codes
@@ -409,7 +433,7 @@ __device__ __forceinline__ LoaderRows loader_rows(const ExpertArgs &a, const MUn
   return lr;
 }
 
-// Issue the copies of stage slot s for K chunk kc.
+// Issue the copies of stage slot s for K chunk kc (one cp.async group).
 __device__ __forceinline__ void loader_issue(MmaSmem &sm, const MUnit &m, const LoaderRows &lr, int s, int kc,
                                              int tau, const void *zero_src) {
   const int c8 = tau & 7, r0 = tau >> 3;
@@ -423,25 +447,35 @@ __device__ __forceinline__ void loader_issue(MmaSmem &sm, const MUnit &m, const 
                        v ? 16u : 0u);
     }
   }
-  cp_async4_zfill(&sm.sfa[s][tau], lr.sfa + kc * 4, 4u);
-  if (tau < m.npad) cp_async4_zfill(&sm.sfb[s][tau], lr.sfb ? lr.sfb + kc * 4 : zero_src, lr.sfb ? 4u : 0u);
+  const int w = (tau & 31) * 4 + (tau >> 5);  // TMEM image order
+  cp_async4_zfill(&sm.sfa[s][w], lr.sfa + kc * 4, 4u);
+  cp_async4_zfill(&sm.sfb[s][w], lr.sfb ? lr.sfb + kc * 4 : zero_src, lr.sfb ? 4u : 0u);
+  cp_async_commit();
 }
 
-// After a loader barrier: the scale words of stage slot s into TMEM, then this
-// thread's arrival on full_b[s].
-__device__ __forceinline__ void loader_signal(MmaSmem &sm, uint32_t tmem, int s, int q, int lane) {
-  uint32_t va[4], vb[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    va[c] = sm.sfa[s][lane + 32 * c];
-    vb[c] = sm.sfb[s][lane + 32 * c];
+// Wait until at most n of this thread's copy groups are still in flight (n < kMStages).
+__device__ __forceinline__ void cp_async_wait_n(uint32_t n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    default: cp_async_wait<5>(); break;
   }
-  const uint32_t t = tmem + (uint32_t(32 * q) << 16) + kScaleCol0 + uint32_t(s) * kScaleSlotCols;
-  tmem_st4(t, va);
-  tmem_st4(t + 16, vb);
-  tmem_wait_st();
-  tmem_fence_before();
-  mbar_arrive(&sm.full_b[s]);
+}
+static_assert(kMStages <= 6, "cp_async_wait_n covers at most 5 newer groups");
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 __device__ __forceinline__ int wait_chunk_ready(const ExpertArgs &a, int chunk, uint32_t target, int u) {
@@ -458,62 +492,54 @@ __device__ __forceinline__ int wait_chunk_ready(const ExpertArgs &a, int chunk, 
   return 1;
 }
 
-__device__ void mma_loaders(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, const Sched &sc, int n_chunks, int mbg,
-                            int hbd) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3;
-  const int tau = (warp - kWarpLoad) * 32 + lane;
+__device__ void mma_loaders(const ExpertArgs &a, MmaSmem &sm, const Sched &sc, int n_chunks, int mbg, int hbd) {
+  const int tau = int(threadIdx.x) - kWarpLoad * 32;
   const void *zero_src = a.xq;  // any valid address: zero-byte copies read nothing
-  uint32_t g = 0, gc = 0;       // stages issued, stages signalled
-  bool alive = true;
-  for (int i = 0; alive; ++i) {
-    const int u = sc.unit(i);
-    if (u < 0) break;
-    const MUnit m = decode_unit(a, u, n_chunks, mbg, hbd);
-    int ok = !aborted(a);
-    if (m.down && !bar_and(kBarLoad, kLoaders, ld_acquire_gpu(a.ready + m.chunk) >= uint32_t(mbg))) {
-      // h of the chunk is not complete yet. Every issued stage reaches the MMA
-      // before this block waits on others.
-      cp_async_wait<0>();
-      fence_proxy_async();
-      named_bar(kBarLoad, kLoaders);
-      for (; gc < g; ++gc) loader_signal(sm, tmem, int(gc % kMStages), q, lane);
-      if (ok) ok = wait_chunk_ready(a, m.chunk, uint32_t(mbg), u);
+  uint32_t g = 0, gc = 0;       // stages issued, stages signalled (this thread's)
+  // this thread's oldest stage in flight: copies landed -> fence -> arrive
+  auto complete_oldest = [&]() {
+    cp_async_wait_n(g - gc - 1);
+    fence_proxy_async();
+    mbar_arrive(&sm.full_b[gc % kMStages]);
+    ++gc;
+  };
+  MUnit m;
+  LoaderRows lr;
+  int kc = 0, kcs = 0, next = 0;
+  while (true) {
+    if (kc == kcs) {  // start the next unit
+      const int u = sc.unit(next++);
+      if (u < 0 || aborted(a)) break;
+      m = decode_unit(a, u, n_chunks, mbg, hbd);
+      if (m.down && ld_acquire_gpu(a.ready + m.chunk) < uint32_t(mbg)) {
+        // h of the chunk is not complete: everything in flight reaches the MMA
+        // before this thread waits on other blocks
+        while (gc < g) complete_oldest();
+        if (!wait_chunk_ready(a, m.chunk, uint32_t(mbg), u)) break;
+      }
+      lr = loader_rows(a, m, tau);
+      kc = 0;
+      kcs = (m.down ? a.I : a.H) / kKC;
     }
-    if (!bar_and(kBarLoad, kLoaders, ok)) {
-      alive = false;
+    const int s = int(g % kMStages);
+    const uint32_t ph = (g / kMStages) & 1u;
+    if (g - gc < uint32_t(kMStages) && mbar_test(&sm.empty[s], ph ^ 1u)) {
+      loader_issue(sm, m, lr, s, kc, tau, zero_src);
+      ++g;
+      ++kc;
+      continue;
+    }
+    if (gc < g) {
+      complete_oldest();
+      continue;
+    }
+    int64_t waited = 0;
+    if (!mbar_wait(&sm.empty[s], ph ^ 1u, a.timeout_ns, &waited)) {
+      fail(a, kDiagEmptyWait, -1, s, kc, -14, waited);
       break;
     }
-    const LoaderRows lr = loader_rows(a, m, tau);
-    const int kcs = (m.down ? a.I : a.H) / kKC;
-    for (int kc = 0; kc < kcs; ++kc) {
-      const int s = int(g % kMStages);
-      const uint32_t ph = (g / kMStages) & 1u;
-      int64_t waited = 0;
-      int ok2 = mbar_wait(&sm.empty[s], ph ^ 1u, a.timeout_ns, &waited) ? 1 : 0;
-      if (ok2) loader_issue(sm, m, lr, s, kc, tau, zero_src);
-      else fail(a, kDiagEmptyWait, u, s, kc, -14, waited);
-      cp_async_commit();
-      ++g;
-      const bool due = g - gc > uint32_t(kLag);
-      if (due) {
-        cp_async_wait<kLag>();  // this thread's copies of stage gc have landed
-        fence_proxy_async();
-      }
-      if (!bar_and(kBarLoad, kLoaders, ok2)) {
-        alive = false;
-        break;
-      }
-      if (due) {
-        loader_signal(sm, tmem, int(gc % kMStages), q, lane);
-        ++gc;
-      }
-    }
   }
-  cp_async_wait<0>();
-  fence_proxy_async();
-  named_bar(kBarLoad, kLoaders);
-  if (alive)
-    for (; gc < g; ++gc) loader_signal(sm, tmem, int(gc % kMStages), q, lane);
+  while (gc < g) complete_oldest();
 }
 
 // ------------------------------------------------------------------ epilogue (warps 6-9)
@@ -664,7 +690,7 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
   } else if (warp == kWarpMma) {
     if (lane == 0) mma_issuer(a, sm, tmem, sc, n_chunks, mbg, hbd);
   } else if (warp < kWarpEpi) {
-    mma_loaders(a, sm, tmem, sc, n_chunks, mbg, hbd);
+    mma_loaders(a, sm, sc, n_chunks, mbg, hbd);
   } else {
     mma_epilogue(a, sm, tmem, sc, n_chunks, mbg, hbd);
   }
