@@ -60,41 +60,55 @@ namespace moe {
 
 namespace {
 
-constexpr int kMStages = 6;                 // ring depth
 constexpr int kKC = 128;                    // bytes (E4M3 values) of K per stage: 4 MMAs of K = 32
 constexpr int kBM = 128;                    // MMA M (weight rows per unit)
 constexpr int kABytes = kBM * kKC;          // 16 KB
-constexpr int kBBytes = kChunkRows * kKC;   // 16 KB
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpLoad = 2, kWarpEpi = 6, kMWarps = 10;
 constexpr int kMThreads = kMWarps * 32;
 constexpr int kLoaders = 128;               // threads of the loader warps
 constexpr int kEpiThreads = 128;            // threads of the epilogue warps
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = 128;          // one fp32 accumulator: N <= 128 columns
-constexpr uint32_t kScaleCol0 = 2 * kAccCols;
 constexpr uint32_t kScaleSlotCols = 32;     // per stage: SFA at +0 (4 columns), SFB at +16 (4 columns)
 constexpr int kBarEpi = 2, kBarGate = 3;   // named barriers (0 is __syncthreads)
-static_assert(kScaleCol0 + kMStages * kScaleSlotCols <= kTmemCols, "TMEM budget");
-static_assert(kChunkRows == 128 && kMmaDownRows == kBM, "unit geometry");
+static_assert(kMmaDownRows == kBM, "unit geometry");
 
-struct MmaSmem {
-  uint8_t a[kMStages][kABytes];       // weight tiles, 128-byte swizzled K-major (TMA)
-  uint8_t b[kMStages][kBBytes];       // token-row tiles, same layout (cp.async)
-  uint32_t sfa[kMStages][kBM];        // the stage's 4 UE8M0 codes (one per 32 K) per weight row, TMEM image order
-  uint32_t sfb[kMStages][kChunkRows]; // the same per token row
-  uint16_t xchg[2][16][64];           // bf16 u of one 16-column slice, [column][i]
-  uint32_t jobs[kChunkRows];          // token rows whose combine a down unit completed
-  uint64_t full_a[kMStages];          // A landed (TMA bytes)
-  uint64_t full_b[kMStages];          // B and the scale words in place (128 loader arrivals)
-  uint64_t empty[kMStages];           // the stage's MMAs are done (tcgen05.commit)
-  uint64_t acc_full[2];               // accumulator complete (tcgen05.commit)
-  uint64_t acc_empty[2];              // accumulator read out (128 epilogue arrivals)
-  uint64_t mma_done;                  // every MMA of the block finished (before TMEM is freed)
-  uint32_t tmem_base;
-  uint32_t n_jobs;
+// One instantiation per chunk size. A chunk of at most NMAX token rows is the
+// MMA's N; the ring holds STAGES stages of a 16 KB weight tile plus an
+// NMAX-row token tile, so smaller chunks leave room for a deeper ring (more
+// weight bytes in flight per SM).
+template <int NMAX_, int STAGES_>
+struct MmaCfg {
+  static constexpr int NMAX = NMAX_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int BBYTES = NMAX * kKC;
+  static constexpr uint32_t ACC_COLS = NMAX < 32 ? 32 : NMAX;  // TMEM columns per accumulator
+  static constexpr uint32_t SCALE_COL0 = 2 * ACC_COLS;
+  struct Smem {
+    uint8_t a[STAGES][kABytes];     // weight tiles, 128-byte swizzled K-major (TMA)
+    uint8_t b[STAGES][BBYTES];      // token-row tiles, same layout (cp.async)
+    uint32_t sfa[STAGES][128];      // the stage's 4 UE8M0 codes (one per 32 K) per weight row, TMEM image order
+    uint32_t sfb[STAGES][128];      // the same per token row (rows past NMAX unused)
+    uint16_t xchg[2][16][64];       // bf16 u of one 16-column slice, [column][i]
+    uint32_t jobs[NMAX];            // token rows whose combine a down unit completed
+    uint64_t full_a[STAGES];        // A landed (TMA bytes)
+    uint64_t full_b[STAGES];        // B and the scale words in place (128 loader arrivals)
+    uint64_t empty[STAGES];         // the stage's MMAs are done (tcgen05.commit)
+    uint64_t acc_full[2];           // accumulator complete (tcgen05.commit)
+    uint64_t acc_empty[2];          // accumulator read out (128 epilogue arrivals)
+    uint64_t mma_done;              // every MMA of the block finished (before TMEM is freed)
+    uint32_t tmem_base;
+    uint32_t n_jobs;
+  };
+  static constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + alignment of the ring to 1024 bytes
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SCALE_COL0 + STAGES * kScaleSlotCols <= kTmemCols, "TMEM budget");
+  static_assert(NMAX % 16 == 0 && NMAX <= 128 && BBYTES % 1024 == 0, "token tile geometry");
+  static_assert(STAGES <= 11, "cp_async_wait_n covers at most 10 newer groups");
 };
-constexpr size_t kMmaSmemBytes = sizeof(MmaSmem) + 1024;  // + alignment of the ring to 1024 bytes
-static_assert(kMmaSmemBytes <= 227 * 1024, "shared memory budget");
+using Cfg16 = MmaCfg<16, 11>;
+using Cfg32 = MmaCfg<32, 10>;
+using Cfg64 = MmaCfg<64, 8>;
+using Cfg128 = MmaCfg<128, 6>;
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -224,11 +238,12 @@ struct MUnit {
   int nch;     // chunks of the expert
 };
 
-// An expert with cnt rows is split into ceil(cnt/128) chunks of nearly equal
+// An expert with cnt rows is split into ceil(cnt/NMAX) chunks of nearly equal
 // size. The units of one expert are consecutive: for each of its blocks in
 // order, every chunk of the expert. Neighbouring units run at about the same
 // time on neighbouring blocks, so the chunks of a multi-chunk expert read
 // each weight block from HBM once and from L2 after that.
+template <int NMAX>
 __device__ __forceinline__ MUnit decode_unit(const ExpertArgs &a, int u, int n_chunks, int mbg, int hbd) {
   MUnit m;
   const int ng = n_chunks * mbg;
@@ -246,7 +261,7 @@ __device__ __forceinline__ MUnit decode_unit(const ExpertArgs &a, int u, int n_c
   m.e = ent >> 16;
   const int cbase = ci0 - (ent & 0xFFFF);  // the expert's first chunk
   const int cnt = __ldcg(a.counts + m.e);
-  m.nch = (cnt + kChunkRows - 1) / kChunkRows;
+  m.nch = (cnt + NMAX - 1) / NMAX;
   const int w = u - cbase * nb;  // unit within the expert's span of nch * nb units
   m.blk = w / m.nch;
   const int c = w - m.blk * m.nch;
@@ -282,14 +297,16 @@ __device__ __forceinline__ void fail(const ExpertArgs &a, int64_t site, int64_t 
 
 // ------------------------------------------------------------------ TMA producer (one lane)
 
-__device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, MmaSmem &sm, const Sched &sc, int n_chunks,
-                             int mbg, int hbd) {
+template <class C>
+__device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename C::Smem &sm, const Sched &sc,
+                             int n_chunks, int mbg, int hbd) {
+  constexpr int kMStages = C::STAGES;
   const uint64_t pol_first = l2_evict_first_policy(), pol_normal = l2_evict_normal_policy();
   uint32_t g = 0;  // stages issued
   for (int i = 0;; ++i) {
     const int u = sc.unit(i);
     if (u < 0 || aborted(a)) break;
-    const MUnit m = decode_unit(a, u, n_chunks, mbg, hbd);
+    const MUnit m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
     const bool sh = m.e == a.E;
     // the chunks of a multi-chunk expert read the same weights at about the same time
     const uint64_t pol = m.nch > 1 ? pol_normal : pol_first;
@@ -328,13 +345,15 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, MmaSmem &
 
 // ------------------------------------------------------------------ MMA issuer (one lane)
 
-__device__ void mma_issuer(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, const Sched &sc, int n_chunks, int mbg,
-                           int hbd) {
+template <class C>
+__device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t tmem, const Sched &sc, int n_chunks,
+                           int mbg, int hbd) {
+  constexpr int kMStages = C::STAGES;
   uint32_t g = 0, nu = 0;  // stages consumed, units done
   for (int i = 0;; ++i) {
     const int u = sc.unit(i);
     if (u < 0 || aborted(a)) break;
-    const MUnit m = decode_unit(a, u, n_chunks, mbg, hbd);
+    const MUnit m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
     const int acc = int(nu & 1u);
     const uint32_t aph = (nu >> 1) & 1u;
     int64_t waited = 0;
@@ -343,7 +362,7 @@ __device__ void mma_issuer(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, cons
       break;
     }
     tmem_fence_after();
-    const uint32_t d = tmem + uint32_t(acc) * kAccCols;
+    const uint32_t d = tmem + uint32_t(acc) * C::ACC_COLS;
     // kind::mxf8f6f4, A and B E4M3, K-major, UE8M0 scales, N = npad, M = 128
     const uint32_t idesc = (1u << 23) | (uint32_t(m.npad >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
     const int kcs = (m.down ? a.I : a.H) / kKC;
@@ -362,7 +381,7 @@ __device__ void mma_issuer(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, cons
         break;
       }
       tmem_fence_after();
-      const uint32_t sfa = tmem + kScaleCol0 + uint32_t(s) * kScaleSlotCols, sfb = sfa + 16;
+      const uint32_t sfa = tmem + C::SCALE_COL0 + uint32_t(s) * kScaleSlotCols, sfb = sfa + 16;
       // the stage's scale words into TMEM (in issue order before the MMAs that read them)
       tmem_cp_32x128b_x4(sfa, sf_desc(smem_u32(sm.sfa[s])));
       tmem_cp_32x128b_x4(sfb, sf_desc(smem_u32(sm.sfb[s])));
@@ -396,19 +415,21 @@ __device__ void mma_issuer(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, cons
 // on that stage's full_b (fence.proxy.async first: the copies were written
 // through the generic proxy, the MMA reads through the async proxy).
 
+template <int NMAX>
 struct LoaderRows {
-  const uint8_t *b[8];  // row i: token (pair) row r = tau/8 + 16 i of the chunk, its K-major codes
+  const uint8_t *b[NMAX / 16];  // row i: token (pair) row r = tau/8 + 16 i of the chunk, its K-major codes
   const uint8_t *sfa;   // scale row of weight row tau
   const uint8_t *sfb;   // scale row of token row tau (or NULL past the chunk)
 };
 
-__device__ __forceinline__ LoaderRows loader_rows(const ExpertArgs &a, const MUnit &m, int tau) {
-  LoaderRows lr;
+template <int NMAX>
+__device__ __forceinline__ LoaderRows<NMAX> loader_rows(const ExpertArgs &a, const MUnit &m, int tau) {
+  LoaderRows<NMAX> lr;
   const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
   const int64_t tk = int64_t(a.T) * a.k;
   const int r0 = tau >> 3;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NMAX / 16; ++i) {
     const int r = r0 + 16 * i;
     lr.b[i] = nullptr;
     if (r < m.n) {
@@ -434,12 +455,13 @@ __device__ __forceinline__ LoaderRows loader_rows(const ExpertArgs &a, const MUn
 }
 
 // Issue the copies of stage slot s for K chunk kc (one cp.async group).
-__device__ __forceinline__ void loader_issue(MmaSmem &sm, const MUnit &m, const LoaderRows &lr, int s, int kc,
-                                             int tau, const void *zero_src) {
+template <class C>
+__device__ __forceinline__ void loader_issue(typename C::Smem &sm, const MUnit &m, const LoaderRows<C::NMAX> &lr,
+                                             int s, int kc, int tau, const void *zero_src) {
   const int c8 = tau & 7, r0 = tau >> 3;
   uint8_t *bs = sm.b[s];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < C::NMAX / 16; ++i) {
     const int r = r0 + 16 * i;
     if (r < m.npad) {
       const bool v = lr.b[i] != nullptr;
@@ -453,7 +475,7 @@ __device__ __forceinline__ void loader_issue(MmaSmem &sm, const MUnit &m, const 
   cp_async_commit();
 }
 
-// Wait until at most n of this thread's copy groups are still in flight (n < kMStages).
+// Wait until at most n (<= 10) of this thread's copy groups are still in flight.
 __device__ __forceinline__ void cp_async_wait_n(uint32_t n) {
   switch (n) {
     case 0: cp_async_wait<0>(); break;
@@ -461,10 +483,14 @@ __device__ __forceinline__ void cp_async_wait_n(uint32_t n) {
     case 2: cp_async_wait<2>(); break;
     case 3: cp_async_wait<3>(); break;
     case 4: cp_async_wait<4>(); break;
-    default: cp_async_wait<5>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 7: cp_async_wait<7>(); break;
+    case 8: cp_async_wait<8>(); break;
+    case 9: cp_async_wait<9>(); break;
+    default: cp_async_wait<10>(); break;
   }
 }
-static_assert(kMStages <= 6, "cp_async_wait_n covers at most 5 newer groups");
 
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
@@ -492,7 +518,10 @@ __device__ __forceinline__ int wait_chunk_ready(const ExpertArgs &a, int chunk, 
   return 1;
 }
 
-__device__ void mma_loaders(const ExpertArgs &a, MmaSmem &sm, const Sched &sc, int n_chunks, int mbg, int hbd) {
+template <class C>
+__device__ void mma_loaders(const ExpertArgs &a, typename C::Smem &sm, const Sched &sc, int n_chunks, int mbg,
+                            int hbd) {
+  constexpr int kMStages = C::STAGES;
   const int tau = int(threadIdx.x) - kWarpLoad * 32;
   const void *zero_src = a.xq;  // any valid address: zero-byte copies read nothing
   uint32_t g = 0, gc = 0;       // stages issued, stages signalled (this thread's)
@@ -504,27 +533,27 @@ __device__ void mma_loaders(const ExpertArgs &a, MmaSmem &sm, const Sched &sc, i
     ++gc;
   };
   MUnit m;
-  LoaderRows lr;
+  LoaderRows<C::NMAX> lr;
   int kc = 0, kcs = 0, next = 0;
   while (true) {
     if (kc == kcs) {  // start the next unit
       const int u = sc.unit(next++);
       if (u < 0 || aborted(a)) break;
-      m = decode_unit(a, u, n_chunks, mbg, hbd);
+      m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
       if (m.down && ld_acquire_gpu(a.ready + m.chunk) < uint32_t(mbg)) {
         // h of the chunk is not complete: everything in flight reaches the MMA
         // before this thread waits on other blocks
         while (gc < g) complete_oldest();
         if (!wait_chunk_ready(a, m.chunk, uint32_t(mbg), u)) break;
       }
-      lr = loader_rows(a, m, tau);
+      lr = loader_rows<C::NMAX>(a, m, tau);
       kc = 0;
       kcs = (m.down ? a.I : a.H) / kKC;
     }
     const int s = int(g % kMStages);
     const uint32_t ph = (g / kMStages) & 1u;
     if (g - gc < uint32_t(kMStages) && mbar_test(&sm.empty[s], ph ^ 1u)) {
-      loader_issue(sm, m, lr, s, kc, tau, zero_src);
+      loader_issue<C>(sm, m, lr, s, kc, tau, zero_src);
       ++g;
       ++kc;
       continue;
@@ -544,8 +573,9 @@ __device__ void mma_loaders(const ExpertArgs &a, MmaSmem &sm, const Sched &sc, i
 
 // ------------------------------------------------------------------ epilogue (warps 6-9)
 
-__device__ void mma_epilogue(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, const Sched &sc, int n_chunks, int mbg,
-                             int hbd) {
+template <class C>
+__device__ void mma_epilogue(const ExpertArgs &a, typename C::Smem &sm, uint32_t tmem, const Sched &sc, int n_chunks,
+                             int mbg, int hbd) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ew = warp - kWarpEpi;
   const int et = ew * 32 + lane;
   const int64_t tk = int64_t(a.T) * a.k;
@@ -554,7 +584,7 @@ __device__ void mma_epilogue(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, co
   for (int i = 0;; ++i) {
     const int u = sc.unit(i);
     if (u < 0) break;
-    const MUnit m = decode_unit(a, u, n_chunks, mbg, hbd);
+    const MUnit m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
     const int acc = int(nu & 1u);
     const uint32_t aph = (nu >> 1) & 1u;
     int ok = !aborted(a);
@@ -565,7 +595,7 @@ __device__ void mma_epilogue(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, co
     }
     if (!bar_and(kBarEpi, kEpiThreads, ok)) break;
     tmem_fence_after();
-    const uint32_t ta = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc) * kAccCols;
+    const uint32_t ta = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc) * C::ACC_COLS;
     const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
     const int slices = m.npad / 16;
     if (!m.down) {
@@ -650,10 +680,13 @@ __device__ void mma_epilogue(const ExpertArgs &a, MmaSmem &sm, uint32_t tmem, co
 
 // ------------------------------------------------------------------ kernel
 
+template <class C>
 __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_constant__ MmaMaps maps,
                                                                    const ExpertArgs a) {
+  constexpr int kMStages = C::STAGES;
   extern __shared__ unsigned char mma_smem_raw[];
-  MmaSmem &sm = *reinterpret_cast<MmaSmem *>((reinterpret_cast<uintptr_t>(mma_smem_raw) + 1023) & ~uintptr_t(1023));
+  typename C::Smem &sm =
+      *reinterpret_cast<typename C::Smem *>((reinterpret_cast<uintptr_t>(mma_smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMStages; ++i) {
@@ -686,13 +719,13 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
   const int mbg = a.I / 64, hbd = a.H / kBM;
   const Sched sc(n_chunks, mbg, hbd);
   if (warp == kWarpTma) {
-    if (lane == 0) mma_producer(maps, a, sm, sc, n_chunks, mbg, hbd);
+    if (lane == 0) mma_producer<C>(maps, a, sm, sc, n_chunks, mbg, hbd);
   } else if (warp == kWarpMma) {
-    if (lane == 0) mma_issuer(a, sm, tmem, sc, n_chunks, mbg, hbd);
+    if (lane == 0) mma_issuer<C>(a, sm, tmem, sc, n_chunks, mbg, hbd);
   } else if (warp < kWarpEpi) {
-    mma_loaders(a, sm, sc, n_chunks, mbg, hbd);
+    mma_loaders<C>(a, sm, sc, n_chunks, mbg, hbd);
   } else {
-    mma_epilogue(a, sm, tmem, sc, n_chunks, mbg, hbd);
+    mma_epilogue<C>(a, sm, tmem, sc, n_chunks, mbg, hbd);
   }
   __syncwarp();
   tmem_fence_before();
@@ -751,24 +784,51 @@ bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *map
   return ok;
 }
 
-size_t experts_mma_smem_bytes() { return kMmaSmemBytes; }
+namespace {
 
-cudaError_t prepare_experts_mma() {
-  return cudaFuncSetAttribute(experts_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMmaSmemBytes));
+template <class C>
+cudaError_t prepare_cfg() {
+  return cudaFuncSetAttribute(experts_mma_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(C::SMEM_BYTES));
 }
 
-cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaStream_t st) {
+template <class C>
+cudaError_t launch_cfg(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMThreads);
-  cfg.dynamicSmemBytes = kMmaSmemBytes;
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, experts_mma_kernel, maps, a);
+  return cudaLaunchKernelEx(&cfg, experts_mma_kernel<C>, maps, a);
+}
+
+}  // namespace
+
+// A chunk never holds more rows than the step (an expert has at most T rows),
+// so the chunk size follows T: the smallest of 16, 32, 64, 128 that covers it.
+int mma_chunk_rows(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128; }
+
+cudaError_t prepare_experts_mma() {
+  cudaError_t e = prepare_cfg<Cfg16>();
+  if (e == cudaSuccess) e = prepare_cfg<Cfg32>();
+  if (e == cudaSuccess) e = prepare_cfg<Cfg64>();
+  if (e == cudaSuccess) e = prepare_cfg<Cfg128>();
+  return e;
+}
+
+cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int grid, int chunk_rows, cudaStream_t st) {
+  switch (chunk_rows) {
+    case 16: return launch_cfg<Cfg16>(maps, a, grid, st);
+    case 32: return launch_cfg<Cfg32>(maps, a, grid, st);
+    case 64: return launch_cfg<Cfg64>(maps, a, grid, st);
+    case 128: return launch_cfg<Cfg128>(maps, a, grid, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

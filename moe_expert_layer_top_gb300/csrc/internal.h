@@ -18,7 +18,7 @@ constexpr int kStages = 5;              // pipeline depth
 constexpr int kRouteThreads = 1024;     // route kernel: block 0 (router + placement)
 constexpr int kQuantThreads = 256;      // route kernel: x-quantisation blocks (one group per thread)
 constexpr int kMaxTimedCalls = 4096;
-constexpr int kChunkRows = 128;         // tensor-core expert kernel: token rows per chunk (MMA N <= 128)
+constexpr int kChunkRowsMax = 128;      // tensor-core expert kernel: most token rows per chunk (MMA N)
 constexpr int kMmaDownRows = 128;       // tensor-core expert kernel: W_down rows per down unit
 constexpr int kMmaMinRowsDefault = 32;  // steps with at least this many rows take the tensor-core kernel
 
@@ -32,7 +32,7 @@ struct Scratch {
   int32_t *rows_of;     // [E + 1][Tmax] pair ids in rank order
   int32_t *tile_list;   // [n_tiles_max] (expert << 16) | tile
   int32_t *n_tiles;     // [1]
-  int32_t *chunk_list;  // [n_tiles_max] (expert << 16) | chunk, chunks of <= kChunkRows rows
+  int32_t *chunk_list;  // [n_tiles_max] (expert << 16) | chunk, chunks of <= mma_chunk_rows(T) rows
   int32_t *n_chunks;    // [1]
   uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile (per chunk on the tensor-core path)
   uint32_t *comb_cnt;   // [Tmax][down blocks] down blocks of a token row finished (fused combine)
@@ -92,6 +92,7 @@ struct RouteArgs {
   int32_t *n_tiles;
   int32_t *chunk_list;  // NULL: no chunk list (the GEMV expert kernel only)
   int32_t *n_chunks;
+  int chunk_rows;       // rows per chunk (16, 32, 64 or 128)
   uint32_t *ready;
   int n_tiles_max;
   uint32_t *comb_cnt;
@@ -110,7 +111,7 @@ struct ExpertArgs {
   const int32_t *rows_of;
   const int32_t *tile_list;
   const int32_t *n_tiles;
-  const int32_t *chunk_list;  // tensor-core kernel: chunks of <= kChunkRows rows per expert
+  const int32_t *chunk_list;  // tensor-core kernel: chunks of <= mma_chunk_rows(T) rows per expert
   const int32_t *n_chunks;
   const uint8_t *xq, *xs;
   uint8_t *hq, *hs;
@@ -141,8 +142,8 @@ size_t experts_smem_bytes();
 // Tensor-core expert kernel (tcgen05 block-scaled MXFP8 MMA).
 bool experts_mma_shape_supported(int H, int I);
 bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *maps);
+int mma_chunk_rows(int T);
 cudaError_t prepare_experts_mma();
-cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaStream_t st);
-size_t experts_mma_smem_bytes();
+cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int grid, int chunk_rows, cudaStream_t st);
 
 }  // namespace moe

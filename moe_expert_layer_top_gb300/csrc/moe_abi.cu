@@ -305,6 +305,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ra.n_tiles = s.n_tiles;
   ra.chunk_list = mma ? s.chunk_list : nullptr;
   ra.n_chunks = s.n_chunks;
+  ra.chunk_rows = mma_chunk_rows(T);
   ra.ready = s.ready;
   ra.n_tiles_max = p->n_tiles_max;
   ra.comb_cnt = s.comb_cnt;
@@ -359,7 +360,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ea.skip_ready_tile = (c.flags & MOE_FLAG_TEST_SKIP_READY) ? 0 : -1;
   const bool timed = (c.flags & MOE_FLAG_TIMING) && p->timed_calls < kMaxTimedCalls;
   if (timed && cudaEventRecord(p->ev_start[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
-  const cudaError_t le = mma ? launch_experts_mma(p->maps, ea, p->num_sms, st) : launch_experts(ea, p->num_sms, st);
+  const cudaError_t le = mma ? launch_experts_mma(p->maps, ea, p->num_sms, ra.chunk_rows, st) : launch_experts(ea, p->num_sms, st);
   if (le != cudaSuccess) return MOE_ERR_CUDA;
   if (timed) {
     if (cudaEventRecord(p->ev_stop[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;

@@ -16,8 +16,8 @@
 // the expert kernel consumes. That layout is:
 //   rows_of[e][rank]   pair ids (t*k + j), in token order;
 //   tile_list[]        (expert, tile) work items for the expert kernel;
-//   chunk_list[]       (expert, chunk) items of <= 128 rows for the tensor-core
-//                      expert kernel.
+//   chunk_list[]       (expert, chunk) items of <= 16..128 rows for the
+//                      tensor-core expert kernel.
 // The lists' per-expert offsets come from block-wide prefixes over the E+1
 // tile (chunk) counts. That is work enumeration, not row placement.
 //
@@ -226,9 +226,9 @@ __device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
   }
   if (tid == 0) *a.n_tiles = min(total, a.n_tiles_max);
 
-  // chunks of <= kChunkRows rows per expert, for the tensor-core expert kernel
+  // chunks of <= chunk_rows rows per expert, for the tensor-core expert kernel
   if (a.chunk_list) {
-    const int nch = tid < nexp ? (cnt + kChunkRows - 1) / kChunkRows : 0;
+    const int nch = tid < nexp ? (cnt + a.chunk_rows - 1) / a.chunk_rows : 0;
     int nch_total = 0;
     const int cexcl = block_exclusive_scan(sm, nch, nch_total);
     for (int j = 0; j < nch; ++j) {

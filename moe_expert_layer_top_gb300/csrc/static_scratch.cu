@@ -179,6 +179,7 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ra.n_tiles = reinterpret_cast<int32_t *>(base + L.nt);
   ra.chunk_list = nullptr;  // this entry point always runs the CUDA-core expert kernel
   ra.n_chunks = nullptr;
+  ra.chunk_rows = kChunkRowsMax;
   ra.ready = reinterpret_cast<uint32_t *>(base + L.ready);
   ra.n_tiles_max = n_tiles_max;
   ra.comb_cnt = reinterpret_cast<uint32_t *>(base + L.comb);
