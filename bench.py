@@ -174,7 +174,7 @@ EXPERT_KERNELS = {
             "experts_mma_kernel_traffic.json"),
 }
 PATH_FLAGS = {"auto": 0, "gemv": 1 << 1, "mma": 1 << 2}
-MMA_MIN_ROWS = 32  # the library's default switch between the two expert kernels
+MMA_MIN_ROWS = 1  # the library's default: the tensor-core kernel at every row count
 
 
 def kernel_path(path, T):
@@ -494,7 +494,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=["tiny", "bs1", "bs4", "bs16", "bs64"])
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
-                    help="expert kernel: auto (GEMV below 32 rows, MMA from 32), or pin gemv / mma")
+                    help="expert kernel: auto (the library default: mma), or pin gemv / mma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -82,15 +82,14 @@ typedef enum {
 
 #define MOE_FLAG_PATH_GEMV (1u << 1)
 #define MOE_FLAG_PATH_MMA (1u << 2)
-/* Expert kernel selection. By default a step with T >= 32 rows runs the
- * tensor-core expert kernel (block-scaled MXFP8 tcgen05 MMA: one MMA covers
- * up to 128 token rows of an expert, so multi-tile experts stream their
- * weights once), and a smaller step runs the CUDA-core GEMV expert kernel
- * (8-row tiles; no tensor-core work for one or two rows). PATH_GEMV and
- * PATH_MMA pin one kernel for every step; setting both is
- * MOE_ERR_INVALID_ARG. Both kernels compute the same result within the fp32
- * summation-order tolerance; routing, placement and every MXFP8 quantisation
- * of a given input are identical. */
+/* Expert kernel selection. By default every step runs the tensor-core expert
+ * kernel: block-scaled MXFP8 tcgen05 MMA, one MMA covering up to 16 or 32
+ * token rows of an expert, so each expert's weights stream once per step.
+ * PATH_GEMV selects the CUDA-core GEMV expert kernel instead (8-row tiles;
+ * an expert's weights stream once per tile). PATH_MMA pins the default.
+ * Setting both is MOE_ERR_INVALID_ARG. Both kernels compute the same result
+ * within the fp32 summation-order tolerance; routing, placement and every
+ * MXFP8 quantisation of a given input are identical. */
 
 #define MOE_FLAG_TEST_SKIP_READY (1u << 8)
 /* Host-side fault injection for tests. The gate/up units of the first placed

@@ -3,11 +3,11 @@
 //
 // The CUDA-core expert kernel streams an expert's weights once per 8-row tile,
 // so an expert with hundreds of rows re-reads them and spends CUDA-core FMAs
-// on every tile. Here each expert's rows are split into chunks of <= 128 rows,
-// and one MMA per 32 K columns covers a whole chunk. The weights are streamed
-// once per chunk (chunks of one expert run side by side and share the lines
-// in L2). Tensor time is small next to the weight stream, so the kernel stays
-// bound by HBM.
+// on every tile. Here each expert's rows are split into chunks of <= 16 or 32
+// rows, and one MMA per 32 K columns covers a whole chunk. The chunks of one
+// expert run side by side on neighbouring blocks and read each weight block
+// from HBM once (the others find it in L2). Tensor time is small next to the
+// weight stream, so the kernel stays bound by HBM, also at one token row.
 //
 // Work units, in each block's order:
 //   gate/up unit (chunk c, block b): rows [64b, 64b + 64) of W_gate and of W_up
@@ -27,7 +27,7 @@
 //
 // Warp roles (10 warps):
 //   warp 0      TMA producer: one lane loads the A tiles (128 bytes of K x 64
-//               or 128 rows per box, 128-byte swizzle) into a 6-stage ring.
+//               or 128 rows per box, 128-byte swizzle) into a 10- or 11-stage ring.
 //   warp 1      MMA issuer: one lane issues tcgen05.mma.kind::mxf8f6f4
 //               .block_scale (4 per stage, K = 32 each) into one of two TMEM
 //               accumulators and commits each stage back to the ring.
@@ -107,8 +107,6 @@ struct MmaCfg {
 };
 using Cfg16 = MmaCfg<16, 11>;
 using Cfg32 = MmaCfg<32, 10>;
-using Cfg64 = MmaCfg<64, 8>;
-using Cfg128 = MmaCfg<128, 6>;
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -581,12 +579,16 @@ __device__ void mma_epilogue(const ExpertArgs &a, typename C::Smem &sm, uint32_t
   const int64_t tk = int64_t(a.T) * a.k;
   const uint32_t target = uint32_t(a.k + a.shared);
   uint32_t nu = 0, xc = 0;  // units done, gate/up column slices done
+  static_assert(C::NMAX <= 32, "one pair id per lane");
   for (int i = 0;; ++i) {
     const int u = sc.unit(i);
     if (u < 0) break;
     const MUnit m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
     const int acc = int(nu & 1u);
     const uint32_t aph = (nu >> 1) & 1u;
+    // pair id of column `lane` of the chunk (-1 past its end), loaded before the wait
+    const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
+    const int pr = lane < m.n ? __ldcg(rows + lane) : -1;
     int ok = !aborted(a);
     if (ok) {
       int64_t waited = 0;
@@ -596,15 +598,12 @@ __device__ void mma_epilogue(const ExpertArgs &a, typename C::Smem &sm, uint32_t
     if (!bar_and(kBarEpi, kEpiThreads, ok)) break;
     tmem_fence_after();
     const uint32_t ta = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc) * C::ACC_COLS;
-    const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
     const int slices = m.npad / 16;
     if (!m.down) {
       // lanes of quadrants 0, 1 hold gate rows 64b + 32q + lane; quadrants 2, 3 the up rows
       for (int j = 0; j < slices; ++j, ++xc) {
         float v[16];
         tmem_ld16(ta + uint32_t(16 * j), v);
-        int pr = -1;
-        if (lane < 16 && 16 * j + lane < m.n) pr = __ldcg(rows + 16 * j + lane);
         uint16_t(*xb)[64] = sm.xchg[xc & 1u];
         if (q >= 2) {
 #pragma unroll
@@ -615,7 +614,7 @@ __device__ void mma_epilogue(const ExpertArgs &a, typename C::Smem &sm, uint32_t
           const int64_t col = int64_t(m.blk) * 64 + 32 * q + lane;
 #pragma unroll 4
           for (int c = 0; c < 16; ++c) {
-            const int p = __shfl_sync(0xFFFFFFFFu, pr, c);
+            const int p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
             if (p < 0) continue;  // the same for the whole warp
             const float gb = bf16_bits_to_float(float_to_bf16_bits(v[c]));
             const float ub = bf16_bits_to_float(xb[c][32 * q + lane]);
@@ -632,32 +631,34 @@ __device__ void mma_epilogue(const ExpertArgs &a, typename C::Smem &sm, uint32_t
       tmem_fence_before();
       mbar_arrive(&sm.acc_empty[acc]);
       if (q < 2) {
-        __threadfence();  // this unit's h stores, before the ready count
+        // The two gate warps' h stores, then one release of the ready count: the
+        // barrier orders them before the fence of the publishing thread.
         named_bar(kBarGate, 64);
-        if (q == 0 && lane == 0 && m.chunk != a.skip_ready_tile) red_release_gpu_add(a.ready + m.chunk, 1u);
+        if (q == 0 && lane == 0 && m.chunk != a.skip_ready_tile) {
+          __threadfence();
+          red_release_gpu_add(a.ready + m.chunk, 1u);
+        }
       }
     } else {
       const int64_t h = int64_t(m.blk) * kBM + 32 * q + lane;
       for (int j = 0; j < slices; ++j) {
         float v[16];
         tmem_ld16(ta + uint32_t(16 * j), v);
-        int pr = -1;
-        if (lane < 16 && 16 * j + lane < m.n) pr = __ldcg(rows + 16 * j + lane);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const int p = __shfl_sync(0xFFFFFFFFu, pr, c);
+          const int p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
           if (p >= 0) a.o[int64_t(p) * a.H + h] = v[c];
         }
       }
       tmem_fence_before();
       mbar_arrive(&sm.acc_empty[acc]);
-      // Count each pair in for (token row, block); the last of a row's k (+ shared)
-      // pairs queues the row's combine (threadfence pattern: stores, fence, barrier, count).
-      __threadfence();
+      // Count each pair in for (token row, block): after the barrier, the counting
+      // thread's fence orders every warp's o stores of the unit before its count.
+      // The last of a row's k (+ shared) pairs queues the row's combine.
       named_bar(kBarEpi, kEpiThreads);
-      if (et < m.n) {
-        const int64_t p = __ldcg(rows + et);
-        const int t = int(p < tk ? p / a.k : p - tk);
+      if (ew == 0 && pr >= 0) {
+        const int t = int(pr < tk ? pr / a.k : pr - tk);
+        __threadfence();
         if (atomicAdd(a.comb_cnt + int64_t(t) * hbd + m.blk, 1u) == target - 1u) {
           const uint32_t idx = atomicAdd(&sm.n_jobs, 1u);
           sm.jobs[idx] = uint32_t(t);
@@ -809,15 +810,16 @@ cudaError_t launch_cfg(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaS
 
 }  // namespace
 
-// A chunk never holds more rows than the step (an expert has at most T rows),
-// so the chunk size follows T: the smallest of 16, 32, 64, 128 that covers it.
-int mma_chunk_rows(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128; }
+// Chunk size. A chunk never holds more rows than the step (an expert has at
+// most T rows), so T <= 16 uses 16-row chunks and 11 stages. Larger steps use
+// 32-row chunks and 10 stages. Chunks of 64 or 128 rows (8 or 6 stages) were
+// slower on GB300 at 48 to 384 rows: the deeper ring is worth more than the
+// weight blocks that the chunks of a hot expert read again from L2.
+int mma_chunk_rows(int T) { return T <= 16 ? 16 : 32; }
 
 cudaError_t prepare_experts_mma() {
   cudaError_t e = prepare_cfg<Cfg16>();
   if (e == cudaSuccess) e = prepare_cfg<Cfg32>();
-  if (e == cudaSuccess) e = prepare_cfg<Cfg64>();
-  if (e == cudaSuccess) e = prepare_cfg<Cfg128>();
   return e;
 }
 
@@ -825,8 +827,6 @@ cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int gri
   switch (chunk_rows) {
     case 16: return launch_cfg<Cfg16>(maps, a, grid, st);
     case 32: return launch_cfg<Cfg32>(maps, a, grid, st);
-    case 64: return launch_cfg<Cfg64>(maps, a, grid, st);
-    case 128: return launch_cfg<Cfg128>(maps, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }

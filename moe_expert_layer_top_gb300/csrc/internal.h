@@ -18,9 +18,9 @@ constexpr int kStages = 5;              // pipeline depth
 constexpr int kRouteThreads = 1024;     // route kernel: block 0 (router + placement)
 constexpr int kQuantThreads = 256;      // route kernel: x-quantisation blocks (one group per thread)
 constexpr int kMaxTimedCalls = 4096;
-constexpr int kChunkRowsMax = 128;      // tensor-core expert kernel: most token rows per chunk (MMA N)
+constexpr int kChunkRowsMax = 32;       // tensor-core expert kernel: most token rows per chunk (MMA N)
 constexpr int kMmaDownRows = 128;       // tensor-core expert kernel: W_down rows per down unit
-constexpr int kMmaMinRowsDefault = 32;  // steps with at least this many rows take the tensor-core kernel
+constexpr int kMmaMinRowsDefault = 1;   // steps with at least this many rows take the tensor-core kernel
 
 // Device scratch and schedule of one plan (all sized for max_rows).
 struct Scratch {
@@ -92,7 +92,7 @@ struct RouteArgs {
   int32_t *n_tiles;
   int32_t *chunk_list;  // NULL: no chunk list (the GEMV expert kernel only)
   int32_t *n_chunks;
-  int chunk_rows;       // rows per chunk (16, 32, 64 or 128)
+  int chunk_rows;       // rows per chunk (16 or 32)
   uint32_t *ready;
   int n_tiles_max;
   uint32_t *comb_cnt;

@@ -11,10 +11,9 @@
 // - Runtime enqueues two kernels:
 //     1. route + place + quantise x;
 //     2. a persistent expert kernel (gate/up, down and the fused combine),
-//        launched with Programmatic Dependent Launch. Steps with fewer rows
-//        than plan->mma_min_rows take the CUDA-core GEMV kernel
-//        (experts.cu); larger ones take the tensor-core kernel
-//        (experts_mma.cu). MOE_FLAG_PATH_GEMV / MOE_FLAG_PATH_MMA pin one.
+//        launched with Programmatic Dependent Launch: the tensor-core kernel
+//        (experts_mma.cu), or the CUDA-core GEMV kernel (experts.cu) when
+//        the plan was built with MOE_FLAG_PATH_GEMV.
 //   It allocates nothing and does not synchronise.
 #include <cuda_runtime.h>
 #include <stdint.h>

@@ -42,10 +42,10 @@ def routed_only(w: MoEWeightsMXFP8) -> MoEWeightsMXFP8:
     return MoEWeightsMXFP8(w.w_gate, w.s_gate, w.w_up, w.s_up, w.w_down, w.s_down)
 
 
-# flags 0: the expert kernel the benchmark times (GEMV below 32 rows, MMA from
-# 32 rows); the pinned cases run the other kernel on the same workload.
+# flags 0: the expert kernel the benchmark times (the tensor-core kernel); the
+# pinned cases run the CUDA-core GEMV kernel on the same workload.
 FULL = [("bs1", 0), ("bs4", 0), ("bs16", 0), ("bs64", 0),
-        ("bs1", abi.MOE_FLAG_PATH_MMA), ("bs4", abi.MOE_FLAG_PATH_MMA), ("bs16", abi.MOE_FLAG_PATH_GEMV)]
+        ("bs1", abi.MOE_FLAG_PATH_GEMV), ("bs4", abi.MOE_FLAG_PATH_GEMV), ("bs16", abi.MOE_FLAG_PATH_GEMV)]
 
 
 @pytest.mark.parametrize("name,flags", FULL, ids=[f"{n}_{'default' if f == 0 else 'mma' if f == abi.MOE_FLAG_PATH_MMA else 'gemv'}"

@@ -222,16 +222,19 @@ def test_path_flags_are_exclusive():
         MoEStep(H, I, E, k, w, T, 0, abi.MOE_FLAG_PATH_GEMV | abi.MOE_FLAG_PATH_MMA)
 
 
-def test_default_path_switches_at_32_rows():
-    """Without a path flag, 31 rows run the GEMV kernel and 32 rows the MMA
-    kernel. Both results match the oracle."""
+def test_default_path_is_the_tensor_core_kernel():
+    """Without a path flag every step runs the MMA kernel: its output is the
+    pinned MMA kernel's, bit for bit, and matches the oracle."""
     H, E, k, I = 512, 8, 2, 256
-    for T in (31, 32):
+    for T in (6, 40):
         g = GpuRun(T, H, E, k, I, "zipf", seed=5).run()
         assert g.status_code == abi.MOE_OK
+        pinned = GpuRun(T, H, E, k, I, "zipf", seed=5, weights=g.weights, flags=abi.MOE_FLAG_PATH_MMA).run()
+        np.testing.assert_array_equal(g.y_bits, pinned.y_bits)
         r = oracle.moe_step(g.x_bits, g.lg, k, oracle_experts(5, E, H, I))
         check_y(g.y_bits, r["y"])
         g.close()
+        pinned.close()
 
 
 def test_timing_flag_records_expert_kernel():
