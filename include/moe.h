@@ -236,7 +236,8 @@ moe_status_t moe_plan_diagnostics(void *plan, int64_t *out8);
  * about 50 rows. It also returns the Guard's errors, as moe_plan does.
  * Every call uses the same array. Calls that overlap on the GPU (two streams,
  * or two host threads) race and corrupt each other's results. Everything that
- * must start at zero is cleared by the step itself.
+ * must start at zero is cleared by the step itself, except one counter at the
+ * start of the array that every completed step leaves at zero.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and sets kernel
  * attributes. Make that first call before any stream capture. Each call also

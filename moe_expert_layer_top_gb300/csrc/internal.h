@@ -36,7 +36,7 @@ struct Scratch {
   int32_t *n_chunks;    // [1]
   uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile (per chunk on the tensor-core path)
   uint32_t *comb_cnt;   // [Tmax][down blocks] down blocks of a token row finished (fused combine)
-  uint32_t *work;       // [2] unit counter, abort flag
+  uint32_t *work;       // [4] unit counter, abort flag, route-kernel ticket
   int32_t *status;      // [1] plan-owned status word
   int64_t *diag;        // [8] first device-side error of the last step (site, unit, tile, ...)
   uint8_t *xq, *xs;     // [Tmax][H], [Tmax][H/32]
@@ -98,6 +98,7 @@ struct RouteArgs {
   uint32_t *comb_cnt;
   int n_comb;
   uint32_t *work;
+  uint32_t *ticket;     // phase-2 ticket of the route grid (zero between steps)
   int32_t *status;
   int64_t *diag;
   uint8_t *xq, *xs;

@@ -196,7 +196,7 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   const size_t o_slot = take(pairs_routed * 4), o_rows = take(size_t(E + 1) * Tm * 4);
   const size_t o_tl = take(size_t(p->n_tiles_max) * 4), o_nt = take(4);
   const size_t o_cl = take(size_t(p->n_tiles_max) * 4), o_nc = take(4);
-  const size_t o_ready = take(size_t(p->n_tiles_max) * 4), o_work = take(8), o_status = take(4);
+  const size_t o_ready = take(size_t(p->n_tiles_max) * 4), o_work = take(16), o_status = take(4);
   const int down_blocks = experts_down_blocks(H, I) > H / kMmaDownRows ? experts_down_blocks(H, I) : H / kMmaDownRows;
   const size_t o_comb = take(size_t(Tm) * down_blocks * 4);
   const size_t o_diag = take(8 * 8);
@@ -310,6 +310,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ra.comb_cnt = s.comb_cnt;
   ra.n_comb = T * (mma ? c.hidden / kMmaDownRows : experts_down_blocks(c.hidden, c.intermediate));
   ra.work = s.work;
+  ra.ticket = s.work + 2;
   ra.status = status;
   ra.diag = s.diag;
   ra.xq = s.xq;

@@ -1,13 +1,17 @@
 // route.cu — router top-k + combine weights, sort-free tile placement, and
 // MXFP8 quantisation of the token rows, in one launch.
 //
-// Block 0 routes and places.
-//  - Top-k per token row uses one warp per row, in k rounds of warp argmax.
-//  - The combine weights are a softmax over the selected logits in binary32,
-//    using exp_rn.
-//  - Token bitmaps are built per expert in shared memory.
-//  - Placement uses population counts: rank(t, e) = popc(bits of expert e
-//    below t). Tile = rank / 8 and row = rank % 8.
+// Two phases in one grid:
+//  1. ceil(T/32) routing blocks route their 32 token rows each, while the
+//     other blocks quantise x.
+//     - Top-k per token row uses one warp per row, in k rounds of warp argmax.
+//     - The combine weights are a softmax over the selected logits in
+//       binary32, using exp_rn.
+//  2. The last routing block to finish phase 1 places the pairs (it takes a
+//     ticket after a fence; no block waits for another).
+//     - Token bitmaps are built per expert in shared memory.
+//     - Placement uses population counts: rank(t, e) = popc(bits of expert e
+//       below t). Tile = rank / 8 and row = rank % 8.
 // This follows "SGLang's Low-Latency Mode Boosts DeepSeek-V4.1-Flash Speed by
 // 1.56x on AMD", "NVIDIA overlaps the dependency chain", bullet "Routing
 // without sorting". A bitmap and population counts place the 8-row tiles with
@@ -21,9 +25,9 @@
 // The lists' per-expert offsets come from block-wide prefixes over the E+1
 // tile (chunk) counts. That is work enumeration, not row placement.
 //
-// Blocks 1.. quantise x to MXFP8 (one 32-group per thread). "Beyond Day-0"
-// 2.1 fuses activation quantisation into the producer, and here it shares
-// the launch with the router.
+// x is quantised to MXFP8 one 32-group per thread. "Beyond Day-0" 2.1 fuses
+// activation quantisation into the producer, and here it shares the launch
+// with the router.
 #include <stdint.h>
 
 #include "device.cuh"
@@ -84,17 +88,21 @@ struct RouteSmem {
   int32_t tiles[kRouteThreads];
   int32_t offs[kRouteThreads];
   int32_t warp_sums[kRouteThreads / 32];
+  int32_t last;  // this block finished phase 1 last
 };
 
 // Top-k and combine weights, one warp per token row. Each lane keeps its NC
 // candidates (lane, lane + 32, ...) in registers as 64-bit keys: the
 // order-preserving bits of the logit, then the complemented expert id. So the
 // largest key is the largest logit and, among equal logits, the lower id.
+// bm: the block's bitmap in shared memory when one block routes every row
+// (the bits are set here); NULL when the last block builds it in phase 2.
 template <int NC>
 __device__ __forceinline__ void route_topk(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, k = a.k, T = a.T, W = a.words;
-  for (int t = warp; t < T; t += kRouteThreads / 32) {
+  constexpr int kWarps = kRouteThreads / 32;
+  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
     const float *row = a.logits + int64_t(t) * E;
     uint64_t key[NC];
 #pragma unroll
@@ -141,7 +149,7 @@ __device__ __forceinline__ void route_topk(const RouteArgs &a, RouteSmem &sm, ui
       const int id = sm.sel_i[warp][lane];
       a.topk_ids[int64_t(t) * k + lane] = id;
       a.topk_w[int64_t(t) * k + lane] = __fdiv_rn(e, s);
-      atomicOr(&bm[id * W + (t >> 5)], 1u << (t & 31));
+      if (bm) atomicOr(&bm[id * W + (t >> 5)], 1u << (t & 31));
     }
     __syncwarp();
   }
@@ -174,29 +182,22 @@ __device__ __forceinline__ int block_exclusive_scan(RouteSmem &sm, int v, int &t
   return x - v + (warp ? sm.warp_sums[warp - 1] : 0);
 }
 
-__device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
+// Phase 2 (one block): bitmaps, counts, work lists and placement of every pair.
+// have_bitmap: phase 1 already set the bits in this block's shared memory.
+__device__ void route_place(const RouteArgs &a, RouteSmem &sm, uint32_t *bm, bool have_bitmap) {
   const int tid = threadIdx.x;
   const int E = a.E, k = a.k, T = a.T, W = a.words;
 
-  if (tid < 8) a.diag[tid] = 0;
-  if (tid == 0) {
-    *a.status = MOE_OK;  // start of the step
-    a.work[0] = 0;       // unit counter
-    a.work[1] = 0;       // abort flag
+  if (!have_bitmap) {
+    for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0;
+    __syncthreads();
+    // the selected experts were written by every block of phase 1: read through L2
+    for (int p = tid; p < T * k; p += blockDim.x) {
+      const int t = p / k;
+      const int id = __ldcg(a.topk_ids + p);
+      atomicOr(&bm[id * W + (t >> 5)], 1u << (t & 31));
+    }
   }
-  for (int i = tid; i < a.n_tiles_max; i += blockDim.x) a.ready[i] = 0;
-  for (int i = tid; i < a.n_comb; i += blockDim.x) a.comb_cnt[i] = 0;
-  for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0;
-  __syncthreads();
-
-  // --- top-k + combine weights: one warp per token row
-  const int nc = (E + 31) / 32;
-  if (nc <= 1) route_topk<1>(a, sm, bm);
-  else if (nc <= 2) route_topk<2>(a, sm, bm);
-  else if (nc <= 4) route_topk<4>(a, sm, bm);
-  else if (nc <= 8) route_topk<8>(a, sm, bm);
-  else if (nc <= 16) route_topk<16>(a, sm, bm);
-  else route_topk<32>(a, sm, bm);
   __syncthreads();
 
   // --- counts and tiles per expert (index E: the shared expert, every row)
@@ -242,7 +243,7 @@ __device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
   // --- placement: rank by population count of lower token bits
   for (int p = tid; p < T * k; p += blockDim.x) {
     const int t = p / k;
-    const int e = a.topk_ids[p];
+    const int e = __ldcg(a.topk_ids + p);
     const uint32_t *b = bm + e * W;
     int rank = __popc(b[t >> 5] & ((1u << (t & 31)) - 1u));
     for (int w = 0; w < (t >> 5); ++w) rank += __popc(b[w]);
@@ -254,20 +255,67 @@ __device__ void route_block(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
   for (int i = tid; i < E * W; i += blockDim.x) a.bitmap[i] = bm[i];
 }
 
+// Blocks [0, R) route R*32 token rows (R = ceil(T/32)); the blocks after them
+// quantise x, one 32-group per thread.
+__device__ __host__ __forceinline__ int route_blocks(int T) { return (T + kRouteThreads / 32 - 1) / (kRouteThreads / 32); }
+
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a) {
   extern __shared__ __align__(16) unsigned char route_smem[];
   // Let the expert kernel's blocks get scheduled early; it waits for this grid before reading.
   pdl_launch_dependents();
-  if (blockIdx.x == 0) {
-    RouteSmem &sm = *reinterpret_cast<RouteSmem *>(route_smem);
-    uint32_t *bm = reinterpret_cast<uint32_t *>(route_smem + sizeof(RouteSmem));
-    route_block(a, sm, bm);
+  RouteSmem &sm = *reinterpret_cast<RouteSmem *>(route_smem);
+  uint32_t *bm = reinterpret_cast<uint32_t *>(route_smem + sizeof(RouteSmem));
+  const int tid = threadIdx.x;
+  const int R = route_blocks(a.T);
+  // the step's counters (the expert kernel reads them after this grid completes)
+  const int64_t gtid = int64_t(blockIdx.x) * blockDim.x + tid, gstride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = gtid; i < a.n_tiles_max; i += gstride) a.ready[i] = 0;
+  for (int64_t i = gtid; i < a.n_comb; i += gstride) a.comb_cnt[i] = 0;
+
+  if (int(blockIdx.x) >= R) {  // x quantisation
+    const int64_t groups = int64_t(a.T) * (a.H / kGroup);
+    const int64_t qstride = int64_t(gridDim.x - R) * blockDim.x;
+    for (int64_t g = int64_t(blockIdx.x - R) * blockDim.x + tid; g < groups; g += qstride)
+      quantize_group32(a.x + g * kGroup, a.xq + g * kGroup, a.xs + g);
     return;
   }
-  const int64_t groups = int64_t(a.T) * (a.H / kGroup);
-  for (int64_t g = int64_t(blockIdx.x - 1) * blockDim.x + threadIdx.x; g < groups;
-       g += int64_t(gridDim.x - 1) * blockDim.x)
-    quantize_group32(a.x + g * kGroup, a.xq + g * kGroup, a.xs + g);
+  if (blockIdx.x == 0) {
+    if (tid < 8) a.diag[tid] = 0;
+    if (tid == 0) {
+      *a.status = MOE_OK;  // start of the step
+      a.work[0] = 0;       // unit counter
+      a.work[1] = 0;       // abort flag
+    }
+  }
+  // One routing block keeps the bitmap in shared memory from the start and
+  // needs no ticket.
+  const bool single = R == 1;
+  if (single) {
+    for (int i = tid; i < a.E * a.words; i += blockDim.x) bm[i] = 0;
+    __syncthreads();
+  }
+
+  // --- phase 1: top-k + combine weights, one warp per row
+  uint32_t *bits = single ? bm : nullptr;
+  const int nc = (a.E + 31) / 32;
+  if (nc <= 1) route_topk<1>(a, sm, bits);
+  else if (nc <= 2) route_topk<2>(a, sm, bits);
+  else if (nc <= 4) route_topk<4>(a, sm, bits);
+  else if (nc <= 8) route_topk<8>(a, sm, bits);
+  else if (nc <= 16) route_topk<16>(a, sm, bits);
+  else route_topk<32>(a, sm, bits);
+
+  // --- phase 2 in the last routing block to finish phase 1 (ticket after a
+  // fence; the ticket counter wraps back to zero on the last ticket)
+  if (!single) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sm.last = atomicInc(a.ticket, uint32_t(R - 1)) == uint32_t(R - 1);
+    __syncthreads();
+    if (!sm.last) return;
+    __threadfence();  // the other blocks' results, before they are read
+  }
+  route_place(a, sm, bm, single);
 }
 
 size_t route_smem_bytes(int E, int words) { return sizeof(RouteSmem) + size_t(E) * words * sizeof(uint32_t); }
@@ -276,11 +324,15 @@ cudaError_t prepare_route(size_t smem) {
   return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
 }
 
+// R routing blocks, then one block per 1024 32-groups of x.
+int route_grid(int T, int H) {
+  const int64_t groups = int64_t(T) * (H / kGroup);
+  return route_blocks(T) + int((groups + kRouteThreads - 1) / kRouteThreads);
+}
+
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
   const size_t smem = route_smem_bytes(a.E, a.words);
-  const int64_t groups = int64_t(a.T) * (a.H / kGroup);
-  const int qblocks = int((groups + kRouteThreads - 1) / kRouteThreads);
-  route_kernel<<<1 + qblocks, kRouteThreads, smem, st>>>(a);
+  route_kernel<<<route_grid(a.T, a.H), kRouteThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -86,10 +86,15 @@ struct Layout {
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
+// The array starts with a control area that keeps its value between calls of
+// any shape: the route kernel's phase-2 ticket, which every step leaves at
+// zero (the array itself starts zeroed). The step's buffers follow it.
+constexpr size_t kControlBytes = 256;
+
 // Scratch for a T-row step (the same buffers moe_plan sizes for max_rows = T).
 Layout layout_for(const moe_config_t &c, int T, int words, int n_tiles_max) {
   Layout L{};
-  size_t off = 0;
+  size_t off = kControlBytes;
   auto take = [&](size_t bytes) {
     const size_t o = off;
     off += up256(bytes);
@@ -185,6 +190,7 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ra.comb_cnt = reinterpret_cast<uint32_t *>(base + L.comb);
   ra.n_comb = T * experts_down_blocks(c.hidden, c.intermediate);
   ra.work = reinterpret_cast<uint32_t *>(base + L.work);
+  ra.ticket = reinterpret_cast<uint32_t *>(base);  // control area: zero between steps
   ra.status = status;
   ra.diag = reinterpret_cast<int64_t *>(base + L.diag);
   ra.xq = base + L.xq;
