@@ -304,6 +304,18 @@ def time_e2e(step, wl, seed, steps, warmup):
             "d2h_bytes_per_step": d2h, "median_us": statistics.median(times) * 1e6}
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise max of per-rank values over the process group (the slowest
+    replica sets the step time). One rank: the values themselves."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -354,12 +366,7 @@ def run_gpu(args):
         dist.barrier()
     clock_rows = clocks.stop()
 
-    ms = main["ms_mean"]
-    exp_ms = main["expert_ms_mean"]
-    if world > 1:
-        t = torch.tensor([ms, exp_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, exp_ms = float(t[0]), float(t[1])
+    ms, exp_ms = max_over_ranks([main["ms_mean"], main["expert_ms_mean"]], world, "cuda")
 
     e2e = None if args.no_e2e else time_e2e(main["step"], wl, seed, max(args.steps, 10), 3)
 

@@ -1,0 +1,59 @@
+"""The multi-GPU path of this build is "replicas only": every rank runs its
+own step on its own GPU, with no data-path collective. bench.py takes the max
+per-step time over ranks, and rank 0 alone prints the line. These tests run
+that logic on CPU with world_size 2 over gloo, and check that the reference
+arm leaves ranks other than 0 idle."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # rank r reports a step of (r + 1) ms and an expert kernel of (3 - r) ms
+    got = bench.max_over_ranks([rank + 1.0, 3.0 - rank], world, "cpu")
+    out.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_size_2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0] == res[1] == [2.0, 3.0]
+
+
+def test_max_over_ranks_single_rank_is_identity():
+    import bench
+    assert bench.max_over_ranks([1.5, 2.5], 1, "cpu") == [1.5, 2.5]
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, env=env, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
