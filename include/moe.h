@@ -180,6 +180,22 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
                          void *y, const moe_taps_t *taps, int32_t *d_status,
                          void *cuda_stream);
 
+/* Runtime with a device-side row count, for CUDA-graph capture and replay.
+ * Same as moe_forward, except that the kernels read the step's T from
+ * *d_T (device int32, 4-byte aligned) when they run, so one captured graph
+ * serves any T in [0, max_rows]. x, logits and y are sized for max_rows
+ * rows; rows at or past T are neither read nor written. A value outside
+ * [0, max_rows] is clamped and MOE_ERR_DEVICE_BOUNDS is written to the
+ * status word; T = 0 is an empty step. Always runs the tensor-core expert
+ * kernel (MOE_ERR_UNSUPPORTED on a plan built with MOE_FLAG_PATH_GEMV) with
+ * the chunk size for max_rows. No taps. Allocates nothing, does not
+ * synchronise. Source: "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in
+ * SGLang", section 3.1: lengths are read from GPU memory, so a replayed
+ * CUDA graph uses the current length, and the work follows the actual
+ * length rather than the capacity. */
+moe_status_t moe_forward_dev(void *plan, const void *x, const float *logits, const int32_t *d_T, void *y,
+                             int32_t *d_status, void *cuda_stream);
+
 /* Runtime with host buffers: copies x and logits from host memory into
  * plan-owned device buffers, runs moe_forward and copies y back to y_host. It
  * then synchronises cuda_stream and returns the device-side status of the

@@ -33,6 +33,7 @@ EXPORTED = (
     "moe_status_string",
     "moe_plan",
     "moe_forward",
+    "moe_forward_dev",
     "moe_forward_host",
     "moe_quantize_mxfp8",
     "moe_kernel_times",
@@ -112,6 +113,8 @@ def load(path: str | None = None):
     lib.moe_plan_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32)]
     lib.moe_plan_diagnostics.restype = ctypes.c_int
     lib.moe_plan_diagnostics.argtypes = [_P, ctypes.POINTER(ctypes.c_int64)]
+    lib.moe_forward_dev.restype = ctypes.c_int
+    lib.moe_forward_dev.argtypes = [_P, _P, _P, _P, _P, _P, _P]
     lib.moe_forward_static_scratch.restype = ctypes.c_int
     lib.moe_forward_static_scratch.argtypes = [ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeWeights), _P, _P,
                                                ctypes.c_int32, _P, _P, _P]
@@ -210,6 +213,12 @@ def moe_plan_diagnostics(plan: int) -> list[int]:
     out = (ctypes.c_int64 * 8)()
     check("moe_plan_diagnostics", lib.moe_plan_diagnostics(plan, out))
     return list(out)
+
+
+def moe_forward_dev(plan, x, logits, d_T, y, d_status=None, stream=None) -> int:
+    """One MoE step whose row count is read from device memory (int32 at d_T)."""
+    lib = load()
+    return lib.moe_forward_dev(plan, ptr(x), ptr(logits), ptr(d_T), ptr(y), ptr(d_status), stream_ptr(stream))
 
 
 def moe_forward_static_scratch(config: MoeConfig, weights: MoeWeights, x, logits, T: int, y, d_status=None,

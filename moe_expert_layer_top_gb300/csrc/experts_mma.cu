@@ -421,10 +421,10 @@ struct LoaderRows {
 };
 
 template <int NMAX>
-__device__ __forceinline__ LoaderRows<NMAX> loader_rows(const ExpertArgs &a, const MUnit &m, int tau) {
+__device__ __forceinline__ LoaderRows<NMAX> loader_rows(const ExpertArgs &a, int T, const MUnit &m, int tau) {
   LoaderRows<NMAX> lr;
   const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
-  const int64_t tk = int64_t(a.T) * a.k;
+  const int64_t tk = int64_t(T) * a.k;
   const int r0 = tau >> 3;
 #pragma unroll
   for (int i = 0; i < NMAX / 16; ++i) {
@@ -517,8 +517,8 @@ __device__ __forceinline__ int wait_chunk_ready(const ExpertArgs &a, int chunk, 
 }
 
 template <class C>
-__device__ void mma_loaders(const ExpertArgs &a, typename C::Smem &sm, const Sched &sc, int n_chunks, int mbg,
-                            int hbd) {
+__device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, const Sched &sc, int n_chunks,
+                            int mbg, int hbd) {
   constexpr int kMStages = C::STAGES;
   const int tau = int(threadIdx.x) - kWarpLoad * 32;
   const void *zero_src = a.xq;  // any valid address: zero-byte copies read nothing
@@ -544,7 +544,7 @@ __device__ void mma_loaders(const ExpertArgs &a, typename C::Smem &sm, const Sch
         while (gc < g) complete_oldest();
         if (!wait_chunk_ready(a, m.chunk, uint32_t(mbg), u)) break;
       }
-      lr = loader_rows<C::NMAX>(a, m, tau);
+      lr = loader_rows<C::NMAX>(a, T, m, tau);
       kc = 0;
       kcs = (m.down ? a.I : a.H) / kKC;
     }
@@ -572,11 +572,11 @@ __device__ void mma_loaders(const ExpertArgs &a, typename C::Smem &sm, const Sch
 // ------------------------------------------------------------------ epilogue (warps 6-9)
 
 template <class C>
-__device__ void mma_epilogue(const ExpertArgs &a, typename C::Smem &sm, uint32_t tmem, const Sched &sc, int n_chunks,
-                             int mbg, int hbd) {
+__device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, uint32_t tmem, const Sched &sc,
+                             int n_chunks, int mbg, int hbd) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ew = warp - kWarpEpi;
   const int et = ew * 32 + lane;
-  const int64_t tk = int64_t(a.T) * a.k;
+  const int64_t tk = int64_t(T) * a.k;
   const uint32_t target = uint32_t(a.k + a.shared);
   uint32_t nu = 0, xc = 0;  // units done, gate/up column slices done
   static_assert(C::NMAX <= 32, "one pair id per lane");
@@ -669,7 +669,7 @@ __device__ void mma_epilogue(const ExpertArgs &a, typename C::Smem &sm, uint32_t
       if (nj) {
         __threadfence();  // the other pairs' o stores, before these reads
         for (uint32_t jj = uint32_t(ew); jj < nj; jj += 4)
-          combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, a.T, a.k, a.shared, a.H, int(sm.jobs[jj]),
+          combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, T, a.k, a.shared, a.H, int(sm.jobs[jj]),
                                       int64_t(m.blk) * kBM, lane);
       }
       named_bar(kBarEpi, kEpiThreads);
@@ -716,6 +716,12 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
 
   // Everything below reads the router's outputs.
   pdl_wait_primary();
+  // the step's row count: a.T, or the device-side value (clamped as the route kernel does)
+  int T = a.T;
+  if (a.d_T) {
+    const int td = *reinterpret_cast<const volatile int32_t *>(a.d_T);
+    T = td < 0 ? 0 : (td > a.Tmax ? a.Tmax : td);
+  }
   const int n_chunks = __ldcg(a.n_chunks);
   const int mbg = a.I / 64, hbd = a.H / kBM;
   const Sched sc(n_chunks, mbg, hbd);
@@ -724,9 +730,9 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
   } else if (warp == kWarpMma) {
     if (lane == 0) mma_issuer<C>(a, sm, tmem, sc, n_chunks, mbg, hbd);
   } else if (warp < kWarpEpi) {
-    mma_loaders<C>(a, sm, sc, n_chunks, mbg, hbd);
+    mma_loaders<C>(a, T, sm, sc, n_chunks, mbg, hbd);
   } else {
-    mma_epilogue<C>(a, sm, tmem, sc, n_chunks, mbg, hbd);
+    mma_epilogue<C>(a, T, sm, tmem, sc, n_chunks, mbg, hbd);
   }
   __syncwarp();
   tmem_fence_before();

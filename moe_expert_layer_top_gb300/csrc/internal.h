@@ -81,7 +81,8 @@ struct Plan {
 struct RouteArgs {
   const float *logits;
   const uint16_t *x;
-  int T, H, E, k, shared, words, Tmax;
+  int T, H, E, k, shared, words, Tmax;  // T: the step's rows, or the grid's bound when d_T is set
+  const int32_t *d_T;   // device-side row count (clamped to Tmax), or NULL
   int32_t *topk_ids;
   float *topk_w;
   uint32_t *bitmap;
@@ -96,7 +97,7 @@ struct RouteArgs {
   uint32_t *ready;
   int n_tiles_max;
   uint32_t *comb_cnt;
-  int n_comb;
+  int comb_per_row;     // combine counters per token row
   uint32_t *work;
   uint32_t *ticket;     // phase-2 ticket of the route grid (zero between steps)
   int32_t *status;
@@ -108,6 +109,7 @@ struct ExpertArgs {
   const uint8_t *w_gate, *s_gate, *w_up, *s_up, *w_down, *s_down;
   const uint8_t *sh_w_gate, *sh_s_gate, *sh_w_up, *sh_s_up, *sh_w_down, *sh_s_down;
   int T, H, I, E, k, Tmax;
+  const int32_t *d_T;   // device-side row count (tensor-core kernel only), or NULL
   const int32_t *counts;
   const int32_t *rows_of;
   const int32_t *tile_list;

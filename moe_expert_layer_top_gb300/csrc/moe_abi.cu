@@ -267,27 +267,25 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   return MOE_OK;
 }
 
-moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t T, void *y,
-                         const moe_taps_t *taps, int32_t *d_status, void *cuda_stream) {
-  Plan *p = static_cast<Plan *>(plan);
-  if (!p) return MOE_ERR_INVALID_ARG;
-  if (T < 0 || T > p->cfg.max_rows) return MOE_ERR_INVALID_ARG;
-  if (T == 0) return MOE_OK;
-  if (!x || !logits || !y || !aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(logits) & 3u))
-    return MOE_ERR_INVALID_ARG;
-  if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return MOE_ERR_INVALID_ARG;
-  DeviceGuard dg(p->device);
-  if (!dg.ok) return MOE_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+}  // extern "C"
+
+namespace {
+
+// Enqueues one step: the route kernel, then an expert kernel with PDL.
+// T sizes the grids. With d_T set, the kernels read the step's row count
+// from device memory (clamped to max_rows) and the tensor-core kernel runs.
+moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T, const int32_t *d_T, void *y,
+                          bool h_tap, int32_t *d_status, cudaStream_t st) {
   const moe_config_t &c = p->cfg;
   Scratch &s = p->s;
   int32_t *status = d_status ? d_status : s.status;
-  const bool mma = T >= p->mma_min_rows;
+  const bool mma = d_T != nullptr || T >= p->mma_min_rows;
 
   RouteArgs ra;
   ra.logits = logits;
   ra.x = static_cast<const uint16_t *>(x);
   ra.T = T;
+  ra.d_T = d_T;
   ra.H = c.hidden;
   ra.E = c.num_experts;
   ra.k = c.top_k;
@@ -308,7 +306,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ra.ready = s.ready;
   ra.n_tiles_max = p->n_tiles_max;
   ra.comb_cnt = s.comb_cnt;
-  ra.n_comb = T * (mma ? c.hidden / kMmaDownRows : experts_down_blocks(c.hidden, c.intermediate));
+  ra.comb_per_row = mma ? c.hidden / kMmaDownRows : experts_down_blocks(c.hidden, c.intermediate);
   ra.work = s.work;
   ra.ticket = s.work + 2;
   ra.status = status;
@@ -331,6 +329,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ea.sh_w_down = p->w.sh_w_down;
   ea.sh_s_down = p->w.sh_s_down;
   ea.T = T;
+  ea.d_T = d_T;
   ea.H = c.hidden;
   ea.I = c.intermediate;
   ea.E = c.num_experts;
@@ -346,7 +345,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
   ea.xs = s.xs;
   ea.hq = s.hq;
   ea.hs = s.hs;
-  ea.h_bf16 = (taps && taps->h_bf16) ? s.h_bf16 : nullptr;
+  ea.h_bf16 = h_tap ? s.h_bf16 : nullptr;
   ea.o = s.o;
   ea.ready = s.ready;
   ea.comb_cnt = s.comb_cnt;
@@ -366,8 +365,41 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
     if (cudaEventRecord(p->ev_stop[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
     ++p->timed_calls;
   }
+  return MOE_OK;
+}
 
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t T, void *y,
+                         const moe_taps_t *taps, int32_t *d_status, void *cuda_stream) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > p->cfg.max_rows) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !logits || !y || !aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(logits) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(p->device);
+  if (!dg.ok) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const moe_status_t r = enqueue_step(p, x, logits, T, nullptr, y, taps && taps->h_bf16, d_status, st);
+  if (r != MOE_OK) return r;
   return copy_taps(p, taps, T, st);
+}
+
+moe_status_t moe_forward_dev(void *plan, const void *x, const float *logits, const int32_t *d_T, void *y,
+                             int32_t *d_status, void *cuda_stream) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p || !d_T || (reinterpret_cast<uintptr_t>(d_T) & 3u)) return MOE_ERR_INVALID_ARG;
+  if (p->cfg.flags & MOE_FLAG_PATH_GEMV) return MOE_ERR_UNSUPPORTED;
+  if (!x || !logits || !y || !aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(logits) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(p->device);
+  if (!dg.ok) return MOE_ERR_CUDA;
+  return enqueue_step(p, x, logits, p->cfg.max_rows, d_T, y, false, d_status, static_cast<cudaStream_t>(cuda_stream));
 }
 
 moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logits_host, int32_t T, void *y_host,

@@ -98,9 +98,9 @@ struct RouteSmem {
 // bm: the block's bitmap in shared memory when one block routes every row
 // (the bits are set here); NULL when the last block builds it in phase 2.
 template <int NC>
-__device__ __forceinline__ void route_topk(const RouteArgs &a, RouteSmem &sm, uint32_t *bm) {
+__device__ __forceinline__ void route_topk(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *bm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int E = a.E, k = a.k, T = a.T, W = a.words;
+  const int E = a.E, k = a.k, W = a.words;
   constexpr int kWarps = kRouteThreads / 32;
   for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
     const float *row = a.logits + int64_t(t) * E;
@@ -184,9 +184,9 @@ __device__ __forceinline__ int block_exclusive_scan(RouteSmem &sm, int v, int &t
 
 // Phase 2 (one block): bitmaps, counts, work lists and placement of every pair.
 // have_bitmap: phase 1 already set the bits in this block's shared memory.
-__device__ void route_place(const RouteArgs &a, RouteSmem &sm, uint32_t *bm, bool have_bitmap) {
+__device__ void route_place(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *bm, bool have_bitmap) {
   const int tid = threadIdx.x;
-  const int E = a.E, k = a.k, T = a.T, W = a.words;
+  const int E = a.E, k = a.k, W = a.words;
 
   if (!have_bitmap) {
     for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0;
@@ -266,16 +266,28 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
   RouteSmem &sm = *reinterpret_cast<RouteSmem *>(route_smem);
   uint32_t *bm = reinterpret_cast<uint32_t *>(route_smem + sizeof(RouteSmem));
   const int tid = threadIdx.x;
-  const int R = route_blocks(a.T);
+  // The step's row count: a.T, or the value at a.d_T (clamped to the plan's
+  // max_rows) when the step was enqueued with a device-side row count. The
+  // grid is sized for a.T either way.
+  int T = a.T;
+  bool bad_T = false;
+  if (a.d_T) {
+    const int td = *reinterpret_cast<const volatile int32_t *>(a.d_T);
+    bad_T = td < 0 || td > a.Tmax;
+    T = td < 0 ? 0 : (td > a.Tmax ? a.Tmax : td);
+  }
+  const int Rg = route_blocks(a.T);  // routing blocks of the grid
+  const int R = route_blocks(T);     // routing blocks with rows
   // the step's counters (the expert kernel reads them after this grid completes)
   const int64_t gtid = int64_t(blockIdx.x) * blockDim.x + tid, gstride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t n_comb = int64_t(T) * a.comb_per_row;
   for (int64_t i = gtid; i < a.n_tiles_max; i += gstride) a.ready[i] = 0;
-  for (int64_t i = gtid; i < a.n_comb; i += gstride) a.comb_cnt[i] = 0;
+  for (int64_t i = gtid; i < n_comb; i += gstride) a.comb_cnt[i] = 0;
 
-  if (int(blockIdx.x) >= R) {  // x quantisation
-    const int64_t groups = int64_t(a.T) * (a.H / kGroup);
-    const int64_t qstride = int64_t(gridDim.x - R) * blockDim.x;
-    for (int64_t g = int64_t(blockIdx.x - R) * blockDim.x + tid; g < groups; g += qstride)
+  if (int(blockIdx.x) >= Rg) {  // x quantisation
+    const int64_t groups = int64_t(T) * (a.H / kGroup);
+    const int64_t qstride = int64_t(gridDim.x - Rg) * blockDim.x;
+    for (int64_t g = int64_t(blockIdx.x - Rg) * blockDim.x + tid; g < groups; g += qstride)
       quantize_group32(a.x + g * kGroup, a.xq + g * kGroup, a.xs + g);
     return;
   }
@@ -285,8 +297,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
       *a.status = MOE_OK;  // start of the step
       a.work[0] = 0;       // unit counter
       a.work[1] = 0;       // abort flag
+      if (bad_T) report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
+      if (T == 0) {        // an empty step: empty work lists
+        *a.n_tiles = 0;
+        if (a.chunk_list) *a.n_chunks = 0;
+      }
     }
   }
+  if (int(blockIdx.x) >= R) return;  // no rows for this routing block
   // One routing block keeps the bitmap in shared memory from the start and
   // needs no ticket.
   const bool single = R == 1;
@@ -298,12 +316,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
   // --- phase 1: top-k + combine weights, one warp per row
   uint32_t *bits = single ? bm : nullptr;
   const int nc = (a.E + 31) / 32;
-  if (nc <= 1) route_topk<1>(a, sm, bits);
-  else if (nc <= 2) route_topk<2>(a, sm, bits);
-  else if (nc <= 4) route_topk<4>(a, sm, bits);
-  else if (nc <= 8) route_topk<8>(a, sm, bits);
-  else if (nc <= 16) route_topk<16>(a, sm, bits);
-  else route_topk<32>(a, sm, bits);
+  if (nc <= 1) route_topk<1>(a, T, sm, bits);
+  else if (nc <= 2) route_topk<2>(a, T, sm, bits);
+  else if (nc <= 4) route_topk<4>(a, T, sm, bits);
+  else if (nc <= 8) route_topk<8>(a, T, sm, bits);
+  else if (nc <= 16) route_topk<16>(a, T, sm, bits);
+  else route_topk<32>(a, T, sm, bits);
 
   // --- phase 2 in the last routing block to finish phase 1 (ticket after a
   // fence; the ticket counter wraps back to zero on the last ticket)
@@ -315,7 +333,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
     if (!sm.last) return;
     __threadfence();  // the other blocks' results, before they are read
   }
-  route_place(a, sm, bm, single);
+  route_place(a, T, sm, bm, single);
 }
 
 size_t route_smem_bytes(int E, int words) { return sizeof(RouteSmem) + size_t(E) * words * sizeof(uint32_t); }

@@ -168,6 +168,7 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ra.logits = logits;
   ra.x = static_cast<const uint16_t *>(x);
   ra.T = T;
+  ra.d_T = nullptr;
   ra.H = c.hidden;
   ra.E = c.num_experts;
   ra.k = c.top_k;
@@ -188,7 +189,7 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ra.ready = reinterpret_cast<uint32_t *>(base + L.ready);
   ra.n_tiles_max = n_tiles_max;
   ra.comb_cnt = reinterpret_cast<uint32_t *>(base + L.comb);
-  ra.n_comb = T * experts_down_blocks(c.hidden, c.intermediate);
+  ra.comb_per_row = experts_down_blocks(c.hidden, c.intermediate);
   ra.work = reinterpret_cast<uint32_t *>(base + L.work);
   ra.ticket = reinterpret_cast<uint32_t *>(base);  // control area: zero between steps
   ra.status = status;
@@ -211,6 +212,7 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ea.sh_w_down = weights->sh_w_down;
   ea.sh_s_down = weights->sh_s_down;
   ea.T = T;
+  ea.d_T = nullptr;
   ea.H = c.hidden;
   ea.I = c.intermediate;
   ea.E = c.num_experts;

@@ -75,6 +75,14 @@ class MoEStep:
         abi.check("moe_forward", abi.moe_forward(self.plan, x, logits, T, y, taps, d_status, st))
         return y
 
+    def forward_dev(self, x: torch.Tensor, logits: torch.Tensor, d_T: torch.Tensor, y: torch.Tensor,
+                    d_status: torch.Tensor | None = None, stream=None) -> None:
+        """A step whose row count is read on the device from d_T (int32, one element):
+        capture it once in a CUDA graph and replay it for any T <= max_rows.
+        x, logits and y hold max_rows rows; rows at or past T are not touched."""
+        st = stream if stream is not None else torch.cuda.current_stream(x.device)
+        abi.check("moe_forward_dev", abi.moe_forward_dev(self.plan, x, logits, d_T, y, d_status, st))
+
     def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, y_host: torch.Tensor, stream=None) -> int:
         st = stream if stream is not None else torch.cuda.current_stream()
         return abi.moe_forward_host(self.plan, x_host, logits_host, x_host.shape[0], y_host, st)
