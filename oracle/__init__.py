@@ -27,7 +27,7 @@ Sources, cited by page title and section:
   "MiniMax-M3: Connecting Attention and Experts". Each expert does its
   up/gate and down projections, for the shared and the routed experts.
 * OCP Microscaling Formats (MX) Specification v1.0:
-  - the E4M3 element encoding;
+  - the E4M3 and E2M1 element encodings (MXFP8, MXFP4);
   - the UE8M0 scale;
   - the rule for choosing a group's shared scale.
 
@@ -37,14 +37,21 @@ brute force, closed forms, hand-worked examples in ``tests/golden/`` and
 special cases that reduce to textbook routines.
 """
 from .formats import (  # noqa: F401
+    E2M1_MAX,
     E4M3_MAX,
     bf16_bits_to_f64,
+    e2m1_decode,
+    e2m1_encode,
     e4m3_decode,
     e4m3_encode,
     f32_to_bf16_bits,
+    mxfp4_dequantize,
+    mxfp4_quantize,
     mxfp8_dequantize,
     mxfp8_quantize,
+    pack_e2m1,
     ue8m0_value,
+    unpack_e2m1,
 )
 from .routing import exp_rn, placement, softmax_topk_weights, topk_ids  # noqa: F401
 from .step import ExpertWeights, expert_weights_from_synth, moe_step  # noqa: F401

@@ -135,3 +135,98 @@ def mxfp8_dequantize(q, s) -> np.ndarray:
     n = q.shape[-1]
     vals = e4m3_decode(q).reshape(q.shape[:-1] + (n // GROUP, GROUP))
     return (vals * ue8m0_value(s)[..., None]).reshape(q.shape)
+
+
+# --------------------------------------------------------------------------- e2m1 / MXFP4
+# OCP MX v1.0, FP4 element E2M1: 1 sign bit, 2 exponent bits (bias 1), 1
+# mantissa bit. There are no infinities or NaNs. The values are
+# +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}; the largest is 6 = 1.5 * 2^2, so emax_elem = 2.
+# MXFP4 uses the same UE8M0 group-32 scale rule as MXFP8 with emax_elem = 2.
+# Two E2M1 codes share a byte: element 2i in the low nibble, 2i+1 in the high
+# nibble (the pages name the format, flashinfer_mxfp4 and "MXFP4 weights",
+# but not a packing; this is the plainest one and the one sub-byte element
+# types commonly use).
+
+E2M1_MAX = 6.0
+E2M1_EMAX = 2
+
+
+def _e2m1_value(code: int) -> float:
+    sign = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return sign * m * 0.5                    # subnormal: (m/2) * 2^(1-1)
+    return sign * (2 + m) * 2.0 ** (e - 2)       # normal: (1 + m/2) * 2^(e-1)
+
+
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+_E2M1_POS = E2M1_TABLE[:8].copy()  # codes 0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Value of E2M1 codes 0..15 (exact in fp64)."""
+    return E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & np.uint8(0xF)]
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """Round fp64 values to E2M1 codes 0..15: nearest, ties to even mantissa,
+    saturating at +-6, sign of zero kept (negative underflow gives 0x8).
+    Inputs must be finite."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), E2M1_MAX)
+    hi = np.clip(np.searchsorted(_E2M1_POS, a, side="left"), 0, 7)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E2M1_POS[lo]
+    d_hi = _E2M1_POS[hi] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(take_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(v), code | np.uint8(0x8), code).astype(np.uint8)
+
+
+def pack_e2m1(codes) -> np.ndarray:
+    """[..., n] codes (n even) -> [..., n/2] bytes, element 2i in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & np.uint8(0xF)) | ((c[..., 1::2] & np.uint8(0xF)) << np.uint8(4))
+
+
+def unpack_e2m1(packed) -> np.ndarray:
+    """[..., n/2] bytes -> [..., n] codes."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & np.uint8(0xF)
+    out[..., 1::2] = p >> np.uint8(4)
+    return out
+
+
+def mxfp4_quantize(v):
+    """Quantise along the last axis in groups of 32 to MXFP4.
+
+    Returns (q, s): q holds the packed E2M1 codes, shape [..., n/2] (uint8);
+    s the UE8M0 codes, shape [..., n/32].
+
+    For each group:
+      amax  = max |v_i|
+      code  = 0 if amax == 0, else clamp(floor(log2 amax) - 2 + 127, 0, 254)
+      q_i   = e2m1_encode(v_i * 2^(127 - code))    (the scaling is exact)
+    """
+    v = np.asarray(v, dtype=np.float64)
+    n = v.shape[-1]
+    if n % GROUP:
+        raise ValueError("last axis must be a multiple of 32")
+    g = v.reshape(v.shape[:-1] + (n // GROUP, GROUP))
+    amax = np.max(np.abs(g), axis=-1)
+    _, ex = np.frexp(amax)
+    code = np.clip(ex.astype(np.int64) - 1 - E2M1_EMAX + UE8M0_BIAS, 0, 254)
+    code = np.where(amax == 0.0, 0, code)
+    scaled = np.ldexp(g, (UE8M0_BIAS - code)[..., None])
+    q = e2m1_encode(scaled).reshape(v.shape)
+    return pack_e2m1(q), code.astype(np.uint8)
+
+
+def mxfp4_dequantize(q, s) -> np.ndarray:
+    """Value of MXFP4 data (packed codes q, scales s), exact in fp64."""
+    codes = unpack_e2m1(q)
+    n = codes.shape[-1]
+    vals = e2m1_decode(codes).reshape(codes.shape[:-1] + (n // GROUP, GROUP))
+    return (vals * ue8m0_value(s)[..., None]).reshape(codes.shape)

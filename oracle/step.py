@@ -17,7 +17,14 @@ Readings where the pages are silent (each listed in the design doc):
 * Intermediate rounding. g and u are rounded to bf16, as an unfused GEMM
   would store them. silu(g)*u is formed in fp64 and rounded to fp32, then to
   bf16. That h is quantised to MXFP8 along I before the down projection.
-* No SwiGLU clip is applied; the pages do not give the limit.
+* SwiGLU clip ("clipped SwiGLU", same page, section 3.1; the limit is not
+  given): with a limit L > 0 the bf16-rounded gate is clamped from above,
+  g' = min(g, L), and the up projection on both sides, u' = clamp(u, -L, L),
+  before h = silu(g') * u'. L <= 0 means no clip (the default).
+* Weight format: MXFP8 (E4M3 + UE8M0 per 32) by default; MXFP4 (E2M1 +
+  UE8M0 per 32, two codes per byte) for the pages' flashinfer_mxfp4 runner
+  ("SGLang's Low-Latency Mode ..." launch command) and "Beyond Day-0" 3.1's
+  MXFP4 expert weights. Activations stay MXFP8 either way.
 * GEMMs: every product of two MXFP8 values is exact in fp64. The sum over K
   is an fp64 matrix product (a library primitive). The result is rounded to
   fp32, the type the device accumulates in.
@@ -31,17 +38,19 @@ from typing import Callable, Mapping
 
 import numpy as np
 
-from .formats import (bf16_bits_to_f64, f32_to_bf16_bits, mxfp8_dequantize,
-                      mxfp8_quantize)
+from .formats import (bf16_bits_to_f64, f32_to_bf16_bits, mxfp4_dequantize, mxfp4_quantize,
+                      mxfp8_dequantize, mxfp8_quantize)
 from .routing import placement, softmax_topk_weights, topk_ids
 
 
 @dataclass
 class ExpertWeights:
-    """One expert's MXFP8 weights in the canonical K-contiguous layout.
+    """One expert's weights in the canonical K-contiguous layout.
 
-    w_gate, w_up: uint8 E4M3 [I][H]; s_gate, s_up: uint8 UE8M0 [I][H/32]
-    w_down:       uint8 E4M3 [H][I]; s_down:       uint8 UE8M0 [H][I/32]
+    fmt "mxfp8":
+      w_gate, w_up: uint8 E4M3 [I][H]; s_gate, s_up: uint8 UE8M0 [I][H/32]
+      w_down:       uint8 E4M3 [H][I]; s_down:       uint8 UE8M0 [H][I/32]
+    fmt "mxfp4": the same, with w_* holding packed E2M1 codes [rows][K/2].
     """
     w_gate: np.ndarray
     s_gate: np.ndarray
@@ -49,11 +58,18 @@ class ExpertWeights:
     s_up: np.ndarray
     w_down: np.ndarray
     s_down: np.ndarray
+    fmt: str = "mxfp8"
+
+    def dequant(self, which: str) -> np.ndarray:
+        """Exact fp64 value of one weight matrix ("gate", "up" or "down")."""
+        q, s = getattr(self, "w_" + which), getattr(self, "s_" + which)
+        return mxfp4_dequantize(q, s) if self.fmt == "mxfp4" else mxfp8_dequantize(q, s)
 
 
-def expert_weights_from_synth(seed: int, e, H: int, I: int) -> ExpertWeights:
+def expert_weights_from_synth(seed: int, e, H: int, I: int, fmt: str = "mxfp8") -> ExpertWeights:
     """Draw expert e's bf16 weights from the seeded generator, then quantise
-    them with the oracle's own MXFP8 rule. e == "shared" selects the shared expert."""
+    them with the oracle's own MXFP8 (or MXFP4) rule. e == "shared" selects
+    the shared expert."""
     import synth
     if e == "shared":
         sg, su, sd = synth.STREAM_SH_GATE, synth.STREAM_SH_UP, synth.STREAM_SH_DOWN
@@ -62,33 +78,41 @@ def expert_weights_from_synth(seed: int, e, H: int, I: int) -> ExpertWeights:
     g = bf16_bits_to_f64(synth.expert_weight_bf16(seed, sg, I, H))
     u = bf16_bits_to_f64(synth.expert_weight_bf16(seed, su, I, H))
     d = bf16_bits_to_f64(synth.expert_weight_bf16(seed, sd, H, I))
-    wg, sgc = mxfp8_quantize(g)
-    wu, suc = mxfp8_quantize(u)
-    wd, sdc = mxfp8_quantize(d)
-    return ExpertWeights(wg, sgc, wu, suc, wd, sdc)
+    quant = mxfp4_quantize if fmt == "mxfp4" else mxfp8_quantize
+    wg, sgc = quant(g)
+    wu, suc = quant(u)
+    wd, sdc = quant(d)
+    return ExpertWeights(wg, sgc, wu, suc, wd, sdc, fmt)
 
 
 def _round_f32(v) -> np.ndarray:
     return np.asarray(v, dtype=np.float64).astype(np.float32)
 
 
-def expert_mlp(xq, xs, w: ExpertWeights):
+def expert_mlp(xq, xs, w: ExpertWeights, swiglu_limit: float = 0.0):
     """SwiGLU expert MLP on MXFP8 token rows xq/xs [n][H].
 
-    Returns g_bf16, u_bf16, h_bf16 ([n][I] bf16 bits), the MXFP8 quantised h
-    (hq [n][I], hs [n][I/32]) and o (fp32 [n][H]).
+    swiglu_limit > 0 clips the bf16 gate to <= L and the bf16 up projection
+    to [-L, L] before the activation (L taken as a binary32 value).
+
+    Returns g_bf16, u_bf16, h_bf16 ([n][I] bf16 bits; g and u before the
+    clip), the MXFP8 quantised h (hq [n][I], hs [n][I/32]) and o (fp32 [n][H]).
     """
     x = mxfp8_dequantize(xq, xs)                              # exact, fp64 [n][H]
-    wg = mxfp8_dequantize(w.w_gate, w.s_gate)                 # [I][H]
-    wu = mxfp8_dequantize(w.w_up, w.s_up)
+    wg = w.dequant("gate")                                    # [I][H]
+    wu = w.dequant("up")
     g = f32_to_bf16_bits(_round_f32(x @ wg.T))                # gate projection
     u = f32_to_bf16_bits(_round_f32(x @ wu.T))                # up projection
     gf = bf16_bits_to_f64(g)
     uf = bf16_bits_to_f64(u)
+    if swiglu_limit > 0:
+        lim = float(np.float32(swiglu_limit))
+        gf = np.minimum(gf, lim)                              # clipped SwiGLU
+        uf = np.clip(uf, -lim, lim)
     silu = gf / (1.0 + np.exp(-gf))                           # SiLU(g) = g * sigmoid(g)
     h = f32_to_bf16_bits(_round_f32(silu * uf))               # SwiGLU: SiLU(gate) * up
     hq, hs = mxfp8_quantize(bf16_bits_to_f64(h))
-    wd = mxfp8_dequantize(w.w_down, w.s_down)                 # [H][I]
+    wd = w.dequant("down")                                    # [H][I]
     o = _round_f32(mxfp8_dequantize(hq, hs) @ wd.T)           # down projection
     return g, u, h, hq, hs, o
 
@@ -96,7 +120,7 @@ def expert_mlp(xq, xs, w: ExpertWeights):
 def moe_step(x_bits, logits, k: int,
              experts: Mapping[int, ExpertWeights] | Callable[[int], ExpertWeights],
              shared: ExpertWeights | None = None,
-             rows=None):
+             rows=None, swiglu_limit: float = 0.0):
     """One MoE step over T token rows.
 
     x_bits: bf16 bit patterns uint16 [T][H]; logits: fp32 [T][E].
@@ -105,6 +129,7 @@ def moe_step(x_bits, logits, k: int,
     rows: optional subset of token rows. The expert MLPs and the combine run
       only for these rows. Routing, placement and x quantisation still cover
       all T rows, and the rows left out of y are 0.
+    swiglu_limit: clip limit of the SwiGLU (<= 0: no clip).
 
     Returns a dict with every intermediate:
       ids, w, bitmap, counts, tiles, slot_e/slot_tile/slot_row, rows_of,
@@ -130,7 +155,7 @@ def moe_step(x_bits, logits, k: int,
     def run(pair_ids, weights):
         nonlocal I
         toks = np.array([p // k if p < T * k else p - T * k for p in pair_ids])
-        g, u, h, hq, hs, o = expert_mlp(xq[toks], xs[toks], weights)
+        g, u, h, hq, hs, o = expert_mlp(xq[toks], xs[toks], weights, swiglu_limit)
         I = g.shape[1]
         for n, p in enumerate(pair_ids):
             pair_res[int(p)] = (g[n], u[n], h[n], hq[n], hs[n], o[n])

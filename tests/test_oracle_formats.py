@@ -149,3 +149,79 @@ def test_mxfp8_groups_are_independent_and_along_last_axis():
         np.testing.assert_array_equal(sg[:, 0], s[:, g])
     with pytest.raises(ValueError):
         oracle.mxfp8_quantize(np.zeros((1, 48)))
+
+
+# ----------------------------------------------------------------------------- E2M1 / MXFP4
+
+_G4 = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "mxfp4_examples.json")))
+
+
+def test_e2m1_decode_matches_the_spec_value_table():
+    pos = np.array(_G4["e2m1_positive_values"])
+    np.testing.assert_array_equal(oracle.e2m1_decode(np.arange(8)), pos)
+    np.testing.assert_array_equal(oracle.e2m1_decode(np.arange(8, 16)), -pos)
+    assert np.signbit(oracle.e2m1_decode(8))  # code 0b1000 is -0
+
+
+def test_e2m1_encode_is_nearest_ties_even_saturating_brute_force():
+    grid = oracle.e2m1_decode(np.arange(16))
+    rng = np.random.default_rng(4)
+    v = np.concatenate([rng.uniform(-8, 8, 20000), np.arange(-80, 81) / 10.0,
+                        grid, (grid[:-1] + grid[1:]) / 2.0, [-0.0, 0.0, 1e-9, -1e-9, 100.0, -100.0]])
+    got = oracle.e2m1_encode(v)
+    for x, c in zip(v, got):
+        a = min(abs(x), 6.0)
+        d = np.abs(grid[:8] - a)
+        best = np.flatnonzero(d == d.min())
+        # ties: the even code (mantissa bit 0)
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        if np.signbit(x):
+            want |= 8
+        assert c == want, (x, c, want)
+
+
+def test_e2m1_pack_order_and_roundtrip():
+    assert oracle.pack_e2m1(np.array([1, 2], dtype=np.uint8))[0] == 0x21  # element 0 in the low nibble
+    codes = np.random.default_rng(5).integers(0, 16, size=(3, 64)).astype(np.uint8)
+    np.testing.assert_array_equal(oracle.unpack_e2m1(oracle.pack_e2m1(codes)), codes)
+
+
+def _mx4_group(name):
+    g = np.zeros(32)
+    if name.startswith("F1"):
+        g[:] = 1.0
+    elif name.startswith("F2"):
+        g[:6] = [6.0, 0.25, 0.75, 2.5, 5.0, 1.25]
+    elif name.startswith("F3"):
+        g[:2] = [7.5, 1.0]
+    elif name.startswith("F4"):
+        g[:4] = [-3.0, -0.1, 6.0, -6.0]
+    elif name.startswith("F5"):
+        g[:2] = [0.046875, 0.0234375]
+    return g
+
+
+@pytest.mark.parametrize("ex", _G4["examples"], ids=[e["name"] for e in _G4["examples"]])
+def test_mxfp4_hand_worked_examples(ex):
+    q, s = oracle.mxfp4_quantize(_mx4_group(ex["name"])[None, :])
+    assert int(s[0, 0]) == ex["scale_code"]
+    codes = oracle.unpack_e2m1(q)[0]
+    np.testing.assert_array_equal(codes[:len(ex["first_codes"])], ex["first_codes"])
+    if "first_bytes" in ex:
+        np.testing.assert_array_equal(q[0, :len(ex["first_bytes"])], ex["first_bytes"])
+
+
+def test_mxfp4_scale_characterisation_and_error_bound():
+    rng = np.random.default_rng(6)
+    v = rng.standard_normal((64, 128)) * np.exp2(rng.integers(-20, 20, size=(64, 1)))
+    q, s = oracle.mxfp4_quantize(v)
+    g = v.reshape(64, 4, 32)
+    scale = np.exp2(s.astype(np.float64) - 127)
+    amax_scaled = np.max(np.abs(g), axis=-1) / scale
+    assert np.all((amax_scaled >= 4.0) & (amax_scaled < 8.0))   # 2^(floor(log2 amax) - 2) puts amax in [4, 8)
+    deq = oracle.mxfp4_dequantize(q, s).reshape(64, 4, 32)
+    a = np.abs(g) / scale[..., None]
+    # grid spacing of E2M1 at |x|: 0.5 below 2, 1 in [2, 4), 2 in [4, 6]; above 6 the value saturates to 6
+    step = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    bound = np.where(a > 6, a - 6, step / 2) * scale[..., None]
+    assert np.all(np.abs(deq - g) <= bound + 1e-300)

@@ -126,3 +126,74 @@ def test_row_subset_matches_full_step():
     part = oracle.moe_step(x, lg, k, ex, rows=[2, 7])
     np.testing.assert_array_equal(part["y"][[2, 7]], full["y"][[2, 7]])
     np.testing.assert_array_equal(part["ids"], full["ids"])
+
+
+# ----------------------------------------------------------------------------- MXFP4 weights, clipped SwiGLU
+
+def _deq4_torch(q, s):
+    """MXFP4 values from the packed codes with torch ops: nibbles split with
+    integer ops, the E2M1 value table the OCP MX spec prints, exp2 scales."""
+    table = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float64)
+    p = torch.from_numpy(np.asarray(q, dtype=np.uint8).astype(np.int64))
+    codes = torch.stack([p & 0xF, p >> 4], dim=-1).reshape(*p.shape[:-1], -1)
+    vals = table[codes & 7] * torch.where((codes & 8) != 0, -1.0, 1.0).to(torch.float64)
+    st = torch.exp2(torch.from_numpy(np.asarray(s, dtype=np.int64)).to(torch.float64) - 127.0)
+    return (vals.reshape(*vals.shape[:-1], -1, 32) * st[..., None]).reshape(vals.shape)
+
+
+def _torch_swiglu(X, w, deq, limit=0.0):
+    gt = F.linear(X, deq(w.w_gate, w.s_gate)).to(torch.float32).to(torch.bfloat16)
+    ut = F.linear(X, deq(w.w_up, w.s_up)).to(torch.float32).to(torch.bfloat16)
+    g64, u64 = gt.to(torch.float64), ut.to(torch.float64)
+    if limit > 0:
+        g64 = torch.clamp(g64, max=limit)
+        u64 = torch.clamp(u64, min=-limit, max=limit)
+    ht = (F.silu(g64) * u64).to(torch.float32).to(torch.bfloat16)
+    return gt, ut, ht
+
+
+def test_mxfp4_dequantize_matches_torch_table_decode():
+    w = oracle.expert_weights_from_synth(2, 0, 512, 256, fmt="mxfp4")
+    assert w.w_gate.shape == (256, 256) and w.s_gate.shape == (256, 16)
+    np.testing.assert_array_equal(w.dequant("gate"), _deq4_torch(w.w_gate, w.s_gate).numpy())
+    np.testing.assert_array_equal(w.dequant("down"), _deq4_torch(w.w_down, w.s_down).numpy())
+
+
+def test_expert_mlp_mxfp4_weights_matches_torch_swiglu():
+    H, I = 512, 256
+    w = oracle.expert_weights_from_synth(3, 1, H, I, fmt="mxfp4")
+    x = synth.x_bf16(3, 5, H)
+    xq, xs = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(x))
+    g, u, h, hq, hs, o = oracle.step.expert_mlp(xq, xs, w)
+    X = _deq_torch(xq, xs)
+    gt, ut, ht = _torch_swiglu(X, w, _deq4_torch)
+    np.testing.assert_array_equal(g, gt.view(torch.int16).numpy().view(np.uint16))
+    np.testing.assert_array_equal(u, ut.view(torch.int16).numpy().view(np.uint16))
+    np.testing.assert_array_equal(h, ht.view(torch.int16).numpy().view(np.uint16))
+    ot = F.linear(_deq_torch(hq, hs), _deq4_torch(w.w_down, w.s_down)).to(torch.float32).numpy()
+    assert np.all(np.abs(o.astype(np.float64) - ot) <= np.spacing(np.abs(ot)))
+
+
+def test_clipped_swiglu_matches_torch_clamp():
+    H, I, limit = 512, 256, 0.375
+    w = oracle.expert_weights_from_synth(4, 2, H, I)
+    x = synth.x_bf16(4, 7, H)
+    xq, xs = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(x))
+    g, u, h, _, _, _ = oracle.step.expert_mlp(xq, xs, w, swiglu_limit=limit)
+    gt, ut, ht = _torch_swiglu(_deq_torch(xq, xs), w, _deq_torch, limit)
+    np.testing.assert_array_equal(h, ht.view(torch.int16).numpy().view(np.uint16))
+    gf, uf = oracle.bf16_bits_to_f64(g), oracle.bf16_bits_to_f64(u)
+    assert np.mean(gf > limit) > 0.1 and np.mean(np.abs(uf) > limit) > 0.1  # the clip is active
+    _, _, h0, _, _, _ = oracle.step.expert_mlp(xq, xs, w)
+    assert np.mean(h != h0) > 0.1
+
+
+def test_clip_with_a_large_limit_changes_nothing():
+    H, I = 512, 256
+    w = oracle.expert_weights_from_synth(5, 3, H, I)
+    x = synth.x_bf16(5, 4, H)
+    xq, xs = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(x))
+    a = oracle.step.expert_mlp(xq, xs, w)
+    b = oracle.step.expert_mlp(xq, xs, w, swiglu_limit=1e30)
+    for p, q in zip(a, b):
+        np.testing.assert_array_equal(p, q)
