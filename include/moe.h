@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
   MOE_OK = 0,
@@ -99,20 +99,35 @@ typedef enum {
  * undefined for that step. The GPU does not fault or hang, and the next
  * moe_forward on a plan without this flag is unaffected. */
 
+/* moe_config_t.weight_format */
+#define MOE_WEIGHTS_MXFP8 0u  /* E4M3 elements, UE8M0 scale per 32 along K */
+#define MOE_WEIGHTS_MXFP4 1u  /* E2M1 elements (two per byte, element 2i in the low nibble), UE8M0 per 32 */
+
 typedef struct moe_config {
-  int32_t hidden;        /* H: token width, the K of gate/up. Power of two, 512..4096. */
-  int32_t intermediate;  /* I: expert width, the K of down. Power of two, 256..4096. */
+  int32_t hidden;        /* H: token width, the K of gate/up. A multiple of 128, 128..16384
+                          * (the GEMV kernel and the static-scratch step: 512, 1024 or 4096). */
+  int32_t intermediate;  /* I: expert width, the K of down. A multiple of 128, 128..16384
+                          * (GEMV kernel: 256, 512 or 2048, paired with H as 512/256, 1024/512, 4096/2048). */
   int32_t num_experts;   /* E: routed experts, 1..1024 */
   int32_t top_k;         /* k: experts per token, 1..min(E, 32) */
   int32_t num_shared;    /* 0 or 1 always-active shared expert (weight 1.0 in the combine) */
   int32_t max_rows;      /* largest T a moe_forward on this plan may pass, 1..4096 */
   uint32_t flags;        /* MOE_FLAG_* */
   int64_t wait_timeout_ns; /* bound on every device-side wait; <= 0 selects 200 ms */
+  uint32_t weight_format;  /* MOE_WEIGHTS_MXFP8 (0) or MOE_WEIGHTS_MXFP4 (tensor-core kernel only) */
+  float swiglu_limit;      /* clipped SwiGLU: with L > 0, h = silu(min(g, L)) * clamp(u, -L, L),
+                            * g and u taken after their bf16 rounding; <= 0: no clip.
+                            * "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", 3.1
+                            * (the pages do not give the limit). */
 } moe_config_t;
 
-/* Expert weights in the canonical MXFP8 layout: group-32 scales along K, K contiguous.
+/* Expert weights in the canonical layout: group-32 scales along K, K contiguous.
+ * MXFP8:
  *   w_gate, w_up: E4M3 [E][I][H]     s_gate, s_up: UE8M0 [E][I][H/32]
  *   w_down:       E4M3 [E][H][I]     s_down:       UE8M0 [E][H][I/32]
+ * MXFP4: the same with w_gate, w_up packed E2M1 [E][I][H/2] and w_down packed
+ * E2M1 [E][H][I/2] (two codes per byte, element 2i in the low nibble); the
+ * w_* pointers must then be 32-byte aligned.
  * The sh_* pointers are the same for one shared expert, without the E axis. They
  * must be NULL when num_shared == 0.
  * Ownership: the plan keeps these pointers. It does not copy the weights. They
@@ -211,6 +226,14 @@ moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logit
  * This also prepares canonical MXFP8 weights from bf16 checkpoints: W_gate[e]
  * is [I][H], quantised along H. The pages' checkpoints are already group-32 FP8. */
 moe_status_t moe_quantize_mxfp8(const void *x, int64_t rows, int32_t cols,
+                                uint8_t *q, uint8_t *s, void *cuda_stream);
+
+/* MXFP4 quantisation of bf16 rows along their last axis, groups of 32 (OCP MX
+ * v1.0: scale 2^(floor(log2 amax) - 2), elements E2M1 rounded to nearest
+ * even and clamped to +-6). Prepares MXFP4 expert weights from bf16.
+ *   x bf16 [rows][cols] (device), cols a multiple of 32
+ *   q packed E2M1 [rows][cols/2] (device), s UE8M0 [rows][cols/32] (device) */
+moe_status_t moe_quantize_mxfp4(const void *x, int64_t rows, int32_t cols,
                                 uint8_t *q, uint8_t *s, void *cuda_stream);
 
 /* Timing read-back for plans built with MOE_FLAG_TIMING. Synchronises with

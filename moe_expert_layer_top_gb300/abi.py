@@ -12,7 +12,7 @@ import os
 
 from . import build as _build
 
-MOE_ABI_VERSION = 1
+MOE_ABI_VERSION = 2
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -21,6 +21,9 @@ MOE_ERR_CUDA = 3
 MOE_ERR_OOM = 4
 MOE_ERR_TIMEOUT = 5
 MOE_ERR_DEVICE_BOUNDS = 6
+
+MOE_WEIGHTS_MXFP8 = 0
+MOE_WEIGHTS_MXFP4 = 1
 
 MOE_FLAG_TIMING = 1 << 0
 MOE_FLAG_PATH_GEMV = 1 << 1
@@ -36,6 +39,7 @@ EXPORTED = (
     "moe_forward_dev",
     "moe_forward_host",
     "moe_quantize_mxfp8",
+    "moe_quantize_mxfp4",
     "moe_kernel_times",
     "moe_plan_status",
     "moe_plan_diagnostics",
@@ -63,6 +67,8 @@ class MoeConfig(ctypes.Structure):
         ("max_rows", ctypes.c_int32),
         ("flags", ctypes.c_uint32),
         ("wait_timeout_ns", ctypes.c_int64),
+        ("weight_format", ctypes.c_uint32),
+        ("swiglu_limit", ctypes.c_float),
     ]
 
 
@@ -107,6 +113,8 @@ def load(path: str | None = None):
     lib.moe_forward_host.argtypes = [_P, _P, _P, ctypes.c_int32, _P, _P]
     lib.moe_quantize_mxfp8.restype = ctypes.c_int
     lib.moe_quantize_mxfp8.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]
+    lib.moe_quantize_mxfp4.restype = ctypes.c_int
+    lib.moe_quantize_mxfp4.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]
     lib.moe_kernel_times.restype = ctypes.c_int
     lib.moe_kernel_times.argtypes = [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)]
     lib.moe_plan_status.restype = ctypes.c_int
@@ -191,6 +199,10 @@ def moe_forward_host(plan: int, x_host, logits_host, T: int, y_host, stream=None
 
 def moe_quantize_mxfp8(x, rows: int, cols: int, q, s, stream=None) -> int:
     return load().moe_quantize_mxfp8(ptr(x), rows, cols, ptr(q), ptr(s), stream_ptr(stream))
+
+
+def moe_quantize_mxfp4(x, rows: int, cols: int, q, s, stream=None) -> int:
+    return load().moe_quantize_mxfp4(ptr(x), rows, cols, ptr(q), ptr(s), stream_ptr(stream))
 
 
 def moe_kernel_times(plan: int) -> tuple[float, int]:

@@ -7,6 +7,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
 
@@ -231,6 +232,24 @@ __device__ __forceinline__ uint32_t mx_scale_code(float amax) {
   int c = fl - 8 + 127;
   c = c < 0 ? 0 : (c > 254 ? 254 : c);
   return uint32_t(c);
+}
+
+// The same rule for an element type whose largest normal has exponent emax
+// (2 for E2M1): code = clamp(floor(log2 amax) - emax + 127, 0, 254).
+__device__ __forceinline__ uint32_t mx_scale_code_emax(float amax, int emax) {
+  const uint32_t b = __float_as_uint(amax) & 0x7FFFFFFFu;
+  if (b == 0) return 0;
+  const int ef = int(b >> 23);
+  const int fl = ef ? ef - 127 : (31 - __clz(int(b & 0x7FFFFFu))) - 149;
+  int c = fl - emax + 127;
+  c = c < 0 ? 0 : (c > 254 ? 254 : c);
+  return uint32_t(c);
+}
+
+// Two floats -> two E2M1 codes in one byte (a in the low nibble), round to
+// nearest even, saturating at +-6.
+__device__ __forceinline__ uint8_t float2_to_e2m1x2(float a, float b) {
+  return static_cast<uint8_t>(__nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest));
 }
 
 // v * 2^(127 - code). The product is exact whenever it lies in the binary32

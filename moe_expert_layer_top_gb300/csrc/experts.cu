@@ -440,8 +440,12 @@ __device__ __forceinline__ void reduce_stage(const ExpertSmem &sm, int stage, in
 template <class S>
 __device__ __forceinline__ void gate_up_epilogue(const ExpertArgs &a, ExpertSmem &sm, const UnitMeta &m, int lane) {
   for (int t = 0; t < m.n; ++t) {
-    const float gb = bf16_bits_to_float(float_to_bf16_bits(sm.gu[t][0][lane]));
-    const float ub = bf16_bits_to_float(float_to_bf16_bits(sm.gu[t][1][lane]));
+    float gb = bf16_bits_to_float(float_to_bf16_bits(sm.gu[t][0][lane]));
+    float ub = bf16_bits_to_float(float_to_bf16_bits(sm.gu[t][1][lane]));
+    if (a.swiglu_limit > 0.0f) {  // clipped SwiGLU
+      gb = fminf(gb, a.swiglu_limit);
+      ub = fminf(fmaxf(ub, -a.swiglu_limit), a.swiglu_limit);
+    }
     const float silu = gb / (1.0f + expf(-gb));
     const uint16_t hb = float_to_bf16_bits(silu * ub);
     const float hv = bf16_bits_to_float(hb);

@@ -300,6 +300,9 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
                              int n_chunks, int mbg, int hbd) {
   constexpr int kMStages = C::STAGES;
   const uint64_t pol_first = l2_evict_first_policy(), pol_normal = l2_evict_normal_policy();
+  // MXFP4 boxes move half the bytes (the transaction count is the packed
+  // global bytes; each 16-code group lands in 16 bytes of shared memory)
+  const uint32_t a_tx_bytes = a.fp4 ? kABytes / 2 : kABytes;
   uint32_t g = 0;  // stages issued
   for (int i = 0;; ++i) {
     const int u = sc.unit(i);
@@ -319,7 +322,7 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&sm.full_a[s], kABytes);
+      mbar_arrive_expect_tx(&sm.full_a[s], a_tx_bytes);
       if (!m.down) {
         const int y = (sh ? 0 : m.e * a.I) + m.blk * 64;
         tma_load_2d(sm.a[s], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full_a[s], pol);
@@ -361,8 +364,10 @@ __device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t t
     }
     tmem_fence_after();
     const uint32_t d = tmem + uint32_t(acc) * C::ACC_COLS;
-    // kind::mxf8f6f4, A and B E4M3, K-major, UE8M0 scales, N = npad, M = 128
-    const uint32_t idesc = (1u << 23) | (uint32_t(m.npad >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+    // kind::mxf8f6f4, A E4M3 (or E2M1 for MXFP4 weights, format 5), B E4M3,
+    // K-major, UE8M0 scales, N = npad, M = 128
+    const uint32_t idesc = (1u << 23) | (uint32_t(m.npad >> 3) << 17) | (uint32_t(kBM >> 4) << 24) |
+                           (a.fp4 ? (5u << 7) : 0u);
     const int kcs = (m.down ? a.I : a.H) / kKC;
     bool ok = true;
     for (int kc = 0; kc < kcs; ++kc) {
@@ -578,6 +583,7 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
   const int et = ew * 32 + lane;
   const int64_t tk = int64_t(T) * a.k;
   const uint32_t target = uint32_t(a.k + a.shared);
+  const float lim = a.swiglu_limit;
   uint32_t nu = 0, xc = 0;  // units done, gate/up column slices done
   static_assert(C::NMAX <= 32, "one pair id per lane");
   for (int i = 0;; ++i) {
@@ -616,8 +622,12 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
           for (int c = 0; c < 16; ++c) {
             const int p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
             if (p < 0) continue;  // the same for the whole warp
-            const float gb = bf16_bits_to_float(float_to_bf16_bits(v[c]));
-            const float ub = bf16_bits_to_float(xb[c][32 * q + lane]);
+            float gb = bf16_bits_to_float(float_to_bf16_bits(v[c]));
+            float ub = bf16_bits_to_float(xb[c][32 * q + lane]);
+            if (lim > 0.0f) {  // clipped SwiGLU
+              gb = fminf(gb, lim);
+              ub = fminf(fmaxf(ub, -lim), lim);
+            }
             const float silu = gb / (1.0f + expf(-gb));
             const uint16_t hb = float_to_bf16_bits(silu * ub);
             const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, uint32_t(hb) & 0x7FFFu);
@@ -759,23 +769,28 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// rows x k_bytes uint8 matrix, row-major; boxes of 128 bytes x box_rows, 128-byte swizzle.
-bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map, const void *base, uint64_t k_bytes,
-                 uint64_t rows, uint32_t box_rows) {
-  const cuuint64_t dims[2] = {k_bytes, rows};
-  const cuuint64_t strides[1] = {k_bytes};
+// rows x k matrix of 8-bit codes (fp4 = false) or packed 4-bit codes (fp4 =
+// true, two per byte), row-major; boxes of 128 codes x box_rows, 128-byte
+// swizzle. Packed 4-bit boxes land as 16 codes per 16 bytes of shared memory
+// (8 bytes of codes, 8 bytes of padding): the layout the block-scaled MMA
+// reads E2M1 operands in, with the same 128-byte rows as 8-bit codes.
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map, const void *base, uint64_t k, uint64_t rows,
+                 uint32_t box_rows, bool fp4) {
+  const cuuint64_t dims[2] = {k, rows};
+  const cuuint64_t strides[1] = {fp4 ? k / 2 : k};
   const cuuint32_t box[2] = {uint32_t(kKC), box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(map, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+             const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
-// K chunks of 128 bytes, 64-row gate/up blocks, 128-row down blocks.
+// K chunks of 128 codes, 64-row gate/up blocks, 128-row down blocks.
 bool experts_mma_shape_supported(int H, int I) {
-  return H >= 128 && I >= 128 && H % 128 == 0 && I % 128 == 0 && H <= 65535 * 32 && I <= 65535 * 32;
+  return H >= 128 && I >= 128 && H % 128 == 0 && I % 128 == 0 && H <= 16384 && I <= 16384;
 }
 
 bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *maps) {
@@ -783,11 +798,14 @@ bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *map
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const uint64_t H = uint64_t(c.hidden), I = uint64_t(c.intermediate), E = uint64_t(c.num_experts);
-  bool ok = encode_rows(enc, &maps->gate, w.w_gate, H, E * I, 64) && encode_rows(enc, &maps->up, w.w_up, H, E * I, 64) &&
-            encode_rows(enc, &maps->down, w.w_down, I, E * H, kBM);
+  const bool f4 = c.weight_format == MOE_WEIGHTS_MXFP4;
+  bool ok = encode_rows(enc, &maps->gate, w.w_gate, H, E * I, 64, f4) &&
+            encode_rows(enc, &maps->up, w.w_up, H, E * I, 64, f4) &&
+            encode_rows(enc, &maps->down, w.w_down, I, E * H, kBM, f4);
   if (ok && c.num_shared)
-    ok = encode_rows(enc, &maps->sh_gate, w.sh_w_gate, H, I, 64) && encode_rows(enc, &maps->sh_up, w.sh_w_up, H, I, 64) &&
-         encode_rows(enc, &maps->sh_down, w.sh_w_down, I, H, kBM);
+    ok = encode_rows(enc, &maps->sh_gate, w.sh_w_gate, H, I, 64, f4) &&
+         encode_rows(enc, &maps->sh_up, w.sh_w_up, H, I, 64, f4) &&
+         encode_rows(enc, &maps->sh_down, w.sh_w_down, I, H, kBM, f4);
   return ok;
 }
 

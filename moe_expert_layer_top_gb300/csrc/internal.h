@@ -130,6 +130,8 @@ struct ExpertArgs {
   int64_t *diag;
   int64_t timeout_ns;
   int skip_ready_tile;  // fault injection: tile index whose ready count is never published, or -1
+  int fp4;              // weights are MXFP4 (E2M1) rather than MXFP8 (tensor-core kernel only)
+  float swiglu_limit;   // clipped SwiGLU limit; <= 0: no clip
 };
 
 size_t route_smem_bytes(int E, int words);
@@ -137,6 +139,7 @@ cudaError_t prepare_route(size_t smem);
 cudaError_t prepare_experts(int H, int I);
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
 cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int cols, uint8_t *q, uint8_t *s, cudaStream_t st);
+cudaError_t launch_quantize_fp4(const uint16_t *x, int64_t rows, int cols, uint8_t *q, uint8_t *s, cudaStream_t st);
 cudaError_t launch_experts(const ExpertArgs &a, int grid, cudaStream_t st);
 int experts_down_blocks(int H, int I);  // H / DB: down units per tile
 bool experts_shape_supported(int H, int I);

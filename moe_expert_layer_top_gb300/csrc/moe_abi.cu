@@ -42,11 +42,14 @@ moe_status_t guard_config(const moe_config_t &c) {
     return MOE_ERR_INVALID_ARG;
   if (c.num_shared != 0 && c.num_shared != 1) return MOE_ERR_INVALID_ARG;
   if ((c.flags & MOE_FLAG_PATH_GEMV) && (c.flags & MOE_FLAG_PATH_MMA)) return MOE_ERR_INVALID_ARG;
+  if (c.weight_format != MOE_WEIGHTS_MXFP8 && c.weight_format != MOE_WEIGHTS_MXFP4) return MOE_ERR_INVALID_ARG;
+  if (!(c.swiglu_limit == c.swiglu_limit)) return MOE_ERR_INVALID_ARG;  // NaN
   if (c.top_k > c.num_experts) return MOE_ERR_INVALID_ARG;
-  if (c.hidden % 32 || c.intermediate % 32) return MOE_ERR_UNSUPPORTED;
-  if (!is_pow2(c.hidden) || !is_pow2(c.intermediate)) return MOE_ERR_UNSUPPORTED;
-  if (!experts_shape_supported(c.hidden, c.intermediate)) return MOE_ERR_UNSUPPORTED;
   if (!experts_mma_shape_supported(c.hidden, c.intermediate)) return MOE_ERR_UNSUPPORTED;
+  if (c.flags & MOE_FLAG_PATH_GEMV) {  // the CUDA-core kernel: compiled MXFP8 shapes only
+    if (!experts_shape_supported(c.hidden, c.intermediate)) return MOE_ERR_UNSUPPORTED;
+    if (c.weight_format != MOE_WEIGHTS_MXFP8) return MOE_ERR_UNSUPPORTED;
+  }
   if (c.num_experts + c.num_shared > kRouteThreads) return MOE_ERR_UNSUPPORTED;
   if (c.top_k > 32) return MOE_ERR_UNSUPPORTED;
   if (c.max_rows > 4096) return MOE_ERR_UNSUPPORTED;
@@ -63,6 +66,11 @@ moe_status_t guard_weights(const moe_config_t &c, const moe_weights_t &w) {
   for (const void *p : shared) {
     if (c.num_shared && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
     if (!c.num_shared && p) return MOE_ERR_INVALID_ARG;
+  }
+  if (c.weight_format == MOE_WEIGHTS_MXFP4) {  // packed 4-bit tensor maps want 32-byte aligned rows
+    const void *codes[6] = {w.w_gate, w.w_up, w.w_down, w.sh_w_gate, w.sh_w_up, w.sh_w_down};
+    for (const void *p : codes)
+      if (p && (reinterpret_cast<uintptr_t>(p) & 31u)) return MOE_ERR_INVALID_ARG;
   }
   return MOE_OK;
 }
@@ -240,8 +248,8 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
     destroy_plan(p);
     return MOE_ERR_CUDA;
   }
-  if (prepare_route(route_smem_bytes(E, p->words)) != cudaSuccess || prepare_experts(H, I) != cudaSuccess ||
-      prepare_experts_mma() != cudaSuccess) {
+  if (prepare_route(route_smem_bytes(E, p->words)) != cudaSuccess ||
+      (experts_shape_supported(H, I) && prepare_experts(H, I) != cudaSuccess) || prepare_experts_mma() != cudaSuccess) {
     destroy_plan(p);
     return MOE_ERR_CUDA;
   }
@@ -357,6 +365,8 @@ moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T
   ea.diag = s.diag;
   ea.timeout_ns = p->timeout_ns;
   ea.skip_ready_tile = (c.flags & MOE_FLAG_TEST_SKIP_READY) ? 0 : -1;
+  ea.fp4 = c.weight_format == MOE_WEIGHTS_MXFP4 ? 1 : 0;
+  ea.swiglu_limit = c.swiglu_limit;
   const bool timed = (c.flags & MOE_FLAG_TIMING) && p->timed_calls < kMaxTimedCalls;
   if (timed && cudaEventRecord(p->ev_start[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
   const cudaError_t le = mma ? launch_experts_mma(p->maps, ea, p->num_sms, ra.chunk_rows, st) : launch_experts(ea, p->num_sms, st);
@@ -432,6 +442,16 @@ moe_status_t moe_quantize_mxfp8(const void *x, int64_t rows, int32_t cols, uint8
   if (!x || !q || !s || !aligned16(x) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
   if (launch_quantize(static_cast<const uint16_t *>(x), rows, cols, q, s, static_cast<cudaStream_t>(cuda_stream)) !=
       cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_mxfp4(const void *x, int64_t rows, int32_t cols, uint8_t *q, uint8_t *s, void *cuda_stream) {
+  if (rows < 0 || cols <= 0 || cols % 32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || !s || !aligned16(x) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (launch_quantize_fp4(static_cast<const uint16_t *>(x), rows, cols, q, s,
+                          static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -73,6 +73,50 @@ __device__ __forceinline__ void quantize_group32(const uint16_t *__restrict__ sr
   *scale = static_cast<uint8_t>(code);
 }
 
+// MXFP4 group quantiser (OCP MX v1.0): code = clamp(floor(log2 amax) - 2 + 127,
+// 0, 254); elements E2M1, round to nearest even, saturating at +-6, two per
+// byte with element 2i in the low nibble.
+__device__ __forceinline__ void quantize_group32_fp4(const uint16_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                                     uint8_t *__restrict__ scale) {
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 r = __ldg(s4 + i);
+    w[4 * i + 0] = r.x;
+    w[4 * i + 1] = r.y;
+    w[4 * i + 2] = r.z;
+    w[4 * i + 3] = r.w;
+  }
+  float v[32];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+  }
+  const uint32_t code = mx_scale_code_emax(amax, 2);
+  uint32_t q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      word |= uint32_t(float2_to_e2m1x2(mx_unscale(v[8 * i + 2 * j], code), mx_unscale(v[8 * i + 2 * j + 1], code)))
+              << (8 * j);
+    q[i] = word;
+  }
+  *reinterpret_cast<uint4 *>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
+  *scale = static_cast<uint8_t>(code);
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_fp4_kernel(const uint16_t *__restrict__ x, int64_t groups,
+                                                                     uint8_t *__restrict__ q, uint8_t *__restrict__ s) {
+  for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < groups; g += int64_t(gridDim.x) * blockDim.x)
+    quantize_group32_fp4(x + g * kGroup, q + g * (kGroup / 2), s + g);
+}
+
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const uint16_t *__restrict__ x, int64_t groups,
                                                                  uint8_t *__restrict__ q, uint8_t *__restrict__ s) {
   for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < groups; g += int64_t(gridDim.x) * blockDim.x)
@@ -351,6 +395,15 @@ int route_grid(int T, int H) {
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
   const size_t smem = route_smem_bytes(a.E, a.words);
   route_kernel<<<route_grid(a.T, a.H), kRouteThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp4(const uint16_t *x, int64_t rows, int cols, uint8_t *q, uint8_t *s, cudaStream_t st) {
+  const int64_t groups = rows * (cols / kGroup);
+  if (groups == 0) return cudaSuccess;
+  int64_t blocks = (groups + kQuantThreads - 1) / kQuantThreads;
+  if (blocks > 65535 * 16) blocks = 65535 * 16;
+  quantize_fp4_kernel<<<unsigned(blocks), kQuantThreads, 0, st>>>(x, groups, q, s);
   return cudaGetLastError();
 }
 

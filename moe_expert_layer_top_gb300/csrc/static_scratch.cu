@@ -141,6 +141,9 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   c.max_rows = T;
   const moe_status_t g = guard_host(c, *weights);
   if (g != MOE_OK) return g;
+  // this entry point runs the CUDA-core GEMV kernel: its compiled MXFP8 shapes only
+  if (!experts_shape_supported(c.hidden, c.intermediate) || c.weight_format != MOE_WEIGHTS_MXFP8)
+    return MOE_ERR_UNSUPPORTED;
   if (!x || !logits || !y || !aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(logits) & 3u))
     return MOE_ERR_INVALID_ARG;
   if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return MOE_ERR_INVALID_ARG;
@@ -240,6 +243,8 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ea.diag = ra.diag;
   ea.timeout_ns = c.wait_timeout_ns > 0 ? c.wait_timeout_ns : 200000000LL;
   ea.skip_ready_tile = -1;
+  ea.fp4 = 0;
+  ea.swiglu_limit = c.swiglu_limit;
   if (launch_experts(ea, d->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   return MOE_OK;

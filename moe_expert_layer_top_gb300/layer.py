@@ -15,10 +15,12 @@ from . import abi
 
 @dataclass
 class MoEWeightsMXFP8:
-    """Canonical MXFP8 expert weights on the device (uint8 tensors).
+    """Canonical expert weights on the device (uint8 tensors).
 
-    w_gate, w_up: [E][I][H] E4M3;  s_gate, s_up: [E][I][H/32] UE8M0
-    w_down:       [E][H][I] E4M3;  s_down:       [E][H][I/32] UE8M0
+    MXFP8: w_gate, w_up: [E][I][H] E4M3;  s_gate, s_up: [E][I][H/32] UE8M0
+           w_down:       [E][H][I] E4M3;  s_down:       [E][H][I/32] UE8M0
+    MXFP4: the same with w_gate, w_up [E][I][H/2] and w_down [E][H][I/2] of
+           packed E2M1 codes (element 2i in the low nibble).
     sh_*: the same for one shared expert without the E axis, or None.
     """
     w_gate: torch.Tensor
@@ -41,6 +43,19 @@ class MoEWeightsMXFP8:
         return w
 
 
+def quantize_mxfp4(x: torch.Tensor, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """MXFP4 (E2M1 packed two per byte, group-32 UE8M0) quantisation of bf16 rows along the last axis."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA bf16 tensor")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    q = torch.empty(x.shape[:-1] + (cols // 2,), dtype=torch.uint8, device=x.device)
+    s = torch.empty(x.shape[:-1] + (cols // 32,), dtype=torch.uint8, device=x.device)
+    st = stream if stream is not None else torch.cuda.current_stream(x.device)
+    abi.check("moe_quantize_mxfp4", abi.moe_quantize_mxfp4(x, rows, cols, q, s, st))
+    return q, s
+
+
 def quantize_mxfp8(x: torch.Tensor, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
     """MXFP8 (E4M3, group-32 UE8M0) quantisation of bf16 rows along the last axis, on the device."""
     if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
@@ -58,9 +73,10 @@ class MoEStep:
     """One planned MoE layer (Guard + Build at construction, Runtime per forward)."""
 
     def __init__(self, hidden: int, intermediate: int, num_experts: int, top_k: int, weights: MoEWeightsMXFP8,
-                 max_rows: int, num_shared: int = 0, flags: int = 0, wait_timeout_ns: int = 0, stream=None):
+                 max_rows: int, num_shared: int = 0, flags: int = 0, wait_timeout_ns: int = 0, stream=None,
+                 weight_format: int = 0, swiglu_limit: float = 0.0):
         self.cfg = abi.MoeConfig(hidden, intermediate, num_experts, top_k, num_shared, max_rows, flags,
-                                 wait_timeout_ns)
+                                 wait_timeout_ns, weight_format, swiglu_limit)
         self.weights = weights  # keeps the device buffers alive for the plan's lifetime
         self.H, self.I, self.E, self.k, self.shared = hidden, intermediate, num_experts, top_k, num_shared
         self.max_rows = max_rows

@@ -49,17 +49,20 @@ class GpuRun:
     """One CUDA-path step with every tap, on seeded inputs."""
 
     def __init__(self, T, H, E, k, I, routing="uniform", shared=0, seed=42, weights=None, max_rows=None,
-                 flags=0, timeout_ns=0, x_lg=None):
+                 flags=0, timeout_ns=0, x_lg=None, fmt="mxfp8", swiglu_limit=0.0):
         self.T, self.H, self.E, self.k, self.I, self.shared, self.seed = T, H, E, k, I, shared, seed
+        self.fmt, self.swiglu_limit = fmt, swiglu_limit
         dev = torch.device("cuda", 0)
-        self.weights = weights if weights is not None else synthetic.make_weights(seed, E, H, I, shared, dev)
+        self.weights = weights if weights is not None else synthetic.make_weights(seed, E, H, I, shared, dev, fmt)
         if x_lg is None:
             self.x_dev, self.lg_dev, self.x_bits, self.lg = synthetic.make_inputs(seed, T, H, E, k, routing, dev)
         else:
             self.x_bits, self.lg = x_lg
             self.x_dev = torch.from_numpy(self.x_bits.view(np.int16).copy()).view(torch.bfloat16).to(dev)
             self.lg_dev = torch.from_numpy(self.lg.copy()).to(dev)
-        self.step = MoEStep(H, I, E, k, self.weights, max_rows or max(T, 1), shared, flags, timeout_ns)
+        self.step = MoEStep(H, I, E, k, self.weights, max_rows or max(T, 1), shared, flags, timeout_ns,
+                            weight_format=abi.MOE_WEIGHTS_MXFP4 if fmt == "mxfp4" else abi.MOE_WEIGHTS_MXFP8,
+                            swiglu_limit=swiglu_limit)
         self.taps_struct, self.taps = taps_for(T, k, E, H, I, shared, dev)
         self.status = torch.full((1,), -1, dtype=torch.int32, device=dev)
 
@@ -76,13 +79,13 @@ class GpuRun:
         self.step.close()
 
 
-def oracle_experts(seed, E, H, I, cache=None):
+def oracle_experts(seed, E, H, I, cache=None, fmt="mxfp8"):
     cache = {} if cache is None else cache
 
     def get(e):
-        key = (seed, e, H, I)
+        key = (seed, e, H, I, fmt)
         if key not in cache:
-            cache[key] = oracle.expert_weights_from_synth(seed, e, H, I)
+            cache[key] = oracle.expert_weights_from_synth(seed, e, H, I, fmt=fmt)
         return cache[key]
     return get
 

@@ -56,7 +56,7 @@ def fake_weights(shared=False):
 
 def cfg(**kw):
     base = dict(hidden=4096, intermediate=2048, num_experts=256, top_k=8, num_shared=0, max_rows=384, flags=0,
-                wait_timeout_ns=0)
+                wait_timeout_ns=0, weight_format=0, swiglu_limit=0.0)
     base.update(kw)
     return abi.MoeConfig(**base)
 
@@ -68,9 +68,14 @@ def cfg(**kw):
     (dict(num_shared=2), abi.MOE_ERR_INVALID_ARG),
     (dict(max_rows=0), abi.MOE_ERR_INVALID_ARG),
     (dict(hidden=32, intermediate=32), abi.MOE_ERR_UNSUPPORTED),
-    (dict(hidden=7168), abi.MOE_ERR_UNSUPPORTED),        # not a power of two
-    (dict(intermediate=2304), abi.MOE_ERR_UNSUPPORTED),
-    (dict(hidden=8192, intermediate=4096), abi.MOE_ERR_UNSUPPORTED),
+    (dict(hidden=7200), abi.MOE_ERR_UNSUPPORTED),        # not a multiple of 128
+    (dict(intermediate=2300), abi.MOE_ERR_UNSUPPORTED),
+    (dict(hidden=32768, intermediate=4096), abi.MOE_ERR_UNSUPPORTED),   # above 16384
+    (dict(intermediate=2304, flags=abi.MOE_FLAG_PATH_GEMV), abi.MOE_ERR_UNSUPPORTED),  # GEMV: compiled shapes
+    (dict(hidden=7168, flags=abi.MOE_FLAG_PATH_GEMV), abi.MOE_ERR_UNSUPPORTED),
+    (dict(weight_format=abi.MOE_WEIGHTS_MXFP4, flags=abi.MOE_FLAG_PATH_GEMV), abi.MOE_ERR_UNSUPPORTED),
+    (dict(weight_format=2), abi.MOE_ERR_INVALID_ARG),
+    (dict(swiglu_limit=float("nan")), abi.MOE_ERR_INVALID_ARG),
     (dict(num_experts=1025, top_k=8), abi.MOE_ERR_UNSUPPORTED),
     (dict(num_experts=64, top_k=33), abi.MOE_ERR_UNSUPPORTED),
     (dict(max_rows=5000), abi.MOE_ERR_UNSUPPORTED),
@@ -91,6 +96,10 @@ def test_guard_checks_weight_pointers(lib):
     # shared pointers must match num_shared
     assert abi.moe_plan_status_code(cfg(num_shared=1), fake_weights(False))[0] == abi.MOE_ERR_INVALID_ARG
     assert abi.moe_plan_status_code(cfg(num_shared=0), fake_weights(True))[0] == abi.MOE_ERR_INVALID_ARG
+    # MXFP4 code arrays must be 32-byte aligned (packed 4-bit tensor maps)
+    w = fake_weights()
+    w.w_gate = 0x10010  # 16-byte but not 32-byte aligned
+    assert abi.moe_plan_status_code(cfg(weight_format=abi.MOE_WEIGHTS_MXFP4), w)[0] == abi.MOE_ERR_INVALID_ARG
 
 
 def test_null_arguments_return_codes(lib):

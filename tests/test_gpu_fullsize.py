@@ -87,3 +87,33 @@ def test_fullsize_parity(name, flags, weights):
     assert np.all(rank < g.t["counts"][e_of])
     assert np.all(np.abs(g.t["topk_w"].sum(axis=1) - 1.0) <= 1e-6)
     g.close()
+
+
+@pytest.mark.parametrize("name", ["bs1", "bs64"])
+def test_fullsize_mxfp4_intermediate_2304_clipped(name):
+    """The pages' checkpoint shape: MXFP4 expert weights, I = 4 x 576 = 2304,
+    clipped SwiGLU (limit 1.0 here; the pages give none), on the tensor-core
+    kernel at the full expert pool, sampled rows against the oracle."""
+    import dataclasses
+    wl = dataclasses.replace(synth.WORKLOADS[name], I=2304)
+    lim = 1.0
+    w = synthetic.make_weights(SEED, wl.E, wl.H, wl.I, wl.shared, torch.device("cuda", 0), "mxfp4")
+    torch.cuda.synchronize()
+    g = GpuRun(wl.T, wl.H, wl.E, wl.k, wl.I, wl.routing, wl.shared, seed=SEED, weights=w, fmt="mxfp4",
+               swiglu_limit=lim).run()
+    assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
+    rows = [0, wl.T - 1]
+    get = oracle_experts(SEED, wl.E, wl.H, wl.I, fmt="mxfp4")
+    sh = oracle.expert_weights_from_synth(SEED, "shared", wl.H, wl.I, fmt="mxfp4") if wl.shared else None
+    r = oracle.moe_step(g.x_bits, g.lg, wl.k, get, shared=sh, rows=rows, swiglu_limit=lim)
+    check_routing_bit_exact(g, r)
+    check_h_quantizer_bit_exact(g)
+    pairs = [t * wl.k + j for t in rows for j in range(wl.k)] + ([wl.T * wl.k + t for t in rows] if wl.shared else [])
+    check_h_close(g, r, pairs)
+    assert rel_fro(g.t["o"][pairs], r["o"][pairs]) <= 1e-2
+    check_y(g.y_bits[rows], r["y"][rows])
+    e = int(r["ids"][0, 0])
+    np.testing.assert_array_equal(to_np(w.w_down[e]), get(e).w_down)
+    g.close()
+    del w
+    torch.cuda.empty_cache()

@@ -15,7 +15,7 @@ import torch
 import oracle
 import synth
 from moe_expert_layer_top_gb300 import abi, synthetic
-from moe_expert_layer_top_gb300.layer import MoEStep, quantize_mxfp8
+from moe_expert_layer_top_gb300.layer import MoEStep, quantize_mxfp4, quantize_mxfp8
 
 from gpu_cases import (GpuRun, bf16_dev_to_bits, check_h_close, check_h_quantizer_bit_exact,
                        check_routing_bit_exact, check_xquant_bit_exact, check_y, oracle_experts, rel_fro, to_np)
@@ -70,6 +70,33 @@ def test_quantiser_exhaustive_bf16_patterns():
         _quant_both(g[keep])
 
 
+def _quant4_both(bits: np.ndarray):
+    x = torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    q, s = quantize_mxfp4(x)
+    torch.cuda.synchronize()
+    qr, sr = oracle.mxfp4_quantize(oracle.bf16_bits_to_f64(bits))
+    np.testing.assert_array_equal(to_np(s), sr)
+    np.testing.assert_array_equal(to_np(q), qr)
+
+
+def test_mxfp4_quantiser_exhaustive_bf16_patterns():
+    """The device MXFP4 quantiser (E2M1 through the hardware conversion) equals
+    the oracle's for every finite bf16 pattern, at several group maxima."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_bits_to_f64(bits)
+    finite = bits[np.isfinite(vals)]
+    pad = (-len(finite)) % 32
+    finite = np.concatenate([finite, np.zeros(pad, dtype=np.uint16)])
+    _quant4_both(finite.reshape(-1, 32))
+    rng = np.random.default_rng(1)
+    _quant4_both(rng.permutation(finite).reshape(-1, 32))
+    for amax_bits in (0x3F80, 0x0D80, 0x7180, 0x40C0):   # 1.0, 2^-100, 2^100, 6.0
+        g = finite.reshape(-1, 32).copy()
+        g[:, 0] = amax_bits
+        keep = np.abs(oracle.bf16_bits_to_f64(g)).max(axis=1) <= oracle.bf16_bits_to_f64(np.uint16(amax_bits))
+        _quant4_both(g[keep])
+
+
 def test_quantiser_special_groups():
     rows = []
     rows.append(np.zeros(32, dtype=np.uint16))                                 # all +0
@@ -114,6 +141,54 @@ def test_small_case_parity(case, path):
     P = T * k + T * shared
     check_h_close(g, r, np.arange(P))
     assert rel_fro(g.t["o"], r["o"]) <= 1e-2
+    check_y(g.y_bits, r["y"])
+    g.close()
+
+
+SMALL4 = [
+    # T, H, E, k, I, routing, shared, swiglu_limit
+    (6, 512, 8, 2, 256, "uniform", 0, 0.0),
+    (40, 512, 8, 2, 384, "zipf", 0, 0.0),     # I not a power of two (a multiple of 128)
+    (70, 512, 8, 3, 256, "zipf", 1, 0.5),     # shared expert, clipped SwiGLU
+    (24, 1024, 16, 4, 640, "uniform", 0, 0.375),
+]
+
+
+@pytest.mark.parametrize("case", SMALL4, ids=[f"T{c[0]}_H{c[1]}_I{c[4]}_sh{c[6]}_lim{c[7]}" for c in SMALL4])
+def test_mxfp4_weights_parity(case):
+    """MXFP4 expert weights on the tensor-core kernel, against the oracle."""
+    T, H, E, k, I, routing, shared, lim = case
+    g = GpuRun(T, H, E, k, I, routing, shared, seed=60 + T, fmt="mxfp4", swiglu_limit=lim).run()
+    assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
+    get = oracle_experts(60 + T, E, H, I, fmt="mxfp4")
+    sh = oracle.expert_weights_from_synth(60 + T, "shared", H, I, fmt="mxfp4") if shared else None
+    r = oracle.moe_step(g.x_bits, g.lg, k, get, shared=sh, swiglu_limit=lim)
+    check_routing_bit_exact(g, r)
+    check_xquant_bit_exact(g, r)
+    check_h_quantizer_bit_exact(g)
+    P = T * k + T * shared
+    check_h_close(g, r, np.arange(P))
+    assert rel_fro(g.t["o"], r["o"]) <= 1e-2
+    check_y(g.y_bits, r["y"])
+    # the device-prepared MXFP4 weights are the oracle's, bit for bit
+    ref = get(0)
+    np.testing.assert_array_equal(to_np(g.weights.w_gate[0]), ref.w_gate)
+    np.testing.assert_array_equal(to_np(g.weights.s_down[0]), ref.s_down)
+    g.close()
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_clipped_swiglu_parity(path):
+    T, H, E, k, I, lim = 24, 512, 8, 2, 256, 0.375
+    g = GpuRun(T, H, E, k, I, "zipf", 1, seed=71, flags=PATHS[path], swiglu_limit=lim).run()
+    assert g.status_code == abi.MOE_OK
+    get = oracle_experts(71, E, H, I)
+    sh = oracle.expert_weights_from_synth(71, "shared", H, I)
+    r = oracle.moe_step(g.x_bits, g.lg, k, get, shared=sh, swiglu_limit=lim)
+    r0 = oracle.moe_step(g.x_bits, g.lg, k, get, shared=sh)
+    assert np.mean(r["h"] != r0["h"]) > 0.1          # the clip changes h
+    check_h_quantizer_bit_exact(g)
+    check_h_close(g, r, np.arange(T * k + T))
     check_y(g.y_bits, r["y"])
     g.close()
 
