@@ -43,9 +43,9 @@ ORACLE_WORKERS = 8     # spawn workers that prepare the oracle's weights (not ti
 # ----------------------------------------------------------------------------- oracle side (CPU)
 
 def _oracle_expert(args):
-    seed, e, H, I = args
+    seed, e, H, I, fmt = args
     import oracle
-    w = oracle.expert_weights_from_synth(seed, e, H, I)
+    w = oracle.expert_weights_from_synth(seed, e, H, I, fmt=fmt)
     return e, w
 
 
@@ -58,9 +58,9 @@ def _oracle_prepare(seed, wl_name, rows, pool):
     lg = synth.router_logits(seed, wl.T, wl.E, wl.k, wl.routing)
     ids = oracle.topk_ids(lg, wl.k)
     experts = sorted(set(int(e) for t in rows for e in ids[t]))
-    jobs = [(seed, e, wl.H, wl.I) for e in experts]
+    jobs = [(seed, e, wl.H, wl.I, wl.fmt) for e in experts]
     if wl.shared:
-        jobs.append((seed, "shared", wl.H, wl.I))
+        jobs.append((seed, "shared", wl.H, wl.I, wl.fmt))
     return x_bits, lg, experts, jobs
 
 
@@ -79,7 +79,7 @@ def oracle_baseline(seed: int, wl_name: str, steps: int, warmup: int, result_q):
     times = []
     for i in range(warmup + steps):
         t0 = time.perf_counter()
-        oracle.moe_step(x_bits, lg, wl.k, got, shared=shared, rows=rows)
+        oracle.moe_step(x_bits, lg, wl.k, got, shared=shared, rows=rows, swiglu_limit=wl.swiglu_limit)
         dt = time.perf_counter() - t0
         if i >= warmup:
             times.append(dt)
@@ -221,7 +221,9 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed, flags=0):
     w = weights if wl.shared else MoEWeightsMXFP8(weights.w_gate, weights.s_gate, weights.w_up, weights.s_up,
                                                   weights.w_down, weights.s_down)
     x, lg, _, lg_np = synthetic.make_inputs(seed, wl.T, wl.H, wl.E, wl.k, wl.routing)
-    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=flags)
+    wfmt = abi.MOE_WEIGHTS_MXFP4 if wl.fmt == "mxfp4" else abi.MOE_WEIGHTS_MXFP8
+    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=flags, weight_format=wfmt,
+                   swiglu_limit=wl.swiglu_limit)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     # one device status word per step: every step must finish with MOE_OK
@@ -246,7 +248,8 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed, flags=0):
         print(f"warning: {len(bad)} of {len(words)} steps reported a device status: first {bad[0]}, "
               f"diagnostics {step.diagnostics()}", file=sys.stderr)
     # second pass: the expert kernel's own duration (CUDA events on the launch stream)
-    kstep = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING | flags)
+    kstep = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING | flags,
+                    weight_format=wfmt, swiglu_limit=wl.swiglu_limit)
     for _ in range(max(3, warmup // 2)):
         flush_buf.zero_()
         kstep.forward(x, lg, y=y)
@@ -350,8 +353,17 @@ def run_gpu(args):
     l2 = getattr(dev_props, "L2_cache_size", 128 << 20)
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
 
-    weights = synthetic.make_weights(seed, wl.E, wl.H, wl.I, shared=1)
-    torch.cuda.synchronize()
+    _wcache = {}
+
+    def weights_for(w_l):
+        """Synthetic weights of a workload's format and shape (with the shared expert), made once."""
+        key = (w_l.fmt, w_l.E, w_l.H, w_l.I)
+        if key not in _wcache:
+            _wcache[key] = synthetic.make_weights(seed, w_l.E, w_l.H, w_l.I, shared=1, fmt=w_l.fmt)
+            torch.cuda.synchronize()
+        return _wcache[key]
+
+    weights = weights_for(wl)
 
     clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
         os.path.join(ROOT, "gpurun_out")) else None)
@@ -372,13 +384,18 @@ def run_gpu(args):
 
     also = {}
     if not args.no_others and world == 1:
-        for name in ("bs4", "bs16", "bs64"):
+        others = ["bs4", "bs16", "bs64"]
+        if flags != PATH_FLAGS["gemv"]:
+            others += ["bs1_fp4", "bs4_fp4", "bs64_fp4"]  # MXFP4: tensor-core kernel only
+        for name in others:
             if name == wl.name:
                 continue
             o = synth.WORKLOADS[name]
-            r = time_gpu_workload(o, weights, max(args.steps // 2, 5), max(args.warmup, 3), flush_buf, seed, flags)
+            r = time_gpu_workload(o, weights_for(o), max(args.steps // 2, 5), max(args.warmup, 3), flush_buf, seed,
+                                  flags)
             peak, _ = measured_peaks()
-            also[name] = {"T": o.T, "expert_kernel": kernel_path(args.path, o.T),
+            also[name] = {"T": o.T, "I": o.I, "weights": o.fmt, "swiglu_limit": o.swiglu_limit,
+                          "expert_kernel": kernel_path(args.path, o.T),
                           "us_per_step": round(r["ms_mean"] * 1e3, 2),
                           "us_median": round(r["ms_median"] * 1e3, 2),
                           "expert_kernel_us": round(r["expert_ms_mean"] * 1e3, 2),
@@ -499,7 +516,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=["tiny", "bs1", "bs4", "bs16", "bs64"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=["tiny", "bs1", "bs4", "bs16", "bs64", "bs1_fp4", "bs4_fp4", "bs64_fp4"])
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="expert kernel: auto (the library default: mma), or pin gemv / mma")
     ap.add_argument("--no-cpu-baseline", action="store_true")

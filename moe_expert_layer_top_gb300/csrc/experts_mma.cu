@@ -90,8 +90,8 @@ struct MmaCfg {
     uint32_t sfb[STAGES][128];      // the same per token row (rows past NMAX unused)
     uint16_t xchg[2][16][64];       // bf16 u of one 16-column slice, [column][i]
     uint32_t jobs[NMAX];            // token rows whose combine a down unit completed
-    uint64_t full_a[STAGES];        // A landed (TMA bytes)
-    uint64_t full_b[STAGES];        // B and the scale words in place (128 loader arrivals)
+    uint64_t full[STAGES];          // A landed (TMA bytes, producer arrival) and B + scale words in place
+                                    // (128 loader arrivals): one wait per stage for the MMA issuer
     uint64_t empty[STAGES];         // the stage's MMAs are done (tcgen05.commit)
     uint64_t acc_full[2];           // accumulator complete (tcgen05.commit)
     uint64_t acc_empty[2];          // accumulator read out (128 epilogue arrivals)
@@ -322,14 +322,14 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&sm.full_a[s], a_tx_bytes);
+      mbar_arrive_expect_tx(&sm.full[s], a_tx_bytes);
       if (!m.down) {
         const int y = (sh ? 0 : m.e * a.I) + m.blk * 64;
-        tma_load_2d(sm.a[s], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full_a[s], pol);
-        tma_load_2d(sm.a[s] + kABytes / 2, sh ? &maps.sh_up : &maps.up, kc * kKC, y, &sm.full_a[s], pol);
+        tma_load_2d(sm.a[s], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full[s], pol);
+        tma_load_2d(sm.a[s] + kABytes / 2, sh ? &maps.sh_up : &maps.up, kc * kKC, y, &sm.full[s], pol);
       } else {
         const int y = (sh ? 0 : m.e * a.H) + m.blk * kBM;
-        tma_load_2d(sm.a[s], sh ? &maps.sh_down : &maps.down, kc * kKC, y, &sm.full_a[s], pol);
+        tma_load_2d(sm.a[s], sh ? &maps.sh_down : &maps.down, kc * kKC, y, &sm.full[s], pol);
       }
       ++g;
     }
@@ -340,7 +340,7 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
   const uint32_t last = g < uint32_t(kMStages) ? g : uint32_t(kMStages);
   for (uint32_t j = 1; j <= last; ++j) {
     const uint32_t gg = g - j;
-    mbar_wait(&sm.full_a[gg % kMStages], (gg / kMStages) & 1u, a.timeout_ns);
+    mbar_wait(&sm.full[gg % kMStages], (gg / kMStages) & 1u, a.timeout_ns);
   }
 }
 
@@ -373,13 +373,8 @@ __device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t t
     for (int kc = 0; kc < kcs; ++kc) {
       const int s = int(g % kMStages);
       const uint32_t ph = (g / kMStages) & 1u;
-      if (!mbar_wait(&sm.full_a[s], ph, a.timeout_ns, &waited)) {
+      if (!mbar_wait(&sm.full[s], ph, a.timeout_ns, &waited)) {
         fail(a, kDiagFullWait, u, s, kc, -12, waited);
-        ok = false;
-        break;
-      }
-      if (!mbar_wait(&sm.full_b[s], ph, a.timeout_ns, &waited)) {
-        fail(a, kDiagFullWait, u, s, kc, -13, waited);
         ok = false;
         break;
       }
@@ -415,7 +410,7 @@ __device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t t
 // copies them with tcgen05.cp). Each thread runs its own pipeline and meets
 // no other thread: it issues a stage as soon as the ring slot is free, and
 // when it cannot issue, it waits for its oldest stage in flight and arrives
-// on that stage's full_b (fence.proxy.async first: the copies were written
+// on that stage's full barrier (fence.proxy.async first: the copies were written
 // through the generic proxy, the MMA reads through the async proxy).
 
 template <int NMAX>
@@ -532,7 +527,7 @@ __device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, co
   auto complete_oldest = [&]() {
     cp_async_wait_n(g - gc - 1);
     fence_proxy_async();
-    mbar_arrive(&sm.full_b[gc % kMStages]);
+    mbar_arrive(&sm.full[gc % kMStages]);
     ++gc;
   };
   MUnit m;
@@ -701,8 +696,7 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMStages; ++i) {
-      mbar_init(&sm.full_a[i], 1);
-      mbar_init(&sm.full_b[i], kLoaders);
+      mbar_init(&sm.full[i], 1 + kLoaders);
       mbar_init(&sm.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {

@@ -150,10 +150,15 @@ class Workload:
     routing: str  # "uniform" or "zipf"
     zipf_s: float = 1.1
     description: str = ""
+    fmt: str = "mxfp8"          # expert weight format: "mxfp8" or "mxfp4"
+    swiglu_limit: float = 0.0   # clipped SwiGLU limit (<= 0: no clip)
 
     @property
     def expert_bytes(self) -> int:
-        """MXFP8 bytes of one expert: 3 matrices of I x H e4m3 plus one scale byte per 32."""
+        """Weight bytes of one expert: 3 matrices of I x H codes (1 byte each for
+        MXFP8, half a byte for MXFP4) plus one scale byte per 32."""
+        if self.fmt == "mxfp4":
+            return 3 * self.I * self.H * 17 // 32
         return 3 * self.I * self.H * 33 // 32
 
 
@@ -168,6 +173,13 @@ WORKLOADS = {
                      description="bs16 verify shape: T=96, Zipf(1.1) routing"),
     "bs64": Workload("bs64", 384, 4096, 256, 8, 2048, 1, "zipf",
                      description="bs64 verify shape: T=384, E=256 + 1 shared expert, Zipf(1.1) routing"),
+    # the pages' checkpoint format: MXFP4 expert weights, I = 4 x 576, clipped SwiGLU (limit not given; 7.0 here)
+    "bs1_fp4": Workload("bs1_fp4", 6, 4096, 256, 8, 2304, 0, "uniform", fmt="mxfp4", swiglu_limit=7.0,
+                        description="bs1 shape with MXFP4 weights, I=2304, clipped SwiGLU"),
+    "bs4_fp4": Workload("bs4_fp4", 24, 4096, 256, 8, 2304, 0, "uniform", fmt="mxfp4", swiglu_limit=7.0,
+                        description="bs4 shape with MXFP4 weights, I=2304, clipped SwiGLU"),
+    "bs64_fp4": Workload("bs64_fp4", 384, 4096, 256, 8, 2304, 1, "zipf", fmt="mxfp4", swiglu_limit=7.0,
+                         description="bs64 shape with MXFP4 weights, I=2304, clipped SwiGLU"),
 }
 
 
