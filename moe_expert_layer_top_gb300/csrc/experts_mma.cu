@@ -73,40 +73,43 @@ constexpr int kBarEpi = 2, kBarGate = 3;   // named barriers (0 is __syncthreads
 static_assert(kMmaDownRows == kBM, "unit geometry");
 
 // One instantiation per chunk size. A chunk of at most NMAX token rows is the
-// MMA's N; the ring holds STAGES stages of a 16 KB weight tile plus an
-// NMAX-row token tile, so smaller chunks leave room for a deeper ring (more
-// weight bytes in flight per SM).
-template <int NMAX_, int STAGES_>
+// MMA's N. A stage holds KPS K-chunks of 128 (a 16 KB weight tile and an
+// NMAX-row token tile each): more chunks per stage spread the per-stage
+// costs of the MMA issuer (one barrier wait, one commit) over more MMAs.
+// The ring holds STAGES stages; smaller token tiles leave room for more.
+template <int NMAX_, int STAGES_, int KPS_>
 struct MmaCfg {
   static constexpr int NMAX = NMAX_;
   static constexpr int STAGES = STAGES_;
+  static constexpr int KPS = KPS_;
   static constexpr int BBYTES = NMAX * kKC;
   static constexpr uint32_t ACC_COLS = NMAX < 32 ? 32 : NMAX;  // TMEM columns per accumulator
   static constexpr uint32_t SCALE_COL0 = 2 * ACC_COLS;
+  static constexpr uint32_t SLOT_COLS = KPS * kScaleSlotCols;  // TMEM scale columns per stage
   struct Smem {
-    uint8_t a[STAGES][kABytes];     // weight tiles, 128-byte swizzled K-major (TMA)
-    uint8_t b[STAGES][BBYTES];      // token-row tiles, same layout (cp.async)
-    uint32_t sfa[STAGES][128];      // the stage's 4 UE8M0 codes (one per 32 K) per weight row, TMEM image order
-    uint32_t sfb[STAGES][128];      // the same per token row (rows past NMAX unused)
-    uint16_t xchg[2][16][64];       // bf16 u of one 16-column slice, [column][i]
-    uint32_t jobs[NMAX];            // token rows whose combine a down unit completed
-    uint64_t full[STAGES];          // A landed (TMA bytes, producer arrival) and B + scale words in place
-                                    // (128 loader arrivals): one wait per stage for the MMA issuer
-    uint64_t empty[STAGES];         // the stage's MMAs are done (tcgen05.commit)
-    uint64_t acc_full[2];           // accumulator complete (tcgen05.commit)
-    uint64_t acc_empty[2];          // accumulator read out (128 epilogue arrivals)
-    uint64_t mma_done;              // every MMA of the block finished (before TMEM is freed)
+    uint8_t a[STAGES][KPS][kABytes];  // weight tiles, 128-byte swizzled K-major (TMA)
+    uint8_t b[STAGES][KPS][BBYTES];   // token-row tiles, same layout (cp.async)
+    uint32_t sfa[STAGES][KPS][128];   // a chunk's 4 UE8M0 codes (one per 32 K) per weight row, TMEM image order
+    uint32_t sfb[STAGES][KPS][128];   // the same per token row (rows past NMAX unused)
+    uint16_t xchg[2][16][64];         // bf16 u of one 16-column slice, [column][i]
+    uint32_t jobs[NMAX];              // token rows whose combine a down unit completed
+    uint64_t full[STAGES];            // A landed (TMA bytes, producer arrival) and B + scale words in place
+                                      // (128 loader arrivals): one wait per stage for the MMA issuer
+    uint64_t empty[STAGES];           // the stage's MMAs are done (tcgen05.commit)
+    uint64_t acc_full[2];             // accumulator complete (tcgen05.commit)
+    uint64_t acc_empty[2];            // accumulator read out (128 epilogue arrivals)
+    uint64_t mma_done;                // every MMA of the block finished (before TMEM is freed)
     uint32_t tmem_base;
     uint32_t n_jobs;
   };
   static constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + alignment of the ring to 1024 bytes
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  static_assert(SCALE_COL0 + STAGES * kScaleSlotCols <= kTmemCols, "TMEM budget");
+  static_assert(SCALE_COL0 + STAGES * SLOT_COLS <= kTmemCols, "TMEM budget");
   static_assert(NMAX % 16 == 0 && NMAX <= 128 && BBYTES % 1024 == 0, "token tile geometry");
   static_assert(STAGES <= 11, "cp_async_wait_n covers at most 10 newer groups");
 };
-using Cfg16 = MmaCfg<16, 11>;
-using Cfg32 = MmaCfg<32, 10>;
+using Cfg16 = MmaCfg<16, 5, 2>;
+using Cfg32 = MmaCfg<32, 5, 2>;
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -313,23 +316,27 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
     const uint64_t pol = m.nch > 1 ? pol_normal : pol_first;
     const int kcs = (m.down ? a.I : a.H) / kKC;
     bool ok = true;
-    for (int kc = 0; kc < kcs; ++kc) {
+    for (int kc0 = 0; kc0 < kcs; kc0 += C::KPS) {
       const int s = int(g % kMStages);
       const uint32_t ph = (g / kMStages) & 1u;
+      const int nck = kcs - kc0 < C::KPS ? kcs - kc0 : C::KPS;
       int64_t waited = 0;
       if (!mbar_wait(&sm.empty[s], ph ^ 1u, a.timeout_ns, &waited)) {
-        fail(a, kDiagEmptyWait, u, s, kc, -10, waited);
+        fail(a, kDiagEmptyWait, u, s, kc0, -10, waited);
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&sm.full[s], a_tx_bytes);
-      if (!m.down) {
-        const int y = (sh ? 0 : m.e * a.I) + m.blk * 64;
-        tma_load_2d(sm.a[s], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full[s], pol);
-        tma_load_2d(sm.a[s] + kABytes / 2, sh ? &maps.sh_up : &maps.up, kc * kKC, y, &sm.full[s], pol);
-      } else {
-        const int y = (sh ? 0 : m.e * a.H) + m.blk * kBM;
-        tma_load_2d(sm.a[s], sh ? &maps.sh_down : &maps.down, kc * kKC, y, &sm.full[s], pol);
+      mbar_arrive_expect_tx(&sm.full[s], a_tx_bytes * uint32_t(nck));
+      for (int j = 0; j < nck; ++j) {
+        const int kc = kc0 + j;
+        if (!m.down) {
+          const int y = (sh ? 0 : m.e * a.I) + m.blk * 64;
+          tma_load_2d(sm.a[s][j], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full[s], pol);
+          tma_load_2d(sm.a[s][j] + kABytes / 2, sh ? &maps.sh_up : &maps.up, kc * kKC, y, &sm.full[s], pol);
+        } else {
+          const int y = (sh ? 0 : m.e * a.H) + m.blk * kBM;
+          tma_load_2d(sm.a[s][j], sh ? &maps.sh_down : &maps.down, kc * kKC, y, &sm.full[s], pol);
+        }
       }
       ++g;
     }
@@ -370,25 +377,30 @@ __device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t t
                            (a.fp4 ? (5u << 7) : 0u);
     const int kcs = (m.down ? a.I : a.H) / kKC;
     bool ok = true;
-    for (int kc = 0; kc < kcs; ++kc) {
+    for (int kc0 = 0; kc0 < kcs; kc0 += C::KPS) {
       const int s = int(g % kMStages);
       const uint32_t ph = (g / kMStages) & 1u;
+      const int nck = kcs - kc0 < C::KPS ? kcs - kc0 : C::KPS;
       if (!mbar_wait(&sm.full[s], ph, a.timeout_ns, &waited)) {
-        fail(a, kDiagFullWait, u, s, kc, -12, waited);
+        fail(a, kDiagFullWait, u, s, kc0, -12, waited);
         ok = false;
         break;
       }
       tmem_fence_after();
-      const uint32_t sfa = tmem + C::SCALE_COL0 + uint32_t(s) * kScaleSlotCols, sfb = sfa + 16;
-      // the stage's scale words into TMEM (in issue order before the MMAs that read them)
-      tmem_cp_32x128b_x4(sfa, sf_desc(smem_u32(sm.sfa[s])));
-      tmem_cp_32x128b_x4(sfb, sf_desc(smem_u32(sm.sfb[s])));
-      const uint64_t adesc = sw128_desc(smem_u32(sm.a[s])), bdesc = sw128_desc(smem_u32(sm.b[s]));
+      for (int j = 0; j < nck; ++j) {
+        const uint32_t sfa = tmem + C::SCALE_COL0 + uint32_t(s) * C::SLOT_COLS + uint32_t(j) * kScaleSlotCols;
+        const uint32_t sfb = sfa + 16;
+        // the chunk's scale words into TMEM (in issue order before the MMAs that read them)
+        tmem_cp_32x128b_x4(sfa, sf_desc(smem_u32(sm.sfa[s][j])));
+        tmem_cp_32x128b_x4(sfb, sf_desc(smem_u32(sm.sfb[s][j])));
+        const uint64_t adesc = sw128_desc(smem_u32(sm.a[s][j])), bdesc = sw128_desc(smem_u32(sm.b[s][j]));
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        // +32 bytes of K per step: +2 in the descriptor's 16-byte start-address field
-        mma_mxf8(d, adesc + uint64_t(2 * k4), bdesc + uint64_t(2 * k4),
-                 idesc | (uint32_t(k4) << 4) | (uint32_t(k4) << 29), sfa, sfb, (kc | k4) != 0 ? 1u : 0u);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          // +32 bytes of K per step: +2 in the descriptor's 16-byte start-address field
+          mma_mxf8(d, adesc + uint64_t(2 * k4), bdesc + uint64_t(2 * k4),
+                   idesc | (uint32_t(k4) << 4) | (uint32_t(k4) << 29), sfa, sfb,
+                   (kc0 + j + k4) != 0 ? 1u : 0u);
+        }
       }
       mma_commit(&sm.empty[s]);
       ++g;
@@ -452,24 +464,29 @@ __device__ __forceinline__ LoaderRows<NMAX> loader_rows(const ExpertArgs &a, int
   return lr;
 }
 
-// Issue the copies of stage slot s for K chunk kc (one cp.async group).
+// Issue the copies of stage slot s for K chunks kc0 .. kc0 + nck - 1 (one cp.async group).
 template <class C>
 __device__ __forceinline__ void loader_issue(typename C::Smem &sm, const MUnit &m, const LoaderRows<C::NMAX> &lr,
-                                             int s, int kc, int tau, const void *zero_src) {
+                                             int s, int kc0, int nck, int tau, const void *zero_src) {
   const int c8 = tau & 7, r0 = tau >> 3;
-  uint8_t *bs = sm.b[s];
-#pragma unroll
-  for (int i = 0; i < C::NMAX / 16; ++i) {
-    const int r = r0 + 16 * i;
-    if (r < m.npad) {
-      const bool v = lr.b[i] != nullptr;
-      cp_async16_zfill(bs + r * kKC + ((c8 ^ (r & 7)) << 4), v ? lr.b[i] + kc * kKC + c8 * 16 : zero_src,
-                       v ? 16u : 0u);
-    }
-  }
   const int w = (tau & 31) * 4 + (tau >> 5);  // TMEM image order
-  cp_async4_zfill(&sm.sfa[s][w], lr.sfa + kc * 4, 4u);
-  cp_async4_zfill(&sm.sfb[s][w], lr.sfb ? lr.sfb + kc * 4 : zero_src, lr.sfb ? 4u : 0u);
+#pragma unroll
+  for (int j = 0; j < C::KPS; ++j) {
+    if (j >= nck) break;
+    const int kc = kc0 + j;
+    uint8_t *bs = sm.b[s][j];
+#pragma unroll
+    for (int i = 0; i < C::NMAX / 16; ++i) {
+      const int r = r0 + 16 * i;
+      if (r < m.npad) {
+        const bool v = lr.b[i] != nullptr;
+        cp_async16_zfill(bs + r * kKC + ((c8 ^ (r & 7)) << 4), v ? lr.b[i] + kc * kKC + c8 * 16 : zero_src,
+                         v ? 16u : 0u);
+      }
+    }
+    cp_async4_zfill(&sm.sfa[s][j][w], lr.sfa + kc * 4, 4u);
+    cp_async4_zfill(&sm.sfb[s][j][w], lr.sfb ? lr.sfb + kc * 4 : zero_src, lr.sfb ? 4u : 0u);
+  }
   cp_async_commit();
 }
 
@@ -551,9 +568,10 @@ __device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, co
     const int s = int(g % kMStages);
     const uint32_t ph = (g / kMStages) & 1u;
     if (g - gc < uint32_t(kMStages) && mbar_test(&sm.empty[s], ph ^ 1u)) {
-      loader_issue<C>(sm, m, lr, s, kc, tau, zero_src);
+      const int nck = kcs - kc < C::KPS ? kcs - kc : C::KPS;
+      loader_issue<C>(sm, m, lr, s, kc, nck, tau, zero_src);
       ++g;
-      ++kc;
+      kc += nck;
       continue;
     }
     if (gc < g) {
