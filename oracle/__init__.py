@@ -26,6 +26,10 @@ Sources, cited by page title and section:
 * "FlyDSL Mono Kernels for High-Interactivity LLM Serving in ATOM", section
   "MiniMax-M3: Connecting Attention and Experts". Each expert does its
   up/gate and down projections, for the shared and the routed experts.
+* "Beyond Day-0 ...", section 2.1, the MoE, mHC and small-operator bullets:
+  the router projection in front of the step, and behind it the residual-stream
+  combination, the next layer's input combination, RMSNorm and MXFP8
+  quantisation (``oracle/fused.py``).
 * OCP Microscaling Formats (MX) Specification v1.0:
   - the E4M3 and E2M1 element encodings (MXFP8, MXFP4);
   - the UE8M0 scale;
@@ -53,5 +57,6 @@ from .formats import (  # noqa: F401
     ue8m0_value,
     unpack_e2m1,
 )
+from .fused import residual_norm_mxfp8, router_logits  # noqa: F401
 from .routing import exp_rn, placement, softmax_topk_weights, topk_ids  # noqa: F401
 from .step import ExpertWeights, expert_weights_from_synth, moe_step  # noqa: F401

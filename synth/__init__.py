@@ -57,6 +57,14 @@ BASE_SEED = 42
 STREAM_X = 1
 STREAM_LOGITS = 2
 STREAM_LOGITS_RETRY = 3
+# The steps either side of the MoE step: router weight, residual streams,
+# RMSNorm weight and per-row stream-mixing coefficients.
+STREAM_ROUTER = 4
+STREAM_RESID = 5
+STREAM_NORM_W = 6
+STREAM_MIX_RES = 7
+STREAM_MIX_POST = 8
+STREAM_MIX_PRE = 9
 
 
 def stream_gate(e: int) -> int:
@@ -246,3 +254,31 @@ def expert_weight_bf16(seed: int, stream: int, rows: int, cols: int,
 def bf16_bits_to_float32(bits: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float32 (a format conversion, no rounding)."""
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def router_weight_bf16(seed: int, E: int, H: int) -> np.ndarray:
+    """Router weight W_r ~ N(0, 1/sqrt(H)) as bf16 bits, [E][H]. With x ~ N(0, 1)
+    the projected logits have about unit variance."""
+    return normal_bf16(seed, STREAM_ROUTER, 0, E * H, expert_sigma(H)).reshape(E, H)
+
+
+def residual_bf16(seed: int, T: int, S: int, H: int) -> np.ndarray:
+    """S residual streams per token row, ~ N(0, 1) as bf16 bits, [T][S][H]."""
+    return normal_bf16(seed, STREAM_RESID, 0, T * S * H, 1.0).reshape(T, S, H)
+
+
+def norm_weight_bf16(seed: int, H: int) -> np.ndarray:
+    """RMSNorm weight gamma ~ 1 + N(0, 0.25) as bf16 bits, [H]: the normal draw,
+    plus 1.0 in binary32, rounded to bf16 (nearest even)."""
+    d = bf16_bits_to_float32(normal_bf16(seed, STREAM_NORM_W, 0, H, 0.25))
+    return _f32_to_bf16_rne(d + np.float32(1.0))
+
+
+def mix_coefficients(seed: int, T: int, S: int):
+    """Per-row stream-mixing coefficients, fp32:
+    res [T][S][S] uniform in (0, 2/S) (each row of the matrix sums to about 1),
+    post [T][S] uniform in (0, 2), pre [T][S] uniform in (0, 1)."""
+    res = (uniform_open01(seed, STREAM_MIX_RES, 0, T * S * S) * (2.0 / S)).astype(np.float32)
+    post = (uniform_open01(seed, STREAM_MIX_POST, 0, T * S) * 2.0).astype(np.float32)
+    pre = uniform_open01(seed, STREAM_MIX_PRE, 0, T * S).astype(np.float32)
+    return res.reshape(T, S, S), post.reshape(T, S), pre.reshape(T, S)
