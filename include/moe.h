@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum {
   MOE_OK = 0,
@@ -210,6 +210,59 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
  * length rather than the capacity. */
 moe_status_t moe_forward_dev(void *plan, const void *x, const float *logits, const int32_t *d_T, void *y,
                              int32_t *d_status, void *cuda_stream);
+
+/* The steps on either side of the MoE step, fused into its two kernels.
+ * Source: "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", section 2.1:
+ *  - MoE bullet: the router produces the downstream layout directly; the
+ *    kernels also fuse the mHC output combination, the next layer's input
+ *    combination or normalisation, to cut intermediate writes;
+ *  - mHC bullet: the weighted combination of the four residual streams is
+ *    fused with RMSNorm, with quantisation on supported paths;
+ *  - small-operator bullet: RMSNorm is fused with MXFP8 quantisation.
+ *
+ * In front (w_router set): the route kernel computes the router logits
+ *   logits[t][e] = sum_h x[t][h] * w_router[e][h]
+ * (bf16 operands, binary32 accumulation in a fixed order, no bias) before its
+ * top-k. The top-k, the softmax weights and the placement then read these
+ * logits.
+ *
+ * Behind (num_streams = S > 0): each token row carries S residual streams.
+ * Once y[t] is combined (bf16), the expert kernel computes:
+ *   new_s[t] = sum_s' mix_res[t][s][s'] * resid_in[t][s'] + mix_post[t][s] * y[t]
+ *              (binary32, stored as bf16 in resid_out)
+ *   u[t]     = sum_s mix_pre[t][s] * new_s[t]                  (binary32)
+ *   z[t]     = bf16( u[t] * norm_weight / sqrt(mean_h(u[t]^2) + rms_eps) )
+ *   zq, zs   = MXFP8 of z[t] along H (the rule used for x)
+ * S = 1 with NULL coefficients is the plain residual add followed by RMSNorm.
+ * The mixing coefficients are inputs; they are computed elsewhere.
+ * y is still written. Fused steps run the tensor-core expert kernel only. */
+typedef struct moe_fused_io {
+  const void *w_router;     /* bf16 [E][H] router weight, or NULL: logits are given */
+  const float *logits;      /* fp32 [T][E]. With w_router == NULL: the router logits (input,
+                             * finite). With w_router set: NULL, or a buffer that receives
+                             * the computed logits. */
+  int32_t num_streams;      /* S: 0 (no epilogue; the members below are ignored) or 1..4 */
+  const void *resid_in;     /* bf16 [T][S][H] residual streams before this layer's output */
+  void *resid_out;          /* bf16 [T][S][H] new streams; may be resid_in (updated in place) */
+  const float *mix_res;     /* fp32 [T][S][S] stream mixing, or NULL (identity); 4-byte aligned */
+  const float *mix_post;    /* fp32 [T][S] weight of y in each stream, or NULL (all 1) */
+  const float *mix_pre;     /* fp32 [T][S] next layer's input combination, or NULL (all 1) */
+  const void *norm_weight;  /* bf16 [H] RMSNorm weight */
+  float rms_eps;            /* RMSNorm epsilon, finite and >= 0 */
+  uint8_t *zq;              /* E4M3 [T][H]: the next layer's quantised input */
+  uint8_t *zs;              /* UE8M0 [T][H/32]; any alignment */
+  void *z;                  /* optional bf16 [T][H]: z before quantisation (a tap), or NULL */
+} moe_fused_io_t;
+
+/* Runtime with the fused steps around the MoE step: as moe_forward, with the
+ * router logits computed from w_router (or read from io->logits) and, with
+ * io->num_streams > 0, the residual-stream epilogue above. Pointers follow
+ * the conventions at the top of this file (16-byte aligned device memory)
+ * unless stated in moe_fused_io_t. Returns MOE_ERR_UNSUPPORTED on a plan
+ * built with MOE_FLAG_PATH_GEMV. Taps as for moe_forward. Allocates nothing,
+ * does not synchronise. */
+moe_status_t moe_forward_fused(void *plan, const void *x, int32_t T, const moe_fused_io_t *io, void *y,
+                               const moe_taps_t *taps, int32_t *d_status, void *cuda_stream);
 
 /* Runtime with host buffers: copies x and logits from host memory into
  * plan-owned device buffers, runs moe_forward and copies y back to y_host. It

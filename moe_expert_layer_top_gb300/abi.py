@@ -12,7 +12,7 @@ import os
 
 from . import build as _build
 
-MOE_ABI_VERSION = 2
+MOE_ABI_VERSION = 3
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -37,6 +37,7 @@ EXPORTED = (
     "moe_plan",
     "moe_forward",
     "moe_forward_dev",
+    "moe_forward_fused",
     "moe_forward_host",
     "moe_quantize_mxfp8",
     "moe_quantize_mxfp4",
@@ -85,6 +86,24 @@ class MoeTaps(ctypes.Structure):
                                   "h_bf16", "hq", "hs", "o")]
 
 
+class MoeFusedIO(ctypes.Structure):
+    _fields_ = [
+        ("w_router", _P),
+        ("logits", _P),
+        ("num_streams", ctypes.c_int32),
+        ("resid_in", _P),
+        ("resid_out", _P),
+        ("mix_res", _P),
+        ("mix_post", _P),
+        ("mix_pre", _P),
+        ("norm_weight", _P),
+        ("rms_eps", ctypes.c_float),
+        ("zq", _P),
+        ("zs", _P),
+        ("z", _P),
+    ]
+
+
 _lib = None
 
 
@@ -123,6 +142,9 @@ def load(path: str | None = None):
     lib.moe_plan_diagnostics.argtypes = [_P, ctypes.POINTER(ctypes.c_int64)]
     lib.moe_forward_dev.restype = ctypes.c_int
     lib.moe_forward_dev.argtypes = [_P, _P, _P, _P, _P, _P, _P]
+    lib.moe_forward_fused.restype = ctypes.c_int
+    lib.moe_forward_fused.argtypes = [_P, _P, ctypes.c_int32, ctypes.POINTER(MoeFusedIO), _P,
+                                      ctypes.POINTER(MoeTaps), _P, _P]
     lib.moe_forward_static_scratch.restype = ctypes.c_int
     lib.moe_forward_static_scratch.argtypes = [ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeWeights), _P, _P,
                                                ctypes.c_int32, _P, _P, _P]
@@ -231,6 +253,23 @@ def moe_forward_dev(plan, x, logits, d_T, y, d_status=None, stream=None) -> int:
     """One MoE step whose row count is read from device memory (int32 at d_T)."""
     lib = load()
     return lib.moe_forward_dev(plan, ptr(x), ptr(logits), ptr(d_T), ptr(y), ptr(d_status), stream_ptr(stream))
+
+
+def fused_io(w_router=None, logits=None, num_streams: int = 0, resid_in=None, resid_out=None, mix_res=None,
+             mix_post=None, mix_pre=None, norm_weight=None, rms_eps: float = 0.0, zq=None, zs=None,
+             z=None) -> MoeFusedIO:
+    """A moe_fused_io_t from tensors (or addresses, or None)."""
+    return MoeFusedIO(ptr(w_router), ptr(logits), num_streams, ptr(resid_in), ptr(resid_out), ptr(mix_res),
+                      ptr(mix_post), ptr(mix_pre), ptr(norm_weight), rms_eps, ptr(zq), ptr(zs), ptr(z))
+
+
+def moe_forward_fused(plan, x, T: int, io: MoeFusedIO, y, taps: MoeTaps | None = None, d_status=None,
+                      stream=None) -> int:
+    """One MoE step with the fused router projection and residual-stream epilogue."""
+    lib = load()
+    return lib.moe_forward_fused(plan, ptr(x), T, ctypes.byref(io) if io is not None else None, ptr(y),
+                                 ctypes.byref(taps) if taps is not None else None, ptr(d_status),
+                                 stream_ptr(stream))
 
 
 def moe_forward_static_scratch(config: MoeConfig, weights: MoeWeights, x, logits, T: int, y, d_status=None,

@@ -19,10 +19,11 @@
 namespace moe {
 
 // Q outputs per lane: h = h0 + lane + 32 q, q < Q (a block of 32 Q rows of H).
+// yb receives the lane's bf16 results as well.
 template <int Q>
 __device__ __forceinline__ void combine_row_block(const float *__restrict__ o, const float *__restrict__ topk_w,
                                                   uint16_t *__restrict__ y, int T, int k, int shared, int H, int t,
-                                                  int64_t h0, int lane) {
+                                                  int64_t h0, int lane, uint16_t (&yb)[Q]) {
   const int64_t hl = h0 + lane;
   float acc[Q];
 #pragma unroll
@@ -52,7 +53,10 @@ __device__ __forceinline__ void combine_row_block(const float *__restrict__ o, c
     for (int q = 0; q < Q; ++q) acc[q] = __fadd_rn(acc[q], __ldcg(src + 32 * q));
   }
 #pragma unroll
-  for (int q = 0; q < Q; ++q) y[int64_t(t) * H + hl + 32 * q] = float_to_bf16_bits(acc[q]);
+  for (int q = 0; q < Q; ++q) {
+    yb[q] = float_to_bf16_bits(acc[q]);
+    y[int64_t(t) * H + hl + 32 * q] = yb[q];
+  }
 }
 
 }  // namespace moe

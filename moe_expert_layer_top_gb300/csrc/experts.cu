@@ -666,7 +666,8 @@ __device__ void consumers(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
 // last of token row t's k (+ shared) pairs to finish block b (combine.cuh).
 template <class S>
 __device__ __forceinline__ void fused_combine(const ExpertArgs &a, int t, int b, int lane) {
-  combine_row_block<S::DB / 32>(a.o, a.topk_w, a.y, a.T, a.k, a.shared, S::H, t, int64_t(b) * S::DB, lane);
+  uint16_t yb[S::DB / 32];
+  combine_row_block<S::DB / 32>(a.o, a.topk_w, a.y, a.T, a.k, a.shared, S::H, t, int64_t(b) * S::DB, lane, yb);
 }
 
 // After a down unit's last stage: count each of its pairs in for (token row,

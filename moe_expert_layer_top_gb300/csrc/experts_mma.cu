@@ -53,6 +53,7 @@
 #include <string.h>
 
 #include "combine.cuh"
+#include "residual_norm.cuh"
 #include "device.cuh"
 #include "internal.h"
 
@@ -691,9 +692,12 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
       const uint32_t nj = *reinterpret_cast<volatile uint32_t *>(&sm.n_jobs);
       if (nj) {
         __threadfence();  // the other pairs' o stores, before these reads
-        for (uint32_t jj = uint32_t(ew); jj < nj; jj += 4)
-          combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, T, a.k, a.shared, a.H, int(sm.jobs[jj]),
-                                      int64_t(m.blk) * kBM, lane);
+        for (uint32_t jj = uint32_t(ew); jj < nj; jj += 4) {
+          const int t = int(sm.jobs[jj]);
+          uint16_t yb[kBM / 32];
+          combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, T, a.k, a.shared, a.H, t, int64_t(m.blk) * kBM, lane, yb);
+          if (a.n_streams) residual_block<kBM / 32>(a, t, int64_t(m.blk) * kBM, m.blk, hbd, lane, yb);
+        }
       }
       named_bar(kBarEpi, kEpiThreads);
       if (et == 0) sm.n_jobs = 0;

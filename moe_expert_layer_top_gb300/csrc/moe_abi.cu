@@ -212,6 +212,9 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   const size_t o_hq = take(size_t(p->pairs_max) * I), o_hs = take(size_t(p->pairs_max) * (I / 32));
   const size_t o_hb = take(size_t(p->pairs_max) * I * 2), o_o = take(size_t(p->pairs_max) * H * 4);
   const size_t o_xd = take(size_t(Tm) * H * 2), o_ld = take(size_t(Tm) * E * 4), o_yd = take(size_t(Tm) * H * 2);
+  const size_t o_lp = take(size_t(Tm) * E * 4), o_rg = take(size_t(p->words) * 4);
+  const size_t o_ub = take(size_t(Tm) * H * 4), o_ssp = take(size_t(Tm) * (H / kMmaDownRows) * 4);
+  const size_t o_rc = take(size_t(Tm) * 4);
   p->arena_bytes = off;
   if (cudaMalloc(&p->arena, off) != cudaSuccess) {
     cudaGetLastError();
@@ -244,6 +247,11 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   s.x_dev = base + o_xd;
   s.logits_dev = reinterpret_cast<float *>(base + o_ld);
   s.y_dev = base + o_yd;
+  s.logits_proj = reinterpret_cast<float *>(base + o_lp);
+  s.rg_cnt = reinterpret_cast<uint32_t *>(base + o_rg);
+  s.u_buf = reinterpret_cast<float *>(base + o_ub);
+  s.ss_part = reinterpret_cast<float *>(base + o_ssp);
+  s.row_cnt = reinterpret_cast<uint32_t *>(base + o_rc);
   if (cudaMemset(p->arena, 0, off) != cudaSuccess) {
     destroy_plan(p);
     return MOE_ERR_CUDA;
@@ -282,16 +290,24 @@ namespace {
 // Enqueues one step: the route kernel, then an expert kernel with PDL.
 // T sizes the grids. With d_T set, the kernels read the step's row count
 // from device memory (clamped to max_rows) and the tensor-core kernel runs.
+// io (or NULL): the fused router projection and residual-stream epilogue;
+// with io set, logits is ignored and the tensor-core kernel runs.
 moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T, const int32_t *d_T, void *y,
-                          bool h_tap, int32_t *d_status, cudaStream_t st) {
+                          bool h_tap, int32_t *d_status, cudaStream_t st, const moe_fused_io_t *io = nullptr) {
   const moe_config_t &c = p->cfg;
   Scratch &s = p->s;
   int32_t *status = d_status ? d_status : s.status;
-  const bool mma = d_T != nullptr || T >= p->mma_min_rows;
+  const bool mma = d_T != nullptr || io != nullptr || T >= p->mma_min_rows;
+  const bool proj = io && io->w_router;
+  const int n_streams = io ? io->num_streams : 0;
 
   RouteArgs ra;
-  ra.logits = logits;
+  ra.logits = proj ? (io->logits ? io->logits : s.logits_proj) : (io ? io->logits : logits);
   ra.x = static_cast<const uint16_t *>(x);
+  ra.w_router = proj ? static_cast<const uint16_t *>(io->w_router) : nullptr;
+  ra.rg_cnt = s.rg_cnt;
+  ra.n_eblk = (c.num_experts + kRouterExperts - 1) / kRouterExperts;
+  ra.row_cnt = n_streams ? s.row_cnt : nullptr;
   ra.T = T;
   ra.d_T = d_T;
   ra.H = c.hidden;
@@ -367,6 +383,20 @@ moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T
   ea.skip_ready_tile = (c.flags & MOE_FLAG_TEST_SKIP_READY) ? 0 : -1;
   ea.fp4 = c.weight_format == MOE_WEIGHTS_MXFP4 ? 1 : 0;
   ea.swiglu_limit = c.swiglu_limit;
+  ea.n_streams = n_streams;
+  ea.resid_in = n_streams ? static_cast<const uint16_t *>(io->resid_in) : nullptr;
+  ea.resid_out = n_streams ? static_cast<uint16_t *>(io->resid_out) : nullptr;
+  ea.mix_res = n_streams ? io->mix_res : nullptr;
+  ea.mix_post = n_streams ? io->mix_post : nullptr;
+  ea.mix_pre = n_streams ? io->mix_pre : nullptr;
+  ea.norm_w = n_streams ? static_cast<const uint16_t *>(io->norm_weight) : nullptr;
+  ea.rms_eps = n_streams ? io->rms_eps : 0.0f;
+  ea.zq = n_streams ? io->zq : nullptr;
+  ea.zs = n_streams ? io->zs : nullptr;
+  ea.z_bf16 = n_streams ? static_cast<uint16_t *>(io->z) : nullptr;
+  ea.u_buf = s.u_buf;
+  ea.ss_part = s.ss_part;
+  ea.row_cnt = s.row_cnt;
   const bool timed = (c.flags & MOE_FLAG_TIMING) && p->timed_calls < kMaxTimedCalls;
   if (timed && cudaEventRecord(p->ev_start[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
   const cudaError_t le = mma ? launch_experts_mma(p->maps, ea, p->num_sms, ra.chunk_rows, st) : launch_experts(ea, p->num_sms, st);
@@ -410,6 +440,39 @@ moe_status_t moe_forward_dev(void *plan, const void *x, const float *logits, con
   DeviceGuard dg(p->device);
   if (!dg.ok) return MOE_ERR_CUDA;
   return enqueue_step(p, x, logits, p->cfg.max_rows, d_T, y, false, d_status, static_cast<cudaStream_t>(cuda_stream));
+}
+
+moe_status_t moe_forward_fused(void *plan, const void *x, int32_t T, const moe_fused_io_t *io, void *y,
+                               const moe_taps_t *taps, int32_t *d_status, void *cuda_stream) {
+  Plan *p = static_cast<Plan *>(plan);
+  if (!p || !io) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > p->cfg.max_rows) return MOE_ERR_INVALID_ARG;
+  if (p->cfg.flags & MOE_FLAG_PATH_GEMV) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  const auto a4 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  if (io->w_router) {
+    if (!aligned16(io->w_router) || (io->logits && !a4(io->logits))) return MOE_ERR_INVALID_ARG;
+  } else if (!io->logits || !a4(io->logits)) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  const int S = io->num_streams;
+  if (S < 0 || S > kMaxStreams) return MOE_ERR_INVALID_ARG;
+  if (S > 0) {
+    if (!io->resid_in || !io->resid_out || !io->norm_weight || !io->zq || !io->zs) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(io->resid_in) || !aligned16(io->resid_out) || !aligned16(io->norm_weight) || !aligned16(io->zq) ||
+        (io->z && !aligned16(io->z)))
+      return MOE_ERR_INVALID_ARG;
+    if (!a4(io->mix_res) || !a4(io->mix_post) || !a4(io->mix_pre)) return MOE_ERR_INVALID_ARG;
+    if (!(io->rms_eps >= 0.0f) || io->rms_eps > 3.4e38f) return MOE_ERR_INVALID_ARG;  // NaN, negative or infinite
+  }
+  if (d_status && !a4(d_status)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(p->device);
+  if (!dg.ok) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const moe_status_t r = enqueue_step(p, x, nullptr, T, nullptr, y, taps && taps->h_bf16, d_status, st, io);
+  if (r != MOE_OK) return r;
+  return copy_taps(p, taps, T, st);
 }
 
 moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logits_host, int32_t T, void *y_host,

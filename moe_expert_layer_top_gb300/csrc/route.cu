@@ -4,6 +4,12 @@
 // Two phases in one grid:
 //  1. ceil(T/32) routing blocks route their 32 token rows each, while the
 //     other blocks quantise x.
+//     - With a router weight W_r [E][H] (bf16), the logits are computed here
+//       first: each row group has ceil(E/8) projection blocks, each for 8
+//       experts. The last projection block of a row group to finish (a
+//       ticket per row group) routes the group's rows. "Beyond Day-0:
+//       Optimizing DeepSeek-V4.1 Flash in SGLang" 2.1: the router produces
+//       the layout the downstream kernels need.
 //     - Top-k per token row uses one warp per row, in k rounds of warp argmax.
 //     - The combine weights are a softmax over the selected logits in
 //       binary32, using exp_rn.
@@ -132,8 +138,65 @@ struct RouteSmem {
   int32_t tiles[kRouteThreads];
   int32_t offs[kRouteThreads];
   int32_t warp_sums[kRouteThreads / 32];
+  float part[4][kRouterExperts][32];  // router projection: [H quarter][expert][row] partial sums
   int32_t last;  // this block finished phase 1 last
 };
+
+// Router projection for row group rg (rows 32 rg ..) and experts 8 eb .. 8 eb + 7:
+// logits[t][e] = sum_h x[t][h] * W_r[e][h], bf16 operands, binary32 sums.
+// Warp w takes expert 8 eb + w / 4 and the quarter w % 4 of H. Each lane
+// accumulates 8 rows at a time over its 8-column vectors (one fused
+// multiply-add per product, in column order); the warp then sums its lanes by
+// a butterfly, and the four quarters are added in order. The order is fixed,
+// so the logits are the same on every run.
+__device__ void router_block(const RouteArgs &a, int T, int rg, int eb, RouteSmem &sm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int es = warp >> 2, qq = warp & 3;
+  const int e = eb * kRouterExperts + es;
+  const int H = a.H, HQ = H / 4;
+  const int t0 = rg * (kRouteThreads / 32);
+  const int nrows = min(kRouteThreads / 32, T - t0);
+  const uint16_t *wrow = a.w_router + int64_t(e < a.E ? e : 0) * H + qq * HQ;
+  const uint16_t *xrow = a.x + int64_t(t0) * H + qq * HQ;
+  for (int rb = 0; rb < nrows; rb += 8) {
+    float acc[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+    for (int c = lane * 8; c < HQ; c += 256) {
+      const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(wrow + c));
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (rb + r < nrows) {
+          const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xrow + int64_t(rb + r) * H + c));
+          const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[r] = __fmaf_rn(__uint_as_float(xx[i] << 16), __uint_as_float(ww[i] << 16), acc[r]);
+            acc[r] = __fmaf_rn(__uint_as_float(xx[i] & 0xFFFF0000u), __uint_as_float(ww[i] & 0xFFFF0000u), acc[r]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      float v = acc[r];
+#pragma unroll
+      for (int off = 16; off; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+      if (lane == 0 && rb + r < 32) sm.part[qq][es][rb + r] = v;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < kRouterExperts * 32) {
+    const int es2 = threadIdx.x >> 5, r = threadIdx.x & 31;
+    const int e2 = eb * kRouterExperts + es2;
+    if (r < nrows && e2 < a.E) {
+      const float l = __fadd_rn(__fadd_rn(__fadd_rn(sm.part[0][es2][r], sm.part[1][es2][r]), sm.part[2][es2][r]),
+                                sm.part[3][es2][r]);
+      const_cast<float *>(a.logits)[int64_t(t0 + r) * a.E + e2] = l;
+    }
+  }
+}
 
 // Top-k and combine weights, one warp per token row. Each lane keeps its NC
 // candidates (lane, lane + 32, ...) in registers as 64-bit keys: the
@@ -141,12 +204,17 @@ struct RouteSmem {
 // largest key is the largest logit and, among equal logits, the lower id.
 // bm: the block's bitmap in shared memory when one block routes every row
 // (the bits are set here); NULL when the last block builds it in phase 2.
+// rg: the row group (rows 32 rg .. 32 rg + 31, one per warp). The logits are
+// read through L2: with a router weight they were written by other blocks of
+// this grid.
 template <int NC>
-__device__ __forceinline__ void route_topk(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *bm) {
+__device__ __forceinline__ void route_topk(const RouteArgs &a, int T, int rg, RouteSmem &sm, uint32_t *bm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, k = a.k, W = a.words;
   constexpr int kWarps = kRouteThreads / 32;
-  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
+  {
+    const int t = rg * kWarps + warp;
+    if (t >= T) return;
     const float *row = a.logits + int64_t(t) * E;
     uint64_t key[NC];
 #pragma unroll
@@ -154,7 +222,7 @@ __device__ __forceinline__ void route_topk(const RouteArgs &a, int T, RouteSmem 
       const int i = j * 32 + lane;
       key[j] = 0;
       if (i < E) {
-        const uint32_t b = __float_as_uint(__ldg(row + i));
+        const uint32_t b = __float_as_uint(__ldcg(row + i));
         const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
         key[j] = (uint64_t(ord) << 32) | uint32_t(0xFFFFFFFFu - uint32_t(i));
       }
@@ -320,18 +388,22 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
     bad_T = td < 0 || td > a.Tmax;
     T = td < 0 ? 0 : (td > a.Tmax ? a.Tmax : td);
   }
-  const int Rg = route_blocks(a.T);  // routing blocks of the grid
-  const int R = route_blocks(T);     // routing blocks with rows
+  const int Rg = route_blocks(a.T);  // row groups of the grid
+  const int R = route_blocks(T);     // row groups with rows
+  const bool proj = a.w_router != nullptr;
+  const int nrb = proj ? Rg * a.n_eblk : Rg;  // routing (projection) blocks of the grid
   // the step's counters (the expert kernel reads them after this grid completes)
   const int64_t gtid = int64_t(blockIdx.x) * blockDim.x + tid, gstride = int64_t(gridDim.x) * blockDim.x;
   const int64_t n_comb = int64_t(T) * a.comb_per_row;
   for (int64_t i = gtid; i < a.n_tiles_max; i += gstride) a.ready[i] = 0;
   for (int64_t i = gtid; i < n_comb; i += gstride) a.comb_cnt[i] = 0;
+  if (a.row_cnt)
+    for (int64_t i = gtid; i < T; i += gstride) a.row_cnt[i] = 0;
 
-  if (int(blockIdx.x) >= Rg) {  // x quantisation
+  if (int(blockIdx.x) >= nrb) {  // x quantisation
     const int64_t groups = int64_t(T) * (a.H / kGroup);
-    const int64_t qstride = int64_t(gridDim.x - Rg) * blockDim.x;
-    for (int64_t g = int64_t(blockIdx.x - Rg) * blockDim.x + tid; g < groups; g += qstride)
+    const int64_t qstride = int64_t(gridDim.x - nrb) * blockDim.x;
+    for (int64_t g = int64_t(blockIdx.x - nrb) * blockDim.x + tid; g < groups; g += qstride)
       quantize_group32(a.x + g * kGroup, a.xq + g * kGroup, a.xs + g);
     return;
   }
@@ -348,7 +420,22 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
       }
     }
   }
-  if (int(blockIdx.x) >= R) return;  // no rows for this routing block
+  int rg = int(blockIdx.x);  // this block's row group
+  if (proj) {
+    rg = int(blockIdx.x) / a.n_eblk;
+    if (rg >= R) return;  // no rows for this row group
+    router_block(a, T, rg, int(blockIdx.x) % a.n_eblk, sm);
+    // The last projection block of the row group routes its rows (ticket
+    // after a fence; the counter wraps back to zero on the last ticket).
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sm.last = atomicInc(a.rg_cnt + rg, uint32_t(a.n_eblk - 1)) == uint32_t(a.n_eblk - 1);
+    __syncthreads();
+    if (!sm.last) return;
+    __threadfence();  // the other projection blocks' logits, before they are read
+  } else if (rg >= R) {
+    return;  // no rows for this routing block
+  }
   // One routing block keeps the bitmap in shared memory from the start and
   // needs no ticket.
   const bool single = R == 1;
@@ -360,12 +447,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
   // --- phase 1: top-k + combine weights, one warp per row
   uint32_t *bits = single ? bm : nullptr;
   const int nc = (a.E + 31) / 32;
-  if (nc <= 1) route_topk<1>(a, T, sm, bits);
-  else if (nc <= 2) route_topk<2>(a, T, sm, bits);
-  else if (nc <= 4) route_topk<4>(a, T, sm, bits);
-  else if (nc <= 8) route_topk<8>(a, T, sm, bits);
-  else if (nc <= 16) route_topk<16>(a, T, sm, bits);
-  else route_topk<32>(a, T, sm, bits);
+  if (nc <= 1) route_topk<1>(a, T, rg, sm, bits);
+  else if (nc <= 2) route_topk<2>(a, T, rg, sm, bits);
+  else if (nc <= 4) route_topk<4>(a, T, rg, sm, bits);
+  else if (nc <= 8) route_topk<8>(a, T, rg, sm, bits);
+  else if (nc <= 16) route_topk<16>(a, T, rg, sm, bits);
+  else route_topk<32>(a, T, rg, sm, bits);
 
   // --- phase 2 in the last routing block to finish phase 1 (ticket after a
   // fence; the ticket counter wraps back to zero on the last ticket)
@@ -386,15 +473,16 @@ cudaError_t prepare_route(size_t smem) {
   return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
 }
 
-// R routing blocks, then one block per 1024 32-groups of x.
-int route_grid(int T, int H) {
+// R routing blocks (R * ceil(E/8) projection blocks with a router weight),
+// then one block per 1024 32-groups of x.
+int route_grid(int T, int H, int nproj) {
   const int64_t groups = int64_t(T) * (H / kGroup);
-  return route_blocks(T) + int((groups + kRouteThreads - 1) / kRouteThreads);
+  return route_blocks(T) * nproj + int((groups + kRouteThreads - 1) / kRouteThreads);
 }
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
   const size_t smem = route_smem_bytes(a.E, a.words);
-  route_kernel<<<route_grid(a.T, a.H), kRouteThreads, smem, st>>>(a);
+  route_kernel<<<route_grid(a.T, a.H, a.w_router ? a.n_eblk : 1), kRouteThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

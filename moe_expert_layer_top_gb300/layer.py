@@ -99,6 +99,43 @@ class MoEStep:
         st = stream if stream is not None else torch.cuda.current_stream(x.device)
         abi.check("moe_forward_dev", abi.moe_forward_dev(self.plan, x, logits, d_T, y, d_status, st))
 
+    def forward_fused(self, x: torch.Tensor, w_router: torch.Tensor | None = None,
+                      logits: torch.Tensor | None = None, resid: torch.Tensor | None = None,
+                      norm_weight: torch.Tensor | None = None, rms_eps: float = 1e-6,
+                      mix_res: torch.Tensor | None = None, mix_post: torch.Tensor | None = None,
+                      mix_pre: torch.Tensor | None = None, in_place: bool = False, z_tap: bool = False,
+                      taps: abi.MoeTaps | None = None, d_status: torch.Tensor | None = None,
+                      stream=None) -> dict:
+        """One step with the steps on either side fused into its kernels.
+
+        w_router (bf16 [E][H]) computes the logits on the device; they are
+        returned as "logits". Without it, logits (fp32 [T][E]) is the input.
+        resid (bf16 [T][S][H], S <= 4) turns on the epilogue. It returns the
+        new streams ("resid", the same tensor when in_place) and the next
+        layer's MXFP8 input ("zq", "zs"), plus "z" (bf16) when z_tap is set.
+        """
+        T = x.shape[0]
+        dev = x.device
+        out = {"y": torch.empty((T, self.H), dtype=torch.bfloat16, device=dev)}
+        if w_router is not None:
+            out["logits"] = logits if logits is not None else torch.empty((T, self.E), dtype=torch.float32,
+                                                                             device=dev)
+        io = abi.fused_io(w_router=w_router, logits=out.get("logits", logits))
+        if resid is not None:
+            S = resid.shape[1]
+            out["resid"] = resid if in_place else torch.empty_like(resid)
+            out["zq"] = torch.empty((T, self.H), dtype=torch.uint8, device=dev)
+            out["zs"] = torch.empty((T, self.H // 32), dtype=torch.uint8, device=dev)
+            if z_tap:
+                out["z"] = torch.empty((T, self.H), dtype=torch.bfloat16, device=dev)
+            io = abi.fused_io(w_router=w_router, logits=out.get("logits", logits), num_streams=S, resid_in=resid,
+                              resid_out=out["resid"], mix_res=mix_res, mix_post=mix_post, mix_pre=mix_pre,
+                              norm_weight=norm_weight, rms_eps=rms_eps, zq=out["zq"], zs=out["zs"],
+                              z=out.get("z"))
+        st = stream if stream is not None else torch.cuda.current_stream(dev)
+        abi.check("moe_forward_fused", abi.moe_forward_fused(self.plan, x, T, io, out["y"], taps, d_status, st))
+        return out
+
     def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, y_host: torch.Tensor, stream=None) -> int:
         st = stream if stream is not None else torch.cuda.current_stream()
         return abi.moe_forward_host(self.plan, x_host, logits_host, x_host.shape[0], y_host, st)

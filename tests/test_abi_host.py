@@ -109,6 +109,8 @@ def test_null_arguments_return_codes(lib):
     assert h.value is None  # *plan_out is cleared on failure
     assert lib.moe_forward(None, None, None, 6, None, None, None, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_forward_host(None, None, None, 6, None, None) == abi.MOE_ERR_INVALID_ARG
+    io = abi.fused_io()
+    assert lib.moe_forward_fused(None, None, 6, ctypes.byref(io), None, None, None, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_destroy(None) == abi.MOE_OK
     assert lib.moe_quantize_mxfp8(None, 4, 48, None, None, None) == abi.MOE_ERR_INVALID_ARG  # cols % 32
     assert lib.moe_quantize_mxfp8(None, 0, 64, None, None, None) == abi.MOE_OK               # empty

@@ -1,0 +1,256 @@
+"""GPU parity of the steps fused on either side of the MoE step (moe_forward_fused).
+
+In front, the router projection: logits = x . W_r^T (bf16 operands, binary32
+sums) in the route kernel.
+* The logits are within the binary32 summation bound of the oracle's:
+  gamma_d * sum_h |x_h w_h|, with d = H/128 + 16. That d bounds the
+  sequential roundings any product meets: the per-lane sums, the butterfly
+  and the adds over the four H quarters.
+* Routing, weights and placement are bit-exact against the oracle's top-k
+  applied to the GPU's own logits. The decision is taken in the kernel's
+  precision.
+* The expert ids equal the oracle's from its own logits on every row whose
+  top-k margins exceed twice the bound.
+Behind, the residual-stream epilogue in the tensor-core kernel's combine.
+* New streams are compared with the oracle applied to the GPU's own y:
+  bit-exact with one plain stream, within one bf16 step with mixing.
+* z is within one bf16 step (at least 99 % equal).
+* The MXFP8 codes are bit-exact on the GPU's own z.
+* The whole chain is within the y tolerance of the oracle's chain.
+Source: "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", section 2.1.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from moe_expert_layer_top_gb300 import abi, synthetic
+from moe_expert_layer_top_gb300.layer import MoEStep, taps_for
+
+from gpu_cases import bf16_dev_to_bits, check_y, oracle_experts, rel_fro, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import moe_expert_layer_top_gb300 as pkg
+    pkg.build.build()
+    abi.load()
+    assert torch.cuda.is_available()
+
+
+def dev_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).to(device)
+
+
+def logits_bound(x_bits, wr_bits) -> np.ndarray:
+    """Largest binary32 summation error of a projection logit, per (t, e)."""
+    H = x_bits.shape[1]
+    d = H // 128 + 16
+    u = 2.0 ** -24
+    gam = d * u / (1 - d * u)
+    ax = np.abs(oracle.bf16_bits_to_f64(x_bits))
+    aw = np.abs(oracle.bf16_bits_to_f64(wr_bits))
+    return gam * (ax @ aw.T) + 1e-30
+
+
+def topk_margin(lg: np.ndarray, k: int) -> np.ndarray:
+    """Smallest gap between adjacent values among each row's k + 1 largest."""
+    s = -np.sort(-lg.astype(np.float64), axis=1)[:, : k + 1]
+    return np.min(s[:, :-1] - s[:, 1:], axis=1)
+
+
+def check_routing_from_gpu_logits(t: dict, lg_gpu: np.ndarray, k: int, E: int):
+    ids = oracle.topk_ids(lg_gpu, k)
+    w = oracle.softmax_topk_weights(lg_gpu, ids)
+    plc = oracle.placement(ids, E)
+    np.testing.assert_array_equal(t["topk_ids"], ids)
+    np.testing.assert_array_equal(t["topk_w"].view(np.uint32), w.view(np.uint32))
+    np.testing.assert_array_equal(t["bitmap"].view(np.uint32), plc["bitmap"])
+    np.testing.assert_array_equal(t["counts"], plc["counts"])
+    ref_slot = (plc["slot_e"].astype(np.int64) << 16) | (plc["slot_tile"] * 8 + plc["slot_row"])
+    np.testing.assert_array_equal(t["slot"].astype(np.int64), ref_slot)
+    return ids
+
+
+# T spans one and two row groups of 32 with a ragged tail; E = 12 leaves a
+# partial block of 8 experts.
+@pytest.mark.parametrize("T,H,E,k,I,shared", [
+    (6, 512, 8, 2, 256, 0),
+    (40, 512, 12, 3, 256, 1),
+    (70, 1024, 64, 8, 256, 0),
+])
+def test_router_projection(T, H, E, k, I, shared):
+    dev = torch.device("cuda", 0)
+    seed = 31
+    w = synthetic.make_weights(seed, E, H, I, shared, dev)
+    x_bits = synth.x_bf16(seed, T, H)
+    wr_bits = synth.router_weight_bf16(seed, E, H)
+    step = MoEStep(H, I, E, k, w, T, shared)
+    taps, tt = taps_for(T, k, E, H, I, shared, dev)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    out = step.forward_fused(dev_bf16(x_bits), w_router=dev_bf16(wr_bits), taps=taps, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == abi.MOE_OK
+    lg_gpu = to_np(out["logits"])
+    lg_ref = oracle.router_logits(x_bits, wr_bits)
+    bound = logits_bound(x_bits, wr_bits)
+    err = np.abs(lg_gpu.astype(np.float64) - lg_ref.astype(np.float64))
+    assert np.all(err <= bound + np.abs(lg_ref) * 2.0 ** -24), float(np.max(err / bound))
+    t = {n: to_np(v) for n, v in tt.items()}
+    ids = check_routing_from_gpu_logits(t, lg_gpu, k, E)
+    # rows with clear margins route as the oracle's own logits do
+    clear = topk_margin(lg_ref, k) > 2 * np.max(bound, axis=1)
+    assert np.mean(clear) > 0.5
+    np.testing.assert_array_equal(ids[clear], oracle.topk_ids(lg_ref, k)[clear])
+    # the step itself, on the GPU's logits
+    get = oracle_experts(seed, E, H, I)
+    sh = oracle.expert_weights_from_synth(seed, "shared", H, I) if shared else None
+    r = oracle.moe_step(x_bits, lg_gpu, k, get, shared=sh)
+    np.testing.assert_array_equal(t["xq"], r["xq"])
+    np.testing.assert_array_equal(t["xs"], r["xs"])
+    check_y(bf16_dev_to_bits(out["y"]), r["y"])
+    # deterministic: a second run gives the same logits and y
+    out2 = step.forward_fused(dev_bf16(x_bits), w_router=dev_bf16(wr_bits))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(out2["logits"]).view(np.uint32), lg_gpu.view(np.uint32))
+    np.testing.assert_array_equal(bf16_dev_to_bits(out2["y"]), bf16_dev_to_bits(out["y"]))
+    step.close()
+
+
+def test_fused_without_extras_equals_moe_forward():
+    dev = torch.device("cuda", 0)
+    T, H, E, k, I = 24, 512, 16, 4, 256
+    w = synthetic.make_weights(5, E, H, I, 0, dev)
+    x, lg, _, _ = synthetic.make_inputs(5, T, H, E, k, "zipf", dev)
+    step = MoEStep(H, I, E, k, w, T, 0)
+    y0 = step.forward(x, lg)
+    out = step.forward_fused(x, logits=lg)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bf16_dev_to_bits(out["y"]), bf16_dev_to_bits(y0))
+    step.close()
+
+
+def _epilogue_inputs(seed, T, S, H, mixed):
+    resid = synth.residual_bf16(seed, T, S, H)
+    gamma = synth.norm_weight_bf16(seed, H)
+    coef = synth.mix_coefficients(seed, T, S) if mixed else (None, None, None)
+    return resid, gamma, coef
+
+
+@pytest.mark.parametrize("T,H,E,k,I,S,mixed,in_place", [
+    (6, 512, 8, 2, 256, 1, False, False),
+    (37, 1024, 16, 4, 256, 1, False, True),
+    (20, 512, 8, 2, 384, 4, True, False),
+    (9, 1024, 16, 3, 256, 2, True, True),
+])
+def test_residual_norm_epilogue(T, H, E, k, I, S, mixed, in_place):
+    dev = torch.device("cuda", 0)
+    seed = 23
+    w = synthetic.make_weights(seed, E, H, I, 0, dev)
+    x, lg, x_bits, lg_np = synthetic.make_inputs(seed, T, H, E, k, "uniform", dev)
+    resid, gamma, (res, post, pre) = _epilogue_inputs(seed, T, S, H, mixed)
+    to_dev = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    eps = 1e-6
+    step = MoEStep(H, I, E, k, w, T, 0)
+    resid_dev = dev_bf16(resid)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    out = step.forward_fused(x, logits=lg, resid=resid_dev, norm_weight=dev_bf16(gamma), rms_eps=eps,
+                             mix_res=to_dev(res), mix_post=to_dev(post), mix_pre=to_dev(pre), in_place=in_place,
+                             z_tap=True, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == abi.MOE_OK
+    if in_place:
+        assert out["resid"].data_ptr() == resid_dev.data_ptr()
+    y_gpu = bf16_dev_to_bits(out["y"])
+    ref = oracle.residual_norm_mxfp8(y_gpu, resid, gamma, eps, res, post, pre)
+    got_resid = bf16_dev_to_bits(out["resid"]).reshape(T, S, H)
+    if not mixed:
+        np.testing.assert_array_equal(got_resid, ref["resid"])
+    else:
+        d = np.abs(got_resid.astype(np.int32) - ref["resid"].astype(np.int32))
+        assert d.max() <= 1 and np.mean(d == 0) > 0.99
+    z_gpu = bf16_dev_to_bits(out["z"])
+    dz = np.abs(z_gpu.astype(np.int32) - ref["z"].astype(np.int32))
+    assert dz.max() <= 1 and np.mean(dz == 0) > 0.99, (dz.max(), np.mean(dz == 0))
+    q, s = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(z_gpu))
+    np.testing.assert_array_equal(to_np(out["zq"]), q)
+    np.testing.assert_array_equal(to_np(out["zs"]), s)
+    # the whole chain against the oracle's own y
+    get = oracle_experts(seed, E, H, I)
+    y_ref = oracle.moe_step(x_bits, lg_np, k, get)["y"]
+    chain = oracle.residual_norm_mxfp8(y_ref, resid, gamma, eps, res, post, pre)
+    check_y(z_gpu, chain["z"])
+    assert rel_fro(oracle.bf16_bits_to_f64(got_resid), oracle.bf16_bits_to_f64(chain["resid"])) <= 1e-2
+    step.close()
+
+
+def test_projection_and_epilogue_full_size_bs1():
+    """Both fused steps at the bs1 shape (T=6, H=4096, E=256, k=8, I=2048):
+    the logits, routing and epilogue everywhere, y on two sampled rows."""
+    dev = torch.device("cuda", 0)
+    T, H, E, k, I = 6, 4096, 256, 8, 2048
+    seed = 42
+    w = synthetic.make_weights(seed, E, H, I, 0, dev)
+    x_bits = synth.x_bf16(seed, T, H)
+    wr_bits = synth.router_weight_bf16(seed, E, H)
+    resid, gamma, _ = _epilogue_inputs(seed, T, 1, H, False)
+    step = MoEStep(H, I, E, k, w, T, 0)
+    taps, tt = taps_for(T, k, E, H, I, 0, dev)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    out = step.forward_fused(dev_bf16(x_bits), w_router=dev_bf16(wr_bits), resid=dev_bf16(resid),
+                             norm_weight=dev_bf16(gamma), rms_eps=1e-6, z_tap=True, taps=taps, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == abi.MOE_OK
+    lg_gpu = to_np(out["logits"])
+    lg_ref = oracle.router_logits(x_bits, wr_bits)
+    err = np.abs(lg_gpu.astype(np.float64) - lg_ref)
+    assert np.all(err <= logits_bound(x_bits, wr_bits) + np.abs(lg_ref) * 2.0 ** -24)
+    t = {n: to_np(v) for n, v in tt.items()}
+    check_routing_from_gpu_logits(t, lg_gpu, k, E)
+    y_gpu = bf16_dev_to_bits(out["y"])
+    ref = oracle.residual_norm_mxfp8(y_gpu, resid, gamma, 1e-6)
+    np.testing.assert_array_equal(bf16_dev_to_bits(out["resid"]).reshape(T, 1, H), ref["resid"])
+    z_gpu = bf16_dev_to_bits(out["z"])
+    assert np.abs(z_gpu.astype(np.int32) - ref["z"].astype(np.int32)).max() <= 1
+    q, s = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(z_gpu))
+    np.testing.assert_array_equal(to_np(out["zq"]), q)
+    np.testing.assert_array_equal(to_np(out["zs"]), s)
+    rows = [0, 5]
+    r = oracle.moe_step(x_bits, lg_gpu, k, oracle_experts(seed, E, H, I), rows=rows)
+    check_y(y_gpu[rows], r["y"][rows])
+    step.close()
+
+
+def test_fused_argument_errors():
+    dev = torch.device("cuda", 0)
+    T, H, E, k, I = 4, 512, 8, 2, 256
+    w = synthetic.make_weights(3, E, H, I, 0, dev)
+    x = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
+    lg = torch.zeros((T, E), dtype=torch.float32, device=dev)
+    y = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
+    resid = torch.zeros((T, 1, H), dtype=torch.bfloat16, device=dev)
+    g = torch.ones((H,), dtype=torch.bfloat16, device=dev)
+    zq = torch.zeros((T, H), dtype=torch.uint8, device=dev)
+    zs = torch.zeros((T, H // 32), dtype=torch.uint8, device=dev)
+    step = MoEStep(H, I, E, k, w, T, 0)
+    call = lambda io, TT=T: abi.moe_forward_fused(step.plan, x, TT, io, y)
+    assert call(abi.fused_io()) == abi.MOE_ERR_INVALID_ARG                       # no logits, no router weight
+    assert call(None) == abi.MOE_ERR_INVALID_ARG
+    assert call(abi.fused_io(logits=lg), T + 1) == abi.MOE_ERR_INVALID_ARG       # T > max_rows
+    assert call(abi.fused_io(logits=lg), 0) == abi.MOE_OK                        # empty step
+    ok = dict(logits=lg, num_streams=1, resid_in=resid, resid_out=resid, norm_weight=g, rms_eps=1e-6, zq=zq, zs=zs)
+    assert call(abi.fused_io(**{**ok, "num_streams": 5})) == abi.MOE_ERR_INVALID_ARG
+    assert call(abi.fused_io(**{**ok, "norm_weight": None})) == abi.MOE_ERR_INVALID_ARG
+    assert call(abi.fused_io(**{**ok, "rms_eps": -1.0})) == abi.MOE_ERR_INVALID_ARG
+    assert call(abi.fused_io(**{**ok, "rms_eps": float("nan")})) == abi.MOE_ERR_INVALID_ARG
+    assert call(abi.fused_io(**{**ok, "zq": zq.data_ptr() + 8})) == abi.MOE_ERR_INVALID_ARG
+    assert call(abi.fused_io(w_router=g.data_ptr() + 2)) == abi.MOE_ERR_INVALID_ARG  # misaligned router weight
+    assert call(abi.fused_io(**ok)) == abi.MOE_OK
+    torch.cuda.synchronize()
+    step.close()
+    gemv = MoEStep(H, I, E, k, w, T, 0, abi.MOE_FLAG_PATH_GEMV)
+    assert abi.moe_forward_fused(gemv.plan, x, T, abi.fused_io(logits=lg), y) == abi.MOE_ERR_UNSUPPORTED
+    gemv.close()
