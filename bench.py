@@ -283,6 +283,120 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed, flags=0):
     return res
 
 
+def time_fused_workload(wl, weights, steps, warmup, flush_buf, seed, n_streams):
+    """Times moe_forward_fused three ways on the same routing. Buffers are
+    allocated once.
+    * "full": the router projection from a bf16 W_r [E][H] in front, and
+      n_streams residual streams behind (mixing coefficients when more than
+      one) with RMSNorm + MXFP8.
+    * "projection": the router projection alone.
+    * "plain": the plain step on the logits that the projection produced.
+    The differences are the cost of each fused step."""
+    import numpy as np
+    import torch
+    import synth
+    from moe_expert_layer_top_gb300 import abi
+    from moe_expert_layer_top_gb300.layer import MoEStep, MoEWeightsMXFP8
+    w = weights if wl.shared else MoEWeightsMXFP8(weights.w_gate, weights.s_gate, weights.w_up, weights.s_up,
+                                                  weights.w_down, weights.s_down)
+    wfmt = abi.MOE_WEIGHTS_MXFP4 if wl.fmt == "mxfp4" else abi.MOE_WEIGHTS_MXFP8
+    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, weight_format=wfmt, swiglu_limit=wl.swiglu_limit)
+    bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16).copy()).view(torch.bfloat16).cuda()
+    T, H, S = wl.T, wl.H, n_streams
+    x = bf(synth.x_bf16(seed, T, H))
+    wr = bf(synth.router_weight_bf16(seed, wl.E, H))
+    resid = bf(synth.residual_bf16(seed, T, S, H))
+    gamma = bf(synth.norm_weight_bf16(seed, H))
+    coef = [None, None, None]
+    if S > 1:
+        coef = [torch.from_numpy(c).cuda() for c in synth.mix_coefficients(seed, T, S)]
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty((T, wl.E), dtype=torch.float32, device="cuda")
+    logits_in = torch.empty_like(logits)
+    resid_out = torch.empty_like(resid)
+    zq = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+    zs = torch.empty((T, H // 32), dtype=torch.uint8, device="cuda")
+    ios = {
+        "full": abi.fused_io(w_router=wr, logits=logits, num_streams=S, resid_in=resid, resid_out=resid_out,
+                             mix_res=coef[0], mix_post=coef[1], mix_pre=coef[2], norm_weight=gamma, rms_eps=1e-6,
+                             zq=zq, zs=zs),
+        "projection": abi.fused_io(w_router=wr, logits=logits),
+        "plain": abi.fused_io(logits=logits_in),
+    }
+    stream = torch.cuda.current_stream()
+    abi.check("moe_forward_fused", abi.moe_forward_fused(step.plan, x, T, ios["projection"], y, None, None, stream))
+    torch.cuda.synchronize()
+    logits_in.copy_(logits)
+    active = active_experts(logits.cpu().numpy(), wl.k, wl.shared)
+    out = {"active_experts": active, "extra_bytes": wl.E * H * 2 + 2 * T * S * H * 2 + H * 2 + T * H + T * H // 32}
+    bad = []
+    for name, io in ios.items():
+        st_words = torch.full((warmup + steps,), -1, dtype=torch.int32, device="cuda")
+        for i in range(warmup):
+            flush_buf.zero_()
+            abi.check("moe_forward_fused", abi.moe_forward_fused(step.plan, x, T, io, y, None, st_words[i:i + 1],
+                                                                 stream))
+        torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush_buf.zero_()
+            starts[i].record(stream)
+            abi.moe_forward_fused(step.plan, x, T, io, y, None, st_words[warmup + i:warmup + i + 1], stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        per_step = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        bad += [v for v in st_words.cpu().tolist() if v != abi.MOE_OK]
+        out[name] = {"ms_mean": sum(per_step) / len(per_step), "ms_median": statistics.median(per_step)}
+    step.close()
+    out["ms_mean"], out["ms_median"] = out["full"]["ms_mean"], out["full"]["ms_median"]
+    out["status"] = bad[0] if bad else 0
+    return out
+
+
+def mxfp8_tensor_peak():
+    """Dense block-scaled MXFP8 MMA peak (TFLOP/s): the measured bf16 GEMM burst
+    figure times the nominal fp8 / bf16 ratio (4.5 / 2.25)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "measured bf16 burst x 2 (nominal fp8/bf16 ratio)"
+    return 2.0 * 1900.0, "fallback bf16 x 2"
+
+
+def step_flops(wl):
+    """Algorithmic flops of the expert GEMMs of one step: 2 * (T*k + T*shared) * 3 * H * I."""
+    return 2 * (wl.T * wl.k + wl.T * wl.shared) * 3 * wl.H * wl.I
+
+
+def time_l2_warm_graph(step, x, lg, wl, steps):
+    """Secondary figure: one step captured in a CUDA graph (moe_forward_dev with
+    the row count on the device), replayed back to back with no L2 flush."""
+    import torch
+    d_T = torch.full((1,), wl.T, dtype=torch.int32, device="cuda")
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step.forward_dev(x, lg, d_T, y, status)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step.forward_dev(x, lg, d_T, y, status)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(steps):
+            g.replay()
+        b.record(s)
+        torch.cuda.synchronize()
+    return {"us_per_step": round(a.elapsed_time(b) * 1e3 / steps, 3), "status": int(status.item()),
+            "how": f"one step captured in a CUDA graph (device-side row count), replayed {steps} times back to "
+                   "back with no L2 flush"}
+
+
 def time_e2e(step, wl, seed, steps, warmup):
     """moe_forward_host: pinned host x/logits in, host y out, copies inside the timed region."""
     import numpy as np
@@ -335,6 +449,8 @@ def run_gpu(args):
         import dataclasses
         wl = dataclasses.replace(wl, E=args.experts, name=f"{wl.name}-E{args.experts}")
         args.no_cpu_baseline = args.no_others = True
+    if args.fused:
+        args.no_cpu_baseline = True
 
     # The oracle's worker pool is spawned before the first GPU call.
     cpu_q = None
@@ -372,6 +488,20 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     flags = PATH_FLAGS[args.path]
+    if args.fused:
+        r = time_fused_workload(wl, weights, args.steps, args.warmup, flush_buf, seed, args.fused)
+        clocks.stop()
+        if rank == 0:
+            print(json.dumps({"metric": "fused MoE step us (router projection + residual streams + RMSNorm + MXFP8)",
+                              "workload": wl.name, "streams": args.fused, "value": round(r["ms_mean"] * 1e3, 3),
+                              "unit": "us/step", "us_median": round(r["ms_median"] * 1e3, 3),
+                              "us_projection_only": round(r["projection"]["ms_mean"] * 1e3, 3),
+                              "us_same_routing_plain": round(r["plain"]["ms_mean"] * 1e3, 3),
+                              "active_experts": r["active_experts"],
+                              "status": r["status"], "steps": args.steps, "warmup": args.warmup}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     main = time_gpu_workload(wl, weights, args.steps, args.warmup, flush_buf, seed, flags)
     torch.cuda.synchronize()
     if world > 1:
@@ -381,12 +511,16 @@ def run_gpu(args):
     ms, exp_ms = max_over_ranks([main["ms_mean"], main["expert_ms_mean"]], world, "cuda")
 
     e2e = None if args.no_e2e else time_e2e(main["step"], wl, seed, max(args.steps, 10), 3)
+    l2_warm = None
+    if kernel_path(args.path, wl.T) == "mma" and world == 1:
+        l2_warm = time_l2_warm_graph(main["step"], main["x"], main["lg"], wl, max(args.steps, 10))
 
     also = {}
     if not args.no_others and world == 1:
         others = ["bs4", "bs16", "bs64"]
         if flags != PATH_FLAGS["gemv"]:
             others += ["bs1_fp4", "bs4_fp4", "bs64_fp4"]  # MXFP4: tensor-core kernel only
+        tpeak, _ = mxfp8_tensor_peak()
         for name in others:
             if name == wl.name:
                 continue
@@ -402,8 +536,26 @@ def run_gpu(args):
                           "active_experts": r["active_experts"],
                           "expert_gbs": round(r["weight_bytes"] / (r["expert_ms_mean"] * 1e-3) / 1e9, 1),
                           "expert_frac": round(r["weight_bytes"] / (r["expert_ms_mean"] * 1e-3) / 1e9 / peak, 3),
+                          "tensor_tflops": round(step_flops(o) / (r["expert_ms_mean"] * 1e-3) / 1e12, 1),
+                          "tensor_frac": round(step_flops(o) / (r["expert_ms_mean"] * 1e-3) / 1e12 / tpeak, 4),
                           "status": r["status"]}
             r["step"].close()
+        # the steps either side, fused: router projection + residual streams + RMSNorm + MXFP8
+        if flags != PATH_FLAGS["gemv"]:
+            for base, S in (("bs1", 1), ("bs64", 4)):
+                o = synth.WORKLOADS[base]
+                r = time_fused_workload(o, weights_for(o), max(args.steps // 2, 5), max(args.warmup, 3), flush_buf,
+                                        seed, S)
+                us = {n: r[n]["ms_mean"] * 1e3 for n in ("full", "projection", "plain")}
+                also[f"{base}_fused_s{S}"] = {
+                    "T": o.T, "streams": S, "router_projection": f"bf16 W_r [{o.E}][{o.H}]",
+                    "active_experts": r["active_experts"],
+                    "us_per_step": round(us["full"], 2), "us_median": round(r["ms_median"] * 1e3, 2),
+                    "us_same_routing_plain": round(us["plain"], 2),
+                    "us_projection_only": round(us["projection"], 2),
+                    "projection_us": round(us["projection"] - us["plain"], 2),
+                    "epilogue_us": round(us["full"] - us["projection"], 2),
+                    "extra_bytes": r["extra_bytes"], "status": r["status"]}
 
     if rank != 0:
         main["step"].close()
@@ -462,6 +614,13 @@ def run_gpu(args):
             "kernel_us": round(exp_ms * 1e3, 3),
         },
         "e2e": e2e,
+        "l2_warm": l2_warm,
+        "tensor": {"tflops": round(step_flops(wl) / (exp_ms * 1e-3) / 1e12, 2),
+                   "peak": round(mxfp8_tensor_peak()[0], 1), "peak_kind": mxfp8_tensor_peak()[1],
+                   "frac": round(step_flops(wl) / (exp_ms * 1e-3) / 1e12 / mxfp8_tensor_peak()[0], 5),
+                   "flops_per_step": step_flops(wl),
+                   "note": "expert GEMM flops 2*(T*k + T*shared)*3*H*I over the expert kernel time; the step is "
+                           "bound by HBM at this row count"},
         "gpu_launches": 2 * args.steps,
         "clocks": summarise_clocks(clock_rows),
     }
@@ -520,6 +679,9 @@ def main():
                     choices=["tiny", "bs1", "bs4", "bs16", "bs64", "bs1_fp4", "bs4_fp4", "bs64_fp4"])
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="expert kernel: auto (the library default: mma), or pin gemv / mma")
+    ap.add_argument("--fused", type=int, default=0, choices=[0, 1, 2, 3, 4],
+                    help="time only the fused step (router projection + this many residual streams with "
+                         "RMSNorm + MXFP8) on the workload; prints its own line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

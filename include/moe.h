@@ -32,7 +32,8 @@
  *      - scratch buffers are reused across calls.
  *  - Same page, section 3.1. The MoE kernels fuse the clipped SwiGLU and keep
  *    the original intermediate rounding. Here g and u are rounded to bf16,
- *    and h = bf16(silu(g) * u) is then quantised to MXFP8. No clip is applied.
+ *    and h = bf16(silu(g) * u) is then quantised to MXFP8. The clip limit is
+ *    a config value (moe_config_t.swiglu_limit; 0 = no clip).
  *  - "FlyDSL Mono Kernels for High-Interactivity LLM Serving in ATOM",
  *    "MiniMax-M3: Connecting Attention and Experts". Each expert does an
  *    up/gate and a down projection, for the shared and the routed experts.
@@ -211,14 +212,17 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
 moe_status_t moe_forward_dev(void *plan, const void *x, const float *logits, const int32_t *d_T, void *y,
                              int32_t *d_status, void *cuda_stream);
 
-/* The steps on either side of the MoE step, fused into its two kernels.
+/* The steps on either side of the MoE step: the router projection fused into
+ * the route kernel, and the residual-stream epilogue as one kernel launched
+ * right behind the expert kernel with programmatic dependent launch (PDL).
  * Source: "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", section 2.1:
  *  - MoE bullet: the router produces the downstream layout directly; the
  *    kernels also fuse the mHC output combination, the next layer's input
  *    combination or normalisation, to cut intermediate writes;
  *  - mHC bullet: the weighted combination of the four residual streams is
- *    fused with RMSNorm, with quantisation on supported paths;
- *  - small-operator bullet: RMSNorm is fused with MXFP8 quantisation.
+ *    fused with RMSNorm in one kernel, with quantisation on supported paths;
+ *  - small-operator bullet: RMSNorm is fused with MXFP8 quantisation;
+ *  - communication bullet: PDL overlaps portions of adjacent kernels.
  *
  * In front (w_router set): the route kernel computes the router logits
  *   logits[t][e] = sum_h x[t][h] * w_router[e][h]
@@ -227,7 +231,7 @@ moe_status_t moe_forward_dev(void *plan, const void *x, const float *logits, con
  * logits.
  *
  * Behind (num_streams = S > 0): each token row carries S residual streams.
- * Once y[t] is combined (bf16), the expert kernel computes:
+ * Once y is complete (bf16), the epilogue kernel computes, per row:
  *   new_s[t] = sum_s' mix_res[t][s][s'] * resid_in[t][s'] + mix_post[t][s] * y[t]
  *              (binary32, stored as bf16 in resid_out)
  *   u[t]     = sum_s mix_pre[t][s] * new_s[t]                  (binary32)

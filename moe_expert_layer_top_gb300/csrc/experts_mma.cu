@@ -53,7 +53,6 @@
 #include <string.h>
 
 #include "combine.cuh"
-#include "residual_norm.cuh"
 #include "device.cuh"
 #include "internal.h"
 
@@ -696,7 +695,6 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
           const int t = int(sm.jobs[jj]);
           uint16_t yb[kBM / 32];
           combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, T, a.k, a.shared, a.H, t, int64_t(m.blk) * kBM, lane, yb);
-          if (a.n_streams) residual_block<kBM / 32>(a, t, int64_t(m.blk) * kBM, m.blk, hbd, lane, yb);
         }
       }
       named_bar(kBarEpi, kEpiThreads);
@@ -742,6 +740,9 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
 
   // Everything below reads the router's outputs.
   pdl_wait_primary();
+  // A dependent kernel (the residual-stream epilogue) may now be scheduled;
+  // it waits for this grid to complete before it reads y.
+  pdl_launch_dependents();
   // the step's row count: a.T, or the device-side value (clamped as the route kernel does)
   int T = a.T;
   if (a.d_T) {

@@ -48,9 +48,6 @@ struct Scratch {
   // fused steps (moe_forward_fused)
   float *logits_proj;   // [Tmax][E] router logits computed by the route kernel
   uint32_t *rg_cnt;     // [ceil(Tmax/32)] projection blocks finished per row group (zero between steps)
-  float *u_buf;         // [Tmax][H] next layer's input combination (fp32)
-  float *ss_part;       // [Tmax][H/128] per-block sums of u^2
-  uint32_t *row_cnt;    // [Tmax] combined blocks per token row
   // staging for moe_forward_host
   void *x_dev;
   float *logits_dev;
@@ -92,7 +89,6 @@ struct RouteArgs {
   const uint16_t *w_router;  // bf16 [E][H] router weight, or NULL (logits are an input)
   uint32_t *rg_cnt;          // per row group: projection blocks finished (w_router set)
   int n_eblk;                // projection blocks per row group: ceil(E / kRouterExperts)
-  uint32_t *row_cnt;         // [T] fused epilogue row counters to clear, or NULL
   int T, H, E, k, shared, words, Tmax;  // T: the step's rows, or the grid's bound when d_T is set
   const int32_t *d_T;   // device-side row count (clamped to Tmax), or NULL
   int32_t *topk_ids;
@@ -144,21 +140,24 @@ struct ExpertArgs {
   int skip_ready_tile;  // fault injection: tile index whose ready count is never published, or -1
   int fp4;              // weights are MXFP4 (E2M1) rather than MXFP8 (tensor-core kernel only)
   float swiglu_limit;   // clipped SwiGLU limit; <= 0: no clip
-  // fused residual-stream epilogue (tensor-core kernel only; n_streams == 0: off)
-  int n_streams;
+};
+
+// The residual-stream + RMSNorm + MXFP8 epilogue (residual_norm.cu), one block per token row.
+struct ResidArgs {
+  const uint16_t *y;         // bf16 [T][H], the step's output
   const uint16_t *resid_in;  // bf16 [T][S][H]
-  uint16_t *resid_out;       // bf16 [T][S][H]
+  uint16_t *resid_out;       // bf16 [T][S][H] (may equal resid_in)
   const float *mix_res, *mix_post, *mix_pre;  // [T][S][S], [T][S], [T][S] or NULL
   const uint16_t *norm_w;    // bf16 [H]
   float rms_eps;
   uint8_t *zq, *zs;          // [T][H], [T][H/32]
   uint16_t *z_bf16;          // [T][H] or NULL
-  float *u_buf;              // [Tmax][H]
-  float *ss_part;            // [Tmax][H/128]
-  uint32_t *row_cnt;         // [Tmax]
+  int T, H, S;
 };
 
 size_t route_smem_bytes(int E, int words);
+cudaError_t prepare_residual_norm(int H);
+cudaError_t launch_residual_norm(const ResidArgs &a, cudaStream_t st);
 cudaError_t prepare_route(size_t smem);
 cudaError_t prepare_experts(int H, int I);
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);

@@ -213,8 +213,6 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   const size_t o_hb = take(size_t(p->pairs_max) * I * 2), o_o = take(size_t(p->pairs_max) * H * 4);
   const size_t o_xd = take(size_t(Tm) * H * 2), o_ld = take(size_t(Tm) * E * 4), o_yd = take(size_t(Tm) * H * 2);
   const size_t o_lp = take(size_t(Tm) * E * 4), o_rg = take(size_t(p->words) * 4);
-  const size_t o_ub = take(size_t(Tm) * H * 4), o_ssp = take(size_t(Tm) * (H / kMmaDownRows) * 4);
-  const size_t o_rc = take(size_t(Tm) * 4);
   p->arena_bytes = off;
   if (cudaMalloc(&p->arena, off) != cudaSuccess) {
     cudaGetLastError();
@@ -249,15 +247,13 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   s.y_dev = base + o_yd;
   s.logits_proj = reinterpret_cast<float *>(base + o_lp);
   s.rg_cnt = reinterpret_cast<uint32_t *>(base + o_rg);
-  s.u_buf = reinterpret_cast<float *>(base + o_ub);
-  s.ss_part = reinterpret_cast<float *>(base + o_ssp);
-  s.row_cnt = reinterpret_cast<uint32_t *>(base + o_rc);
   if (cudaMemset(p->arena, 0, off) != cudaSuccess) {
     destroy_plan(p);
     return MOE_ERR_CUDA;
   }
   if (prepare_route(route_smem_bytes(E, p->words)) != cudaSuccess ||
-      (experts_shape_supported(H, I) && prepare_experts(H, I) != cudaSuccess) || prepare_experts_mma() != cudaSuccess) {
+      (experts_shape_supported(H, I) && prepare_experts(H, I) != cudaSuccess) || prepare_experts_mma() != cudaSuccess ||
+      prepare_residual_norm(H) != cudaSuccess) {
     destroy_plan(p);
     return MOE_ERR_CUDA;
   }
@@ -307,7 +303,6 @@ moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T
   ra.w_router = proj ? static_cast<const uint16_t *>(io->w_router) : nullptr;
   ra.rg_cnt = s.rg_cnt;
   ra.n_eblk = (c.num_experts + kRouterExperts - 1) / kRouterExperts;
-  ra.row_cnt = n_streams ? s.row_cnt : nullptr;
   ra.T = T;
   ra.d_T = d_T;
   ra.H = c.hidden;
@@ -383,20 +378,6 @@ moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T
   ea.skip_ready_tile = (c.flags & MOE_FLAG_TEST_SKIP_READY) ? 0 : -1;
   ea.fp4 = c.weight_format == MOE_WEIGHTS_MXFP4 ? 1 : 0;
   ea.swiglu_limit = c.swiglu_limit;
-  ea.n_streams = n_streams;
-  ea.resid_in = n_streams ? static_cast<const uint16_t *>(io->resid_in) : nullptr;
-  ea.resid_out = n_streams ? static_cast<uint16_t *>(io->resid_out) : nullptr;
-  ea.mix_res = n_streams ? io->mix_res : nullptr;
-  ea.mix_post = n_streams ? io->mix_post : nullptr;
-  ea.mix_pre = n_streams ? io->mix_pre : nullptr;
-  ea.norm_w = n_streams ? static_cast<const uint16_t *>(io->norm_weight) : nullptr;
-  ea.rms_eps = n_streams ? io->rms_eps : 0.0f;
-  ea.zq = n_streams ? io->zq : nullptr;
-  ea.zs = n_streams ? io->zs : nullptr;
-  ea.z_bf16 = n_streams ? static_cast<uint16_t *>(io->z) : nullptr;
-  ea.u_buf = s.u_buf;
-  ea.ss_part = s.ss_part;
-  ea.row_cnt = s.row_cnt;
   const bool timed = (c.flags & MOE_FLAG_TIMING) && p->timed_calls < kMaxTimedCalls;
   if (timed && cudaEventRecord(p->ev_start[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
   const cudaError_t le = mma ? launch_experts_mma(p->maps, ea, p->num_sms, ra.chunk_rows, st) : launch_experts(ea, p->num_sms, st);
@@ -404,6 +385,24 @@ moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T
   if (timed) {
     if (cudaEventRecord(p->ev_stop[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
     ++p->timed_calls;
+  }
+  if (n_streams) {  // the epilogue: one block per row, launched to overlap the expert kernel's end
+    ResidArgs na;
+    na.y = static_cast<const uint16_t *>(y);
+    na.resid_in = static_cast<const uint16_t *>(io->resid_in);
+    na.resid_out = static_cast<uint16_t *>(io->resid_out);
+    na.mix_res = io->mix_res;
+    na.mix_post = io->mix_post;
+    na.mix_pre = io->mix_pre;
+    na.norm_w = static_cast<const uint16_t *>(io->norm_weight);
+    na.rms_eps = io->rms_eps;
+    na.zq = io->zq;
+    na.zs = io->zs;
+    na.z_bf16 = static_cast<uint16_t *>(io->z);
+    na.T = T;
+    na.H = c.hidden;
+    na.S = n_streams;
+    if (launch_residual_norm(na, st) != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }

@@ -138,9 +138,80 @@ struct RouteSmem {
   int32_t tiles[kRouteThreads];
   int32_t offs[kRouteThreads];
   int32_t warp_sums[kRouteThreads / 32];
-  float part[4][kRouterExperts][32];  // router projection: [H quarter][expert][row] partial sums
+  float part[4][kRouterExperts][32];  // router projection, <= 8 rows: [H quarter][expert][row] partial sums
+  float part_mma[16][32][kRouterExperts];  // router projection, > 8 rows: [K slice][row][expert]
   int32_t last;  // this block finished phase 1 last
 };
+
+// One warp-level tensor-core product D[16x8] += A[16x16] * B[16x8]: bf16
+// operands, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Router projection for a row group of more than 8 rows (up to 32: two
+// 16-row tiles) and experts 8 eb .. 8 eb + 7, on the tensor cores.
+// Warp w takes the row tile w % 2 and the K slice w / 2: 32-column blocks
+// kb = slice, slice + 16, ... Within a 32-column block, lane (g, t) loads 8
+// contiguous columns 8t .. 8t+7 of its two rows (g, g + 8) and of expert g.
+// The two MMAs of the block take columns {8t .. 8t+3} and {8t+4 .. 8t+7} in
+// the k positions (2t, 2t+1, 2t+8, 2t+9) of A and B alike. A permutation of k
+// applied to both operands leaves the sum unchanged, and every load is one
+// 16-byte vector. The 16 slices' partial sums are then added in slice order.
+__device__ void router_block_mma(const RouteArgs &a, int T, int rg, int eb, RouteSmem &sm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int mt = warp & 1, ks = warp >> 1;
+  const int H = a.H, nkb = H / 32;
+  const int t0 = rg * (kRouteThreads / 32);
+  const int nrows = min(kRouteThreads / 32, T - t0);
+  const int ra = mt * 16 + g, rb = ra + 8;  // this lane's two rows within the group
+  const int e = eb * kRouterExperts + g;
+  const bool va = ra < nrows, vb = rb < nrows, ve = e < a.E;
+  const uint16_t *xa = a.x + int64_t(t0 + (va ? ra : 0)) * H + 8 * t4;
+  const uint16_t *xb = a.x + int64_t(t0 + (vb ? rb : 0)) * H + 8 * t4;
+  const uint16_t *wr = a.w_router + int64_t(ve ? e : 0) * H + 8 * t4;
+  float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  for (int kb = ks; kb < nkb; kb += 32) {
+    // two 32-column blocks in flight: kb and kb + 16
+    uint4 A0[2], B0[2], W0[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int k = kb + 16 * u;
+      const bool in = k < nkb;
+      A0[u] = (in && va) ? __ldg(reinterpret_cast<const uint4 *>(xa + 32 * k)) : z4;
+      B0[u] = (in && vb) ? __ldg(reinterpret_cast<const uint4 *>(xb + 32 * k)) : z4;
+      W0[u] = (in && ve) ? __ldg(reinterpret_cast<const uint4 *>(wr + 32 * k)) : z4;
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      mma_bf16_16816(d, A0[u].x, B0[u].x, A0[u].y, B0[u].y, W0[u].x, W0[u].y);
+      mma_bf16_16816(d, A0[u].z, B0[u].z, A0[u].w, B0[u].w, W0[u].z, W0[u].w);
+    }
+  }
+  // D: lane (g, t) holds rows (g, g + 8) of its tile, experts (2t, 2t + 1)
+  sm.part_mma[ks][mt * 16 + g][2 * t4] = d[0];
+  sm.part_mma[ks][mt * 16 + g][2 * t4 + 1] = d[1];
+  sm.part_mma[ks][mt * 16 + g + 8][2 * t4] = d[2];
+  sm.part_mma[ks][mt * 16 + g + 8][2 * t4 + 1] = d[3];
+  __syncthreads();
+  if (threadIdx.x < 32 * kRouterExperts) {
+    const int r = threadIdx.x / kRouterExperts, es = threadIdx.x % kRouterExperts;
+    const int e2 = eb * kRouterExperts + es;
+    if (r < nrows && e2 < a.E) {
+      float l = sm.part_mma[0][r][es];
+#pragma unroll
+      for (int s = 1; s < 16; ++s) l = __fadd_rn(l, sm.part_mma[s][r][es]);
+      const_cast<float *>(a.logits)[int64_t(t0 + r) * a.E + e2] = l;
+    }
+  }
+}
 
 // Router projection for row group rg (rows 32 rg ..) and experts 8 eb .. 8 eb + 7:
 // logits[t][e] = sum_h x[t][h] * W_r[e][h], bf16 operands, binary32 sums.
@@ -162,18 +233,29 @@ __device__ void router_block(const RouteArgs &a, int T, int rg, int eb, RouteSme
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-    for (int c = lane * 8; c < HQ; c += 256) {
-      const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(wrow + c));
-      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    // four W_r vectors in flight at a time, then their products with the rows
+    for (int c0 = lane * 8; c0 < HQ; c0 += 256 * 4) {
+      uint4 wv[4];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        if (rb + r < nrows) {
-          const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xrow + int64_t(rb + r) * H + c));
-          const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 256 * j;
+        wv[j] = c < HQ ? __ldg(reinterpret_cast<const uint4 *>(wrow + c)) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[r] = __fmaf_rn(__uint_as_float(xx[i] << 16), __uint_as_float(ww[i] << 16), acc[r]);
-            acc[r] = __fmaf_rn(__uint_as_float(xx[i] & 0xFFFF0000u), __uint_as_float(ww[i] & 0xFFFF0000u), acc[r]);
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 256 * j;
+        if (c >= HQ) break;
+        const uint32_t ww[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (rb + r < nrows) {
+            const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xrow + int64_t(rb + r) * H + c));
+            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[r] = __fmaf_rn(__uint_as_float(xx[i] << 16), __uint_as_float(ww[i] << 16), acc[r]);
+              acc[r] = __fmaf_rn(__uint_as_float(xx[i] & 0xFFFF0000u), __uint_as_float(ww[i] & 0xFFFF0000u), acc[r]);
+            }
           }
         }
       }
@@ -397,8 +479,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
   const int64_t n_comb = int64_t(T) * a.comb_per_row;
   for (int64_t i = gtid; i < a.n_tiles_max; i += gstride) a.ready[i] = 0;
   for (int64_t i = gtid; i < n_comb; i += gstride) a.comb_cnt[i] = 0;
-  if (a.row_cnt)
-    for (int64_t i = gtid; i < T; i += gstride) a.row_cnt[i] = 0;
 
   if (int(blockIdx.x) >= nrb) {  // x quantisation
     const int64_t groups = int64_t(T) * (a.H / kGroup);
@@ -424,7 +504,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
   if (proj) {
     rg = int(blockIdx.x) / a.n_eblk;
     if (rg >= R) return;  // no rows for this row group
-    router_block(a, T, rg, int(blockIdx.x) % a.n_eblk, sm);
+    // up to 8 rows: CUDA-core sums (latency-bound); more: tensor cores
+    if (T - rg * (kRouteThreads / 32) > 8) router_block_mma(a, T, rg, int(blockIdx.x) % a.n_eblk, sm);
+    else router_block(a, T, rg, int(blockIdx.x) % a.n_eblk, sm);
     // The last projection block of the row group routes its rows (ticket
     // after a fence; the counter wraps back to zero on the last ticket).
     __threadfence();

@@ -173,7 +173,6 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ra.w_router = nullptr;  // logits are an input here
   ra.rg_cnt = nullptr;
   ra.n_eblk = 1;
-  ra.row_cnt = nullptr;
   ra.T = T;
   ra.d_T = nullptr;
   ra.H = c.hidden;
@@ -249,16 +248,6 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ea.skip_ready_tile = -1;
   ea.fp4 = 0;
   ea.swiglu_limit = c.swiglu_limit;
-  ea.n_streams = 0;  // no fused epilogue on this entry point
-  ea.resid_in = nullptr;
-  ea.resid_out = nullptr;
-  ea.mix_res = ea.mix_post = ea.mix_pre = nullptr;
-  ea.norm_w = nullptr;
-  ea.rms_eps = 0.0f;
-  ea.zq = ea.zs = nullptr;
-  ea.z_bf16 = nullptr;
-  ea.u_buf = ea.ss_part = nullptr;
-  ea.row_cnt = nullptr;
   if (launch_experts(ea, d->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   return MOE_OK;

@@ -3,15 +3,20 @@
 In front, the router projection: logits = x . W_r^T (bf16 operands, binary32
 sums) in the route kernel.
 * The logits are within the binary32 summation bound of the oracle's:
-  gamma_d * sum_h |x_h w_h|, with d = H/128 + 16. That d bounds the
-  sequential roundings any product meets: the per-lane sums, the butterfly
-  and the adds over the four H quarters.
+  gamma_d * sum_h |x_h w_h|. Up to 8 rows the kernel sums on CUDA cores (per-lane
+  fused multiply-adds, a butterfly, four H quarters): at most H/128 + 8
+  roundings per product. Beyond 8 rows it uses tensor-core MMAs (m16n8k16,
+  fp32 accumulate) in 16 K slices. d = 40 * H/256 + 64 covers both paths with
+  room to spare: up to 17 accumulation steps per MMA, H/256 MMAs in a chain,
+  each step allowed two units in the last place (the tensor core may truncate
+  rather than round), plus the slice sums.
 * Routing, weights and placement are bit-exact against the oracle's top-k
   applied to the GPU's own logits. The decision is taken in the kernel's
   precision.
 * The expert ids equal the oracle's from its own logits on every row whose
   top-k margins exceed twice the bound.
-Behind, the residual-stream epilogue in the tensor-core kernel's combine.
+Behind, the residual-stream epilogue: one kernel per step, one block per row,
+launched right behind the expert kernel.
 * New streams are compared with the oracle applied to the GPU's own y:
   bit-exact with one plain stream, within one bf16 step with mixing.
 * z is within one bf16 step (at least 99 % equal).
@@ -48,7 +53,7 @@ def dev_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
 def logits_bound(x_bits, wr_bits) -> np.ndarray:
     """Largest binary32 summation error of a projection logit, per (t, e)."""
     H = x_bits.shape[1]
-    d = H // 128 + 16
+    d = 40 * max(1, H // 256) + 64
     u = 2.0 ** -24
     gam = d * u / (1 - d * u)
     ax = np.abs(oracle.bf16_bits_to_f64(x_bits))
@@ -145,6 +150,7 @@ def _epilogue_inputs(seed, T, S, H, mixed):
     (37, 1024, 16, 4, 256, 1, False, True),
     (20, 512, 8, 2, 384, 4, True, False),
     (9, 1024, 16, 3, 256, 2, True, True),
+    (3, 16384, 4, 2, 128, 2, True, False),   # 512 groups per row: two per thread
 ])
 def test_residual_norm_epilogue(T, H, E, k, I, S, mixed, in_place):
     dev = torch.device("cuda", 0)
