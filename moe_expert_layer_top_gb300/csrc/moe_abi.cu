@@ -34,7 +34,6 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
 // Pure host checks of the Guard (no device access).
 moe_status_t guard_config(const moe_config_t &c) {
