@@ -16,7 +16,7 @@ The JSON line reports:
 * cpu_baseline: the oracle timed on the host cores on a bounded sample.
 * also: the other row counts (24/96/384) as context.
 
---impl reference times the oracle instead (the CPU restatement).
+--impl reference times the oracle instead: the plain CPU restatement of the step.
 Under torchrun each rank runs an independent replica. There is no collective
 in the data path.
 """
@@ -481,8 +481,7 @@ def run_gpu(args):
 
     weights = weights_for(wl)
 
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else None)
+    clocks = ClockSampler(local, args.clocks_log)
     time.sleep(0.05)
     if world > 1:
         dist.barrier()
@@ -682,6 +681,8 @@ def main():
     ap.add_argument("--fused", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="time only the fused step (router projection + this many residual streams with "
                          "RMSNorm + MXFP8) on the workload; prints its own line")
+    ap.add_argument("--clocks-log", default=None,
+                    help="also write the raw nvidia-smi clock samples of the timed region to this CSV file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -27,7 +27,8 @@
 //
 // Warp roles (10 warps):
 //   warp 0      TMA producer: one lane loads the A tiles (128 bytes of K x 64
-//               or 128 rows per box, 128-byte swizzle) into a 10- or 11-stage ring.
+//               or 128 rows per box, 128-byte swizzle) into a 5-stage ring of
+//               two K chunks per stage.
 //   warp 1      MMA issuer: one lane issues tcgen05.mma.kind::mxf8f6f4
 //               .block_scale (4 per stage, K = 32 each) into one of two TMEM
 //               accumulators and commits each stage back to the ring.
@@ -852,10 +853,10 @@ cudaError_t launch_cfg(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaS
 }  // namespace
 
 // Chunk size. A chunk never holds more rows than the step (an expert has at
-// most T rows), so T <= 16 uses 16-row chunks and 11 stages. Larger steps use
-// 32-row chunks and 10 stages. Chunks of 64 or 128 rows (8 or 6 stages) were
-// slower on GB300 at 48 to 384 rows: the deeper ring is worth more than the
-// weight blocks that the chunks of a hot expert read again from L2.
+// most T rows), so T <= 16 uses 16-row chunks. Larger steps use 32-row chunks.
+// Chunks of 64 or 128 rows (fewer stages) were slower on GB300 at 48 to 384
+// rows: the deeper ring is worth more than the weight blocks that the chunks
+// of a hot expert read again from L2.
 int mma_chunk_rows(int T) { return T <= 16 ? 16 : 32; }
 
 cudaError_t prepare_experts_mma() {

@@ -17,7 +17,7 @@ section 2.1):
   fused with RMSNorm, with quantisation added on supported paths.
 * The small-operator bullet. Q RMSNorm is fused with MXFP8 quantisation.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * Router projection. x (bf16) times W_r (bf16, [E][H], one row per routed
   expert), with no bias and no scaling. Every product of two bf16 values is

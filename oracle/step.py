@@ -12,7 +12,7 @@ Passages followed:
     expert outputs fused with the shared-expert addition;
   - section 3.1: the SwiGLU keeps the original intermediate rounding.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * Intermediate rounding. g and u are rounded to bf16, as an unfused GEMM
   would store them. silu(g)*u is formed in fp64 and rounded to fp32, then to

@@ -45,7 +45,7 @@ def check_y(y_gpu_bits, y_ref_bits):
     return fro, mx, rms
 
 
-class GpuRun:
+class CudaStep:
     """One CUDA-path step with every tap, on seeded inputs."""
 
     def __init__(self, T, H, E, k, I, routing="uniform", shared=0, seed=42, weights=None, max_rows=None,
@@ -90,7 +90,7 @@ def oracle_experts(seed, E, H, I, cache=None, fmt="mxfp8"):
     return get
 
 
-def check_routing_bit_exact(g: GpuRun, r: dict):
+def check_routing_bit_exact(g: CudaStep, r: dict):
     np.testing.assert_array_equal(g.t["topk_ids"], r["ids"])
     np.testing.assert_array_equal(g.t["topk_w"].view(np.uint32), r["w"].view(np.uint32))
     np.testing.assert_array_equal(g.t["bitmap"].view(np.uint32), r["bitmap"])
@@ -99,12 +99,12 @@ def check_routing_bit_exact(g: GpuRun, r: dict):
     np.testing.assert_array_equal(g.t["slot"].astype(np.int64), ref_slot)
 
 
-def check_xquant_bit_exact(g: GpuRun, r: dict):
+def check_xquant_bit_exact(g: CudaStep, r: dict):
     np.testing.assert_array_equal(g.t["xq"], r["xq"])
     np.testing.assert_array_equal(g.t["xs"], r["xs"])
 
 
-def check_h_quantizer_bit_exact(g: GpuRun, pairs=None):
+def check_h_quantizer_bit_exact(g: CudaStep, pairs=None):
     """The GPU's MXFP8 h must be the oracle's quantisation of the GPU's own bf16 h."""
     hb = g.t["h_bf16"].view(np.uint16)
     if pairs is not None:
@@ -117,7 +117,7 @@ def check_h_quantizer_bit_exact(g: GpuRun, pairs=None):
     np.testing.assert_array_equal(hs, s)
 
 
-def check_h_close(g: GpuRun, r: dict, pairs):
+def check_h_close(g: CudaStep, r: dict, pairs):
     """bf16 h: equal except for rare one-ulp rounding flips."""
     hg = g.t["h_bf16"].view(np.uint16)[pairs].astype(np.int32)
     hr = r["h"][pairs].astype(np.int32)

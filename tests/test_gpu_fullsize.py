@@ -18,7 +18,7 @@ from moe_expert_layer_top_gb300 import abi, synthetic
 from moe_expert_layer_top_gb300.layer import MoEWeightsMXFP8
 
 import synth
-from gpu_cases import (GpuRun, check_h_close, check_h_quantizer_bit_exact, check_routing_bit_exact,
+from gpu_cases import (CudaStep, check_h_close, check_h_quantizer_bit_exact, check_routing_bit_exact,
                        check_xquant_bit_exact, check_y, oracle_experts, rel_fro, to_np)
 
 pytestmark = pytest.mark.gpu
@@ -53,7 +53,7 @@ FULL = [("bs1", 0), ("bs4", 0), ("bs16", 0), ("bs64", 0),
 def test_fullsize_parity(name, flags, weights):
     wl = synth.WORKLOADS[name]
     w = weights if wl.shared else routed_only(weights)
-    g = GpuRun(wl.T, wl.H, wl.E, wl.k, wl.I, wl.routing, wl.shared, seed=SEED, weights=w, flags=flags).run()
+    g = CudaStep(wl.T, wl.H, wl.E, wl.k, wl.I, wl.routing, wl.shared, seed=SEED, weights=w, flags=flags).run()
     assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     # sampled rows: the first and the last token row
     rows = [0, wl.T - 1]
@@ -99,7 +99,7 @@ def test_fullsize_mxfp4_intermediate_2304_clipped(name):
     lim = 1.0
     w = synthetic.make_weights(SEED, wl.E, wl.H, wl.I, wl.shared, torch.device("cuda", 0), "mxfp4")
     torch.cuda.synchronize()
-    g = GpuRun(wl.T, wl.H, wl.E, wl.k, wl.I, wl.routing, wl.shared, seed=SEED, weights=w, fmt="mxfp4",
+    g = CudaStep(wl.T, wl.H, wl.E, wl.k, wl.I, wl.routing, wl.shared, seed=SEED, weights=w, fmt="mxfp4",
                swiglu_limit=lim).run()
     assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     rows = [0, wl.T - 1]

@@ -17,7 +17,7 @@ import synth
 from moe_expert_layer_top_gb300 import abi, synthetic
 from moe_expert_layer_top_gb300.layer import MoEStep, quantize_mxfp4, quantize_mxfp8
 
-from gpu_cases import (GpuRun, bf16_dev_to_bits, check_h_close, check_h_quantizer_bit_exact,
+from gpu_cases import (CudaStep, bf16_dev_to_bits, check_h_close, check_h_quantizer_bit_exact,
                        check_routing_bit_exact, check_xquant_bit_exact, check_y, oracle_experts, rel_fro, to_np)
 
 pytestmark = pytest.mark.gpu
@@ -130,7 +130,7 @@ PATHS = {"gemv": abi.MOE_FLAG_PATH_GEMV, "mma": abi.MOE_FLAG_PATH_MMA}
 @pytest.mark.parametrize("case", SMALL, ids=[f"T{c[0]}_H{c[1]}_E{c[2]}_k{c[3]}_sh{c[6]}" for c in SMALL])
 def test_small_case_parity(case, path):
     T, H, E, k, I, routing, shared = case
-    g = GpuRun(T, H, E, k, I, routing, shared, seed=42 + T, flags=PATHS[path]).run()
+    g = CudaStep(T, H, E, k, I, routing, shared, seed=42 + T, flags=PATHS[path]).run()
     assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     get = oracle_experts(42 + T, E, H, I)
     sh = oracle.expert_weights_from_synth(42 + T, "shared", H, I) if shared else None
@@ -158,7 +158,7 @@ SMALL4 = [
 def test_mxfp4_weights_parity(case):
     """MXFP4 expert weights on the tensor-core kernel, against the oracle."""
     T, H, E, k, I, routing, shared, lim = case
-    g = GpuRun(T, H, E, k, I, routing, shared, seed=60 + T, fmt="mxfp4", swiglu_limit=lim).run()
+    g = CudaStep(T, H, E, k, I, routing, shared, seed=60 + T, fmt="mxfp4", swiglu_limit=lim).run()
     assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
     get = oracle_experts(60 + T, E, H, I, fmt="mxfp4")
     sh = oracle.expert_weights_from_synth(60 + T, "shared", H, I, fmt="mxfp4") if shared else None
@@ -180,7 +180,7 @@ def test_mxfp4_weights_parity(case):
 @pytest.mark.parametrize("path", list(PATHS))
 def test_clipped_swiglu_parity(path):
     T, H, E, k, I, lim = 24, 512, 8, 2, 256, 0.375
-    g = GpuRun(T, H, E, k, I, "zipf", 1, seed=71, flags=PATHS[path], swiglu_limit=lim).run()
+    g = CudaStep(T, H, E, k, I, "zipf", 1, seed=71, flags=PATHS[path], swiglu_limit=lim).run()
     assert g.status_code == abi.MOE_OK
     get = oracle_experts(71, E, H, I)
     sh = oracle.expert_weights_from_synth(71, "shared", H, I)
@@ -213,7 +213,7 @@ def test_routing_tie_break_on_device():
     lg[2] = [-1, 3, 3, -2, 3, 0, 1, 1]
     lg[3] = np.arange(8)[::-1]
     x = synth.x_bf16(3, T, H)
-    g = GpuRun(T, H, E, k, I, x_lg=(x, lg)).run()
+    g = CudaStep(T, H, E, k, I, x_lg=(x, lg)).run()
     r = oracle.moe_step(x, lg, k, oracle_experts(42, E, H, I))
     check_routing_bit_exact(g, r)
     np.testing.assert_array_equal(g.t["topk_ids"][0], [1, 2, 3])
@@ -226,12 +226,12 @@ def test_routing_tie_break_on_device():
 @pytest.mark.parametrize("path", list(PATHS))
 def test_deterministic_and_token_permutation_invariant(path):
     T, H, E, k, I = 40, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I, "zipf", flags=PATHS[path]).run()
+    g = CudaStep(T, H, E, k, I, "zipf", flags=PATHS[path]).run()
     y1 = g.y_bits.copy()
     g.run()
     np.testing.assert_array_equal(g.y_bits, y1)             # same input twice -> same bits
     perm = np.random.default_rng(5).permutation(T)
-    g2 = GpuRun(T, H, E, k, I, weights=g.weights, x_lg=(g.x_bits[perm], g.lg[perm]), flags=PATHS[path]).run()
+    g2 = CudaStep(T, H, E, k, I, weights=g.weights, x_lg=(g.x_bits[perm], g.lg[perm]), flags=PATHS[path]).run()
     # each row's arithmetic does not depend on its tile-mates
     np.testing.assert_array_equal(g2.y_bits, y1[perm])
     g.close()
@@ -240,7 +240,7 @@ def test_deterministic_and_token_permutation_invariant(path):
 
 def test_empty_step_and_argument_errors():
     T, H, E, k, I = 6, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I)
+    g = CudaStep(T, H, E, k, I)
     y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     st = torch.cuda.current_stream()
     assert abi.moe_forward(g.step.plan, g.x_dev, g.lg_dev, 0, y, None, None, st) == abi.MOE_OK
@@ -256,7 +256,7 @@ def test_empty_step_and_argument_errors():
 @pytest.mark.parametrize("path", list(PATHS))
 def test_fewer_rows_than_planned(path):
     T, H, E, k, I = 9, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I, max_rows=64, flags=PATHS[path]).run()
+    g = CudaStep(T, H, E, k, I, max_rows=64, flags=PATHS[path]).run()
     r = oracle.moe_step(g.x_bits, g.lg, k, oracle_experts(42, E, H, I))
     check_routing_bit_exact(g, r)
     check_y(g.y_bits, r["y"])
@@ -269,10 +269,10 @@ def test_bounded_wait_timeout_is_reported_and_recoverable(path):
     down units' bounded wait gives up, the step reports MOE_ERR_TIMEOUT, and the
     GPU stays usable: a normal plan afterwards matches the oracle."""
     T, H, E, k, I = 6, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I, flags=abi.MOE_FLAG_TEST_SKIP_READY | PATHS[path], timeout_ns=20_000_000).run()
+    g = CudaStep(T, H, E, k, I, flags=abi.MOE_FLAG_TEST_SKIP_READY | PATHS[path], timeout_ns=20_000_000).run()
     assert g.status_code == abi.MOE_ERR_TIMEOUT
     g.close()
-    ok = GpuRun(T, H, E, k, I).run()
+    ok = CudaStep(T, H, E, k, I).run()
     assert ok.status_code == abi.MOE_OK
     r = oracle.moe_step(ok.x_bits, ok.lg, k, oracle_experts(42, E, H, I))
     check_y(ok.y_bits, r["y"])
@@ -281,7 +281,7 @@ def test_bounded_wait_timeout_is_reported_and_recoverable(path):
 
 def test_forward_host_matches_device_forward():
     T, H, E, k, I = 6, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I).run()
+    g = CudaStep(T, H, E, k, I).run()
     xh = torch.from_numpy(g.x_bits.view(np.int16).copy()).pin_memory()
     lh = torch.from_numpy(g.lg.copy()).pin_memory()
     yh = torch.empty((T, H), dtype=torch.int16).pin_memory()
@@ -302,9 +302,9 @@ def test_default_path_is_the_tensor_core_kernel():
     pinned MMA kernel's, bit for bit, and matches the oracle."""
     H, E, k, I = 512, 8, 2, 256
     for T in (6, 40):
-        g = GpuRun(T, H, E, k, I, "zipf", seed=5).run()
+        g = CudaStep(T, H, E, k, I, "zipf", seed=5).run()
         assert g.status_code == abi.MOE_OK
-        pinned = GpuRun(T, H, E, k, I, "zipf", seed=5, weights=g.weights, flags=abi.MOE_FLAG_PATH_MMA).run()
+        pinned = CudaStep(T, H, E, k, I, "zipf", seed=5, weights=g.weights, flags=abi.MOE_FLAG_PATH_MMA).run()
         np.testing.assert_array_equal(g.y_bits, pinned.y_bits)
         r = oracle.moe_step(g.x_bits, g.lg, k, oracle_experts(5, E, H, I))
         check_y(g.y_bits, r["y"])
@@ -314,7 +314,7 @@ def test_default_path_is_the_tensor_core_kernel():
 
 def test_timing_flag_records_expert_kernel():
     T, H, E, k, I = 6, 512, 8, 2, 256
-    g = GpuRun(T, H, E, k, I, flags=abi.MOE_FLAG_TIMING)
+    g = CudaStep(T, H, E, k, I, flags=abi.MOE_FLAG_TIMING)
     for _ in range(3):
         g.run()
     ms, n = g.step.kernel_times()

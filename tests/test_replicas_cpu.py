@@ -1,4 +1,4 @@
-"""The multi-GPU path of this build is "replicas only": every rank runs its
+"""The multi-GPU path is "replicas only": every rank runs its
 own step on its own GPU, with no data-path collective. bench.py takes the max
 per-step time over ranks, and rank 0 alone prints the line. These tests run
 that logic on CPU with world_size 2 over gloo, and check that the reference
