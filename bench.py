@@ -64,7 +64,55 @@ def _oracle_prepare(seed, wl_name, rows, pool):
     return x_bits, lg, experts, jobs
 
 
-def oracle_baseline(seed: int, wl_name: str, steps: int, warmup: int, result_q):
+_ROW_CACHE = {}
+
+
+def _oracle_row(args):
+    """One token row of the step through the oracle, in a worker process. The
+    worker draws the experts its row needs once (first call) and keeps them."""
+    seed, wl_name, t = args
+    import oracle
+    import synth
+    wl = synth.WORKLOADS[wl_name]
+    c = _ROW_CACHE.get((seed, wl_name))
+    if c is None:
+        c = {"x": synth.x_bf16(seed, wl.T, wl.H), "lg": synth.router_logits(seed, wl.T, wl.E, wl.k, wl.routing),
+             "w": {}, "sh": None}
+        if wl.shared:
+            c["sh"] = oracle.expert_weights_from_synth(seed, "shared", wl.H, wl.I, fmt=wl.fmt)
+        _ROW_CACHE[(seed, wl_name)] = c
+    for e in oracle.topk_ids(c["lg"][t:t + 1], wl.k)[0]:
+        if int(e) not in c["w"]:
+            c["w"][int(e)] = oracle.expert_weights_from_synth(seed, int(e), wl.H, wl.I, fmt=wl.fmt)
+    r = oracle.moe_step(c["x"], c["lg"], wl.k, c["w"], shared=c["sh"], rows=[t], swiglu_limit=wl.swiglu_limit)
+    return t, r["y"][t]
+
+
+def oracle_all_cores(seed: int, wl_name: str, steps: int, check_rows: dict):
+    """The oracle over every token row of the step at once, one spawned process
+    per row (up to the host's cores): the wall time of a whole step. The rows
+    must equal the single-thread run's (check_rows: row -> y bits)."""
+    import numpy as np
+    import synth
+    wl = synth.WORKLOADS[wl_name]
+    n = max(1, min(wl.T, os.cpu_count() or 1))
+    ctx = mp.get_context("spawn")
+    jobs = [(seed, wl_name, t) for t in range(wl.T)]
+    with ctx.Pool(n) as pool:
+        first = dict(pool.map(_oracle_row, jobs, chunksize=1))  # draws the weights (untimed)
+        times = []
+        for _ in range(steps):
+            t0 = time.perf_counter()
+            got = dict(pool.map(_oracle_row, jobs, chunksize=1))
+            times.append(time.perf_counter() - t0)
+    for t, y in check_rows.items():
+        if not np.array_equal(first[t], y) or not np.array_equal(got[t], y):
+            raise RuntimeError(f"all-cores oracle row {t} differs from the single-thread run")
+    return {"us_per_step": statistics.median(times) * 1e6, "cores": n, "steps": steps}
+
+
+def oracle_baseline(seed: int, wl_name: str, steps: int, warmup: int, result_q, gpu_done=None,
+                    with_all_cores=True):
     """Runs in a spawned process: times the oracle on a bounded sample of the workload."""
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     import oracle
@@ -79,12 +127,22 @@ def oracle_baseline(seed: int, wl_name: str, steps: int, warmup: int, result_q):
     times = []
     for i in range(warmup + steps):
         t0 = time.perf_counter()
-        oracle.moe_step(x_bits, lg, wl.k, got, shared=shared, rows=rows, swiglu_limit=wl.swiglu_limit)
+        r = oracle.moe_step(x_bits, lg, wl.k, got, shared=shared, rows=rows, swiglu_limit=wl.swiglu_limit)
         dt = time.perf_counter() - t0
         if i >= warmup:
             times.append(dt)
     per_sample = statistics.median(times)
     scale = wl.T / len(rows)
+    all_cores = None
+    # every row at once, one process per row: the whole step's wall time. It
+    # uses many host cores, so it waits until the GPU timing is over.
+    if gpu_done is not None:
+        gpu_done.wait(timeout=600)
+    if with_all_cores and wl.T <= 64:
+        try:
+            all_cores = oracle_all_cores(seed, wl_name, 3, {t: r["y"][t] for t in rows})
+        except Exception as exc:  # reported, not fatal: the single-thread baseline stands
+            all_cores = {"error": str(exc)[:200]}
     result_q.put({
         "us_per_step": per_sample * scale * 1e6,
         "sample_s": per_sample,
@@ -93,6 +151,7 @@ def oracle_baseline(seed: int, wl_name: str, steps: int, warmup: int, result_q):
         "scale": scale,
         "steps": steps,
         "cores": 1,
+        "all_cores": all_cores,
     })
 
 
@@ -458,7 +517,8 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ctx = mp.get_context("spawn")
         cpu_q = ctx.Queue()
-        cpu_proc = ctx.Process(target=oracle_baseline, args=(seed, args.workload, 3, 1, cpu_q))
+        gpu_done = ctx.Event()
+        cpu_proc = ctx.Process(target=oracle_baseline, args=(seed, args.workload, 3, 1, cpu_q, gpu_done))
         cpu_proc.start()
 
     _build.build()
@@ -564,6 +624,7 @@ def run_gpu(args):
 
     cpu = None
     if cpu_q is not None:
+        gpu_done.set()  # the GPU timing is over: the oracle may use every host core now
         cpu = cpu_q.get(timeout=900)
         cpu_proc.join(timeout=60)
 
@@ -629,6 +690,15 @@ def run_gpu(args):
             "sample": f"{cpu['rows']} of {wl.T} token rows ({cpu['experts']} expert MLPs), median of "
                       f"{cpu['steps']} runs of {cpu['sample_s']:.2f} s, scaled x{cpu['scale']:.0f} to a step",
         }
+        ac = cpu.get("all_cores")
+        if ac and "us_per_step" in ac:
+            line["cpu_baseline_all_cores"] = {
+                "value": round(ac["us_per_step"], 1), "unit": "us/step", "cores": ac["cores"], "kind": "oracle",
+                "sample": f"all {wl.T} token rows of the step at once, one spawned process per row (the oracle "
+                          f"unchanged), wall time, median of {ac['steps']}; rows equal the single-thread run's",
+            }
+        elif ac:
+            line["cpu_baseline_all_cores"] = ac
     if also:
         line["also"] = also
     main["step"].close()
@@ -647,7 +717,7 @@ def run_reference(args):
     wl = synth.WORKLOADS[args.workload]
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    p = ctx.Process(target=oracle_baseline, args=(synth.BASE_SEED, wl.name, args.steps, args.warmup, q))
+    p = ctx.Process(target=oracle_baseline, args=(synth.BASE_SEED, wl.name, args.steps, args.warmup, q, None, False))
     p.start()
     r = q.get(timeout=3600)
     p.join(timeout=60)
