@@ -456,6 +456,24 @@ def time_l2_warm_graph(step, x, lg, wl, steps):
                    "back with no L2 flush"}
 
 
+def input_checksums(wl, weights, seed):
+    """Fingerprints of the step's synthetic inputs, so a run can be matched to
+    its inputs: sha256 of the token rows' and logits' bytes (host), and the
+    wrapping sum of each weight tensor's 64-bit words (device)."""
+    import hashlib
+    import synth
+    x = synth.x_bf16(seed, wl.T, wl.H)
+    lg = synth.router_logits(seed, wl.T, wl.E, wl.k, wl.routing)
+    out = {"x_sha256": hashlib.sha256(x.tobytes()).hexdigest()[:16],
+           "logits_sha256": hashlib.sha256(lg.tobytes()).hexdigest()[:16]}
+    import torch
+    for name in ("w_gate", "s_gate", "w_up", "s_up", "w_down", "s_down"):
+        t = getattr(weights, name)
+        n = t.numel() // 8 * 8
+        out[name + "_sum64"] = int(t.reshape(-1)[:n].view(torch.int64).sum().item()) & ((1 << 64) - 1)
+    return out
+
+
 def time_e2e(step, wl, seed, steps, warmup):
     """moe_forward_host: pinned host x/logits in, host y out, copies inside the timed region."""
     import numpy as np
@@ -502,7 +520,7 @@ def run_gpu(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    seed = synth.BASE_SEED
+    seed = args.seed
     wl = synth.WORKLOADS[args.workload]
     if args.experts:
         import dataclasses
@@ -659,6 +677,8 @@ def run_gpu(args):
             "parallelism": "replicas" if world > 1 else "single GPU",
             "status": main["status"],
             "steps_with_device_error": main["bad_steps"],
+            "seed": seed,
+            "inputs": input_checksums(wl, weights, seed),
         },
         "roofline": {
             "bound": "hbm",
@@ -717,7 +737,7 @@ def run_reference(args):
     wl = synth.WORKLOADS[args.workload]
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    p = ctx.Process(target=oracle_baseline, args=(synth.BASE_SEED, wl.name, args.steps, args.warmup, q, None, False))
+    p = ctx.Process(target=oracle_baseline, args=(args.seed, wl.name, args.steps, args.warmup, q, None, False))
     p.start()
     r = q.get(timeout=3600)
     p.join(timeout=60)
@@ -751,6 +771,7 @@ def main():
     ap.add_argument("--fused", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="time only the fused step (router projection + this many residual streams with "
                          "RMSNorm + MXFP8) on the workload; prints its own line")
+    ap.add_argument("--seed", type=int, default=42, help="seed of every synthetic input (default 42)")
     ap.add_argument("--clocks-log", default=None,
                     help="also write the raw nvidia-smi clock samples of the timed region to this CSV file")
     ap.add_argument("--no-cpu-baseline", action="store_true")

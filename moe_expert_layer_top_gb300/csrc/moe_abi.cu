@@ -21,6 +21,8 @@
 
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 #include "moe.h"
 
@@ -282,6 +284,13 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
 
 namespace {
 
+// A named NVTX range over one entry-point call (no cost unless a profiler is
+// attached): profilers can pick out each step's launches by it.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 // Enqueues one step: the route kernel, then an expert kernel with PDL.
 // T sizes the grids. With d_T set, the kernels read the step's row count
 // from device memory (clamped to max_rows) and the tensor-core kernel runs.
@@ -412,6 +421,7 @@ extern "C" {
 
 moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t T, void *y,
                          const moe_taps_t *taps, int32_t *d_status, void *cuda_stream) {
+  const NvtxRange nvtx_range("moe_forward");
   Plan *p = static_cast<Plan *>(plan);
   if (!p) return MOE_ERR_INVALID_ARG;
   if (T < 0 || T > p->cfg.max_rows) return MOE_ERR_INVALID_ARG;
@@ -429,6 +439,7 @@ moe_status_t moe_forward(void *plan, const void *x, const float *logits, int32_t
 
 moe_status_t moe_forward_dev(void *plan, const void *x, const float *logits, const int32_t *d_T, void *y,
                              int32_t *d_status, void *cuda_stream) {
+  const NvtxRange nvtx_range("moe_forward_dev");
   Plan *p = static_cast<Plan *>(plan);
   if (!p || !d_T || (reinterpret_cast<uintptr_t>(d_T) & 3u)) return MOE_ERR_INVALID_ARG;
   if (p->cfg.flags & MOE_FLAG_PATH_GEMV) return MOE_ERR_UNSUPPORTED;
@@ -442,6 +453,7 @@ moe_status_t moe_forward_dev(void *plan, const void *x, const float *logits, con
 
 moe_status_t moe_forward_fused(void *plan, const void *x, int32_t T, const moe_fused_io_t *io, void *y,
                                const moe_taps_t *taps, int32_t *d_status, void *cuda_stream) {
+  const NvtxRange nvtx_range("moe_forward_fused");
   Plan *p = static_cast<Plan *>(plan);
   if (!p || !io) return MOE_ERR_INVALID_ARG;
   if (T < 0 || T > p->cfg.max_rows) return MOE_ERR_INVALID_ARG;
@@ -475,6 +487,7 @@ moe_status_t moe_forward_fused(void *plan, const void *x, int32_t T, const moe_f
 
 moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logits_host, int32_t T, void *y_host,
                               void *cuda_stream) {
+  const NvtxRange nvtx_range("moe_forward_host");
   Plan *p = static_cast<Plan *>(plan);
   if (!p) return MOE_ERR_INVALID_ARG;
   if (T < 0 || T > p->cfg.max_rows) return MOE_ERR_INVALID_ARG;
