@@ -64,51 +64,65 @@ def _oracle_prepare(seed, wl_name, rows, pool):
     return x_bits, lg, experts, jobs
 
 
-_ROW_CACHE = {}
-
-
-def _oracle_row(args):
-    """One token row of the step through the oracle, in a worker process. The
-    worker draws the experts its row needs once (first call) and keeps them."""
-    seed, wl_name, t = args
+def _oracle_row_server(conn, seed: int, wl_name: str, t: int):
+    """One token row of the step through the oracle, in its own process: draws
+    the experts the row needs once, then computes the row on every request."""
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
     import oracle
     import synth
     wl = synth.WORKLOADS[wl_name]
-    c = _ROW_CACHE.get((seed, wl_name))
-    if c is None:
-        c = {"x": synth.x_bf16(seed, wl.T, wl.H), "lg": synth.router_logits(seed, wl.T, wl.E, wl.k, wl.routing),
-             "w": {}, "sh": None}
-        if wl.shared:
-            c["sh"] = oracle.expert_weights_from_synth(seed, "shared", wl.H, wl.I, fmt=wl.fmt)
-        _ROW_CACHE[(seed, wl_name)] = c
-    for e in oracle.topk_ids(c["lg"][t:t + 1], wl.k)[0]:
-        if int(e) not in c["w"]:
-            c["w"][int(e)] = oracle.expert_weights_from_synth(seed, int(e), wl.H, wl.I, fmt=wl.fmt)
-    r = oracle.moe_step(c["x"], c["lg"], wl.k, c["w"], shared=c["sh"], rows=[t], swiglu_limit=wl.swiglu_limit)
-    return t, r["y"][t]
+    x = synth.x_bf16(seed, wl.T, wl.H)
+    lg = synth.router_logits(seed, wl.T, wl.E, wl.k, wl.routing)
+    w = {int(e): oracle.expert_weights_from_synth(seed, int(e), wl.H, wl.I, fmt=wl.fmt)
+         for e in oracle.topk_ids(lg[t:t + 1], wl.k)[0]}
+    sh = oracle.expert_weights_from_synth(seed, "shared", wl.H, wl.I, fmt=wl.fmt) if wl.shared else None
+    conn.send("ready")
+    while conn.recv() is not None:
+        r = oracle.moe_step(x, lg, wl.k, w, shared=sh, rows=[t], swiglu_limit=wl.swiglu_limit)
+        conn.send(r["y"][t])
 
 
 def oracle_all_cores(seed: int, wl_name: str, steps: int, check_rows: dict):
-    """The oracle over every token row of the step at once, one spawned process
-    per row (up to the host's cores): the wall time of a whole step. The rows
-    must equal the single-thread run's (check_rows: row -> y bits)."""
+    """The oracle over every token row of the step at once, one persistent
+    spawned process per row: the wall time of a whole step. The rows must
+    equal the single-thread run's (check_rows: row -> y bits)."""
     import numpy as np
     import synth
     wl = synth.WORKLOADS[wl_name]
-    n = max(1, min(wl.T, os.cpu_count() or 1))
+    if wl.T > (os.cpu_count() or 1):
+        raise RuntimeError("more token rows than host cores")
     ctx = mp.get_context("spawn")
-    jobs = [(seed, wl_name, t) for t in range(wl.T)]
-    with ctx.Pool(n) as pool:
-        first = dict(pool.map(_oracle_row, jobs, chunksize=1))  # draws the weights (untimed)
-        times = []
+    conns, procs = [], []
+    try:
+        for t in range(wl.T):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_row_server, args=(b, seed, wl_name, t), daemon=True)
+            p.start()
+            conns.append(a)
+            procs.append(p)
+        for c in conns:
+            if c.recv() != "ready":
+                raise RuntimeError("row process failed")
+        times, got = [], {}
         for _ in range(steps):
             t0 = time.perf_counter()
-            got = dict(pool.map(_oracle_row, jobs, chunksize=1))
+            for c in conns:
+                c.send(1)
+            got = {t: c.recv() for t, c in enumerate(conns)}
             times.append(time.perf_counter() - t0)
+    finally:
+        for c in conns:
+            try:
+                c.send(None)
+            except (BrokenPipeError, OSError):
+                pass
+        for p in procs:
+            p.join(timeout=30)
     for t, y in check_rows.items():
-        if not np.array_equal(first[t], y) or not np.array_equal(got[t], y):
+        if not np.array_equal(got[t], y):
             raise RuntimeError(f"all-cores oracle row {t} differs from the single-thread run")
-    return {"us_per_step": statistics.median(times) * 1e6, "cores": n, "steps": steps}
+    return {"us_per_step": statistics.median(times) * 1e6, "cores": wl.T, "steps": steps}
 
 
 def oracle_baseline(seed: int, wl_name: str, steps: int, warmup: int, result_q, gpu_done=None,
@@ -714,8 +728,9 @@ def run_gpu(args):
         if ac and "us_per_step" in ac:
             line["cpu_baseline_all_cores"] = {
                 "value": round(ac["us_per_step"], 1), "unit": "us/step", "cores": ac["cores"], "kind": "oracle",
-                "sample": f"all {wl.T} token rows of the step at once, one spawned process per row (the oracle "
-                          f"unchanged), wall time, median of {ac['steps']}; rows equal the single-thread run's",
+                "sample": f"all {wl.T} token rows of the step at once, one persistent spawned process per row "
+                          f"(the oracle unchanged, one BLAS thread each), wall time, median of {ac['steps']}; "
+                          f"rows equal the single-thread run's",
             }
         elif ac:
             line["cpu_baseline_all_cores"] = ac
