@@ -854,7 +854,6 @@ cudaError_t launch_shape(const ExpertArgs &a, int grid, cudaStream_t st) {
 
 }  // namespace
 
-size_t experts_smem_bytes() { return sizeof(ExpertSmem); }
 
 int experts_down_blocks(int H, int I) {
   if (H == 4096 && I == 2048) return Shape<4096, 2048>::NBD;

@@ -38,7 +38,7 @@ struct Scratch {
   int32_t *n_chunks;    // [1]
   uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile (per chunk on the tensor-core path)
   uint32_t *comb_cnt;   // [Tmax][down blocks] down blocks of a token row finished (fused combine)
-  uint32_t *work;       // [4] unit counter, abort flag, route-kernel ticket
+  uint32_t *work;       // [4] (unused), abort flag, route-kernel ticket, (unused)
   int32_t *status;      // [1] plan-owned status word
   int64_t *diag;        // [8] first device-side error of the last step (site, unit, tile, ...)
   uint8_t *xq, *xs;     // [Tmax][H], [Tmax][H/32]
@@ -167,7 +167,6 @@ cudaError_t launch_experts(const ExpertArgs &a, int grid, cudaStream_t st);
 int experts_down_blocks(int H, int I);  // H / DB: down units per tile
 bool experts_shape_supported(int H, int I);
 moe_status_t guard_host(const moe_config_t &c, const moe_weights_t &w);
-size_t experts_smem_bytes();
 // Tensor-core expert kernel (tcgen05 block-scaled MXFP8 MMA).
 bool experts_mma_shape_supported(int H, int I);
 bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *maps);
