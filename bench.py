@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 
 DEFAULT_WORKLOAD = "bs1"
 SAMPLE_ROWS = 2        # oracle sample: this many token rows of the step, with every expert they touch
+LAYER_COPIES = 4       # copies of the layer's weights the timed steps cycle through (no L2 flush)
 ORACLE_WORKERS = 8     # spawn workers that prepare the oracle's weights (not timed)
 
 
@@ -282,35 +283,47 @@ def active_experts(lg, k, shared):
     return len(set(ids.ravel().tolist())) + (1 if shared else 0)
 
 
-def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed, flags=0):
-    """Times `steps` steps (L2 flushed before each, outside the events), then,
-    in a second pass with the plan's kernel timing on, the expert kernel alone.
-    Kernel timing records events between the two launches, which would break
-    their programmatic-dependent-launch overlap, so the step times come from a
-    plan without it."""
+def flush(buf):
+    """Evict L2 before a step by writing a buffer of twice its size (buf None: no flush)."""
+    if buf is not None:
+        buf.zero_()
+
+
+def time_gpu_workload(wl, weight_sets, steps, warmup, flush_buf, seed, flags=0):
+    """Times `steps` steps, then, in a second pass with the plans' kernel timing
+    on, the expert kernel alone. Kernel timing records events between the two
+    launches, which would break their programmatic-dependent-launch overlap,
+    so the step times come from plans without it.
+    weight_sets: one or more copies of the layer's weights at different
+    addresses, one plan each; steps alternate between them. With no flush this
+    is a stack of identical layers: every step streams weights that the
+    previous step did not touch, while the kernels' code and the small inputs
+    stay in L2. flush_buf (or None) evicts L2 before every step instead."""
     import torch
     from moe_expert_layer_top_gb300 import abi, synthetic
     from moe_expert_layer_top_gb300.layer import MoEStep, MoEWeightsMXFP8
-    w = weights if wl.shared else MoEWeightsMXFP8(weights.w_gate, weights.s_gate, weights.w_up, weights.s_up,
-                                                  weights.w_down, weights.s_down)
+
+    def routed(w):
+        return w if wl.shared else MoEWeightsMXFP8(w.w_gate, w.s_gate, w.w_up, w.s_up, w.w_down, w.s_down)
+    ws = [routed(w) for w in weight_sets]
     x, lg, _, lg_np = synthetic.make_inputs(seed, wl.T, wl.H, wl.E, wl.k, wl.routing)
     wfmt = abi.MOE_WEIGHTS_MXFP4 if wl.fmt == "mxfp4" else abi.MOE_WEIGHTS_MXFP8
-    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=flags, weight_format=wfmt,
-                   swiglu_limit=wl.swiglu_limit)
+    steps_ = [MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=flags, weight_format=wfmt,
+                      swiglu_limit=wl.swiglu_limit) for w in ws]
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     # one device status word per step: every step must finish with MOE_OK
     st_words = torch.full((warmup + steps,), -1, dtype=torch.int32, device="cuda")
     for i in range(warmup):
-        flush_buf.zero_()
-        step.forward(x, lg, y=y, d_status=st_words[i:i + 1])
+        flush(flush_buf)
+        steps_[i % len(steps_)].forward(x, lg, y=y, d_status=st_words[i:i + 1])
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
-        flush_buf.zero_()
+        flush(flush_buf)
         starts[i].record(stream)
-        step.forward(x, lg, y=y, d_status=st_words[warmup + i:warmup + i + 1])
+        steps_[(warmup + i) % len(steps_)].forward(x, lg, y=y, d_status=st_words[warmup + i:warmup + i + 1])
         ends[i].record(stream)
     torch.cuda.synchronize()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -319,20 +332,27 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed, flags=0):
     status = 0 if not bad else bad[0][1]
     if bad:
         print(f"warning: {len(bad)} of {len(words)} steps reported a device status: first {bad[0]}, "
-              f"diagnostics {step.diagnostics()}", file=sys.stderr)
+              f"diagnostics {steps_[0].diagnostics()}", file=sys.stderr)
     # second pass: the expert kernel's own duration (CUDA events on the launch stream)
-    kstep = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING | flags,
-                    weight_format=wfmt, swiglu_limit=wl.swiglu_limit)
-    for _ in range(max(3, warmup // 2)):
-        flush_buf.zero_()
-        kstep.forward(x, lg, y=y)
+    ksteps = [MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, flags=abi.MOE_FLAG_TIMING | flags,
+                      weight_format=wfmt, swiglu_limit=wl.swiglu_limit) for w in ws]
+    for i in range(max(3, warmup // 2)):
+        flush(flush_buf)
+        ksteps[i % len(ksteps)].forward(x, lg, y=y)
     torch.cuda.synchronize()
-    kstep.kernel_times()
-    for _ in range(steps):
-        flush_buf.zero_()
-        kstep.forward(x, lg, y=y)
-    expert_ms, launches = kstep.kernel_times()
-    kstep.close()
+    for k in ksteps:
+        k.kernel_times()
+    for i in range(steps):
+        flush(flush_buf)
+        ksteps[i % len(ksteps)].forward(x, lg, y=y)
+    expert_ms, launches = 0.0, 0
+    for k in ksteps:
+        m_, n_ = k.kernel_times()
+        expert_ms += m_
+        launches += n_
+        k.close()
+    for s_ in steps_[1:]:
+        s_.close()
     A = active_experts(lg_np, wl.k, wl.shared)
     weight_bytes = A * wl.expert_bytes
     step_bytes = weight_bytes + wl.T * wl.H * 2 + wl.T * wl.E * 4 + wl.T * wl.H * 2
@@ -349,14 +369,14 @@ def time_gpu_workload(wl, weights, steps, warmup, flush_buf, seed, flags=0):
         "step_bytes": step_bytes,
         "status": status,
         "bad_steps": len(bad),
-        "step": step,
+        "step": steps_[0],
         "x": x,
         "lg": lg,
     }
     return res
 
 
-def time_fused_workload(wl, weights, steps, warmup, flush_buf, seed, n_streams):
+def time_fused_workload(wl, weight_sets, steps, warmup, flush_buf, seed, n_streams):
     """Times moe_forward_fused three ways on the same routing. Buffers are
     allocated once.
     * "full": the router projection from a bf16 W_r [E][H] in front, and
@@ -370,10 +390,14 @@ def time_fused_workload(wl, weights, steps, warmup, flush_buf, seed, n_streams):
     import synth
     from moe_expert_layer_top_gb300 import abi
     from moe_expert_layer_top_gb300.layer import MoEStep, MoEWeightsMXFP8
-    w = weights if wl.shared else MoEWeightsMXFP8(weights.w_gate, weights.s_gate, weights.w_up, weights.s_up,
-                                                  weights.w_down, weights.s_down)
     wfmt = abi.MOE_WEIGHTS_MXFP4 if wl.fmt == "mxfp4" else abi.MOE_WEIGHTS_MXFP8
-    step = MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, weight_format=wfmt, swiglu_limit=wl.swiglu_limit)
+    plans = []
+    for weights in weight_sets:  # steps alternate between the copies, as in time_gpu_workload
+        w = weights if wl.shared else MoEWeightsMXFP8(weights.w_gate, weights.s_gate, weights.w_up, weights.s_up,
+                                                      weights.w_down, weights.s_down)
+        plans.append(MoEStep(wl.H, wl.I, wl.E, wl.k, w, wl.T, wl.shared, weight_format=wfmt,
+                             swiglu_limit=wl.swiglu_limit))
+    step = plans[0]
     bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16).copy()).view(torch.bfloat16).cuda()
     T, H, S = wl.T, wl.H, n_streams
     x = bf(synth.x_bf16(seed, T, H))
@@ -406,22 +430,24 @@ def time_fused_workload(wl, weights, steps, warmup, flush_buf, seed, n_streams):
     for name, io in ios.items():
         st_words = torch.full((warmup + steps,), -1, dtype=torch.int32, device="cuda")
         for i in range(warmup):
-            flush_buf.zero_()
-            abi.check("moe_forward_fused", abi.moe_forward_fused(step.plan, x, T, io, y, None, st_words[i:i + 1],
-                                                                 stream))
+            flush(flush_buf)
+            abi.check("moe_forward_fused", abi.moe_forward_fused(plans[i % len(plans)].plan, x, T, io, y, None,
+                                                                 st_words[i:i + 1], stream))
         torch.cuda.synchronize()
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         for i in range(steps):
-            flush_buf.zero_()
+            flush(flush_buf)
             starts[i].record(stream)
-            abi.moe_forward_fused(step.plan, x, T, io, y, None, st_words[warmup + i:warmup + i + 1], stream)
+            abi.moe_forward_fused(plans[(warmup + i) % len(plans)].plan, x, T, io, y, None,
+                                  st_words[warmup + i:warmup + i + 1], stream)
             ends[i].record(stream)
         torch.cuda.synchronize()
         per_step = [a.elapsed_time(b) for a, b in zip(starts, ends)]
         bad += [v for v in st_words.cpu().tolist() if v != abi.MOE_OK]
         out[name] = {"ms_mean": sum(per_step) / len(per_step), "ms_median": statistics.median(per_step)}
-    step.close()
+    for p_ in plans:
+        p_.close()
     out["ms_mean"], out["ms_median"] = out["full"]["ms_mean"], out["full"]["ms_median"]
     out["status"] = bad[0] if bad else 0
     return out
@@ -573,14 +599,39 @@ def run_gpu(args):
 
     weights = weights_for(wl)
 
+    _wcopies = {}
+
+    def weight_sets_for(w_l):
+        """LAYER_COPIES copies of a layer's weights at different addresses (see
+        time_gpu_workload). Four: the copies' scale bytes, which the kernel reads
+        at normal L2 priority, then exceed the L2 together (at bs1 about 4 x 35 MB)."""
+        key = (w_l.fmt, w_l.E, w_l.H, w_l.I)
+        if key not in _wcopies:
+            from moe_expert_layer_top_gb300.layer import MoEWeightsMXFP8
+            w0 = weights_for(w_l)
+            sets = [w0]
+            for _ in range(LAYER_COPIES - 1):
+                sets.append(MoEWeightsMXFP8(*[None if getattr(w0, f) is None else getattr(w0, f).clone()
+                                              for f in MoEWeightsMXFP8.__dataclass_fields__]))
+            torch.cuda.synchronize()
+            _wcopies[key] = sets
+        return _wcopies[key]
+
     clocks = ClockSampler(local, args.clocks_log)
     time.sleep(0.05)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     flags = PATH_FLAGS[args.path]
+    # L2 between timed steps. "inputs" (default): no flush; every step streams its active
+    # weights (about 9x the L2 at bs1) from HBM, and the kernels' code and the step's
+    # small inputs stay in L2, as they would across a model's layers. "flush": L2 is
+    # evicted before every step (outside the timed events). The other policy is also
+    # timed on the main workload and reported beside the value.
+    main_flush = flush_buf if args.l2 == "flush" else None
+    other_flush = None if args.l2 == "flush" else flush_buf
     if args.fused:
-        r = time_fused_workload(wl, weights, args.steps, args.warmup, flush_buf, seed, args.fused)
+        r = time_fused_workload(wl, weight_sets_for(wl), args.steps, args.warmup, main_flush, seed, args.fused)
         clocks.stop()
         if rank == 0:
             print(json.dumps({"metric": "fused MoE step us (router projection + residual streams + RMSNorm + MXFP8)",
@@ -593,7 +644,7 @@ def run_gpu(args):
         if world > 1:
             dist.destroy_process_group()
         return
-    main = time_gpu_workload(wl, weights, args.steps, args.warmup, flush_buf, seed, flags)
+    main = time_gpu_workload(wl, weight_sets_for(wl), args.steps, args.warmup, main_flush, seed, flags)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -601,6 +652,9 @@ def run_gpu(args):
 
     ms, exp_ms = max_over_ranks([main["ms_mean"], main["expert_ms_mean"]], world, "cuda")
 
+    other = time_gpu_workload(wl, weight_sets_for(wl), max(args.steps // 2, 5), max(args.warmup, 3), other_flush,
+                              seed, flags)
+    other["step"].close()
     e2e = None if args.no_e2e else time_e2e(main["step"], wl, seed, max(args.steps, 10), 3)
     l2_warm = None
     if kernel_path(args.path, wl.T) == "mma" and world == 1:
@@ -616,7 +670,7 @@ def run_gpu(args):
             if name == wl.name:
                 continue
             o = synth.WORKLOADS[name]
-            r = time_gpu_workload(o, weights_for(o), max(args.steps // 2, 5), max(args.warmup, 3), flush_buf, seed,
+            r = time_gpu_workload(o, weight_sets_for(o), max(args.steps // 2, 5), max(args.warmup, 3), main_flush, seed,
                                   flags)
             peak, _ = measured_peaks()
             also[name] = {"T": o.T, "I": o.I, "weights": o.fmt, "swiglu_limit": o.swiglu_limit,
@@ -635,7 +689,7 @@ def run_gpu(args):
         if flags != PATH_FLAGS["gemv"]:
             for base, S in (("bs1", 1), ("bs64", 4)):
                 o = synth.WORKLOADS[base]
-                r = time_fused_workload(o, weights_for(o), max(args.steps // 2, 5), max(args.warmup, 3), flush_buf,
+                r = time_fused_workload(o, weight_sets_for(o), max(args.steps // 2, 5), max(args.warmup, 3), main_flush,
                                         seed, S)
                 us = {n: r[n]["ms_mean"] * 1e3 for n in ("full", "projection", "plain")}
                 also[f"{base}_fused_s{S}"] = {
@@ -687,7 +741,16 @@ def run_gpu(args):
             "us_median": round(main["ms_median"] * 1e3, 3),
             "us_min": round(main["ms_min"] * 1e3, 3),
             "us_max": round(main["ms_max"] * 1e3, 3),
-            "l2": "flushed before every step (memset of a buffer >= 2x L2, outside the timed events)",
+            "l2": ("flushed before every step (memset of a buffer >= 2x L2, outside the timed events)"
+                   if args.l2 == "flush" else
+                   f"inputs larger than L2: no flush; steps cycle through {LAYER_COPIES} copies of the layer's "
+                   f"weights (a stack of identical layers), so every step streams "
+                   f"{main['weight_bytes'] / 1e6:.0f} MB of active expert weights that the last {LAYER_COPIES - 1} "
+                   f"steps did not touch through the {l2 / 1e6:.0f} MB L2; the kernels' code and the step's small "
+                   f"inputs stay in L2"),
+            ("us_l2_flushed" if args.l2 != "flush" else "us_no_flush"): round(other["ms_mean"] * 1e3, 3),
+            ("expert_kernel_us_l2_flushed" if args.l2 != "flush" else "expert_kernel_us_no_flush"):
+                round(other["expert_ms_mean"] * 1e3, 3),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "status": main["status"],
             "steps_with_device_error": main["bad_steps"],
@@ -787,6 +850,9 @@ def main():
                     help="time only the fused step (router projection + this many residual streams with "
                          "RMSNorm + MXFP8) on the workload; prints its own line")
     ap.add_argument("--seed", type=int, default=42, help="seed of every synthetic input (default 42)")
+    ap.add_argument("--l2", default="inputs", choices=["inputs", "flush"],
+                    help="between timed steps: no flush, the step's weights being larger than L2 (inputs), or an "
+                         "L2 flush (flush); the other policy is reported beside the value")
     ap.add_argument("--clocks-log", default=None,
                     help="also write the raw nvidia-smi clock samples of the timed region to this CSV file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
