@@ -305,7 +305,8 @@ moe_status_t moe_kernel_times(void *plan, double *expert_ms_out, int32_t *launch
 moe_status_t moe_plan_status(void *plan, int32_t *status_out);
 
 /* Diagnostics of the last device-side error on this plan: 8 int64 words
- *   [0] site: 1 ready-counter wait, 2 pipeline full wait, 3 pipeline empty wait, 4 router
+ *   [0] site: 1 ready-counter wait, 2 pipeline full wait, 3 pipeline empty wait, 4 router,
+ *       5 unit-queue wait (tensor-core expert kernel)
  *   [1] work unit, [2] tile (or ring stage), [3] value observed, [4] value expected,
  *   [5] ns waited, [6] SM cycles waited, [7] block index.
  * All zero when the last step had no device-side error. Synchronises the device. */

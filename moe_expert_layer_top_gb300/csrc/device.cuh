@@ -48,7 +48,7 @@ struct WaitClock {
 
 // Diagnostic record of the first device-side error of a step (plan-owned, 8 words):
 // site, unit, tile, observed, expected, elapsed ns, elapsed cycles, block.
-enum DiagSite : int64_t { kDiagReadyWait = 1, kDiagFullWait = 2, kDiagEmptyWait = 3, kDiagRoute = 4 };
+enum DiagSite : int64_t { kDiagReadyWait = 1, kDiagFullWait = 2, kDiagEmptyWait = 3, kDiagRoute = 4, kDiagQueueWait = 5 };
 
 __device__ __forceinline__ void report_diag(int32_t *status, int64_t *diag, int32_t code, int64_t site, int64_t unit,
                                             int64_t tile, int64_t observed, int64_t expected, int64_t ns,

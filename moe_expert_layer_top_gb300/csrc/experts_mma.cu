@@ -19,16 +19,19 @@
 //       chunk's rows of h (MXFP8) as B. It waits (bounded) until ready[c]
 //       counts every gate/up unit of c. Epilogue: o[pair][h] in fp32, then the
 //       fused combine of every (token row, block) this unit completes.
-// Static schedule: block b runs gate/up units b, b + G, ... and then down
-// units G-1-b, 2G-1-b, ... (G blocks; the reversed order evens out the
-// per-block unit counts). Every gate/up unit precedes every down unit in each
-// block's order, so a down unit only waits on gate/up units, which never
-// wait. The waits cannot form a cycle, and every wait is bounded anyway.
+// Dynamic schedule: every block takes its next unit from the step's counter
+// when it is about to need it, so blocks that stream faster take more units
+// and all blocks finish within about one unit of each other (a static split of
+// 512 KB and 256 KB units left the last blocks 10 to 25 us behind the first).
+// The counter hands out every gate/up unit before any down unit, so a down
+// unit only waits on gate/up units that blocks have already taken, and those
+// never wait. The waits cannot form a cycle, and every wait is bounded anyway.
 //
 // Warp roles (10 warps):
-//   warp 0      TMA producer: one lane loads the A tiles (128 bytes of K x 64
-//               or 128 rows per box, 128-byte swizzle) into a 5-stage ring of
-//               two K chunks per stage.
+//   warp 0      TMA producer: one lane takes the block's units from the
+//               counter and queues them for the other roles; it loads the A
+//               tiles (128 bytes of K x 64 or 128 rows per box, 128-byte
+//               swizzle) into a 5-stage ring of two K chunks per stage.
 //   warp 1      MMA issuer: one lane issues tcgen05.mma.kind::mxf8f6f4
 //               .block_scale (4 per stage, K = 32 each) into one of two TMEM
 //               accumulators and commits each stage back to the ring.
@@ -71,7 +74,21 @@ constexpr int kEpiThreads = 128;            // threads of the epilogue warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kScaleSlotCols = 32;     // per stage: SFA at +0 (4 columns), SFB at +16 (4 columns)
 constexpr int kBarEpi = 2, kBarGate = 3;   // named barriers (0 is __syncthreads)
+constexpr int kUnitQ = 4;                   // entries of the block's unit queue
 static_assert(kMmaDownRows == kBM, "unit geometry");
+
+// One work unit, decoded.
+struct MUnit {
+  int u;       // unit index (-1: no more units)
+  int down;    // 0: gate/up, 1: down
+  int chunk;   // index into chunk_list
+  int blk;     // 64-row block of I (gate/up) or 128-row block of H (down)
+  int e;       // expert (E: the shared expert; -1: no more units)
+  int start;   // first rank of the chunk within the expert's rows
+  int n;       // token rows of the chunk (1..128)
+  int npad;    // n rounded up to 16 (the MMA's N)
+  int nch;     // chunks of the expert
+};
 
 // One instantiation per chunk size. A chunk of at most NMAX token rows is the
 // MMA's N. A stage holds KPS K-chunks of 128 (a 16 KB weight tile and an
@@ -100,6 +117,9 @@ struct MmaCfg {
     uint64_t acc_full[2];             // accumulator complete (tcgen05.commit)
     uint64_t acc_empty[2];            // accumulator read out (128 epilogue arrivals)
     uint64_t mma_done;                // every MMA of the block finished (before TMEM is freed)
+    uint64_t uq_full[kUnitQ];         // queue entry written (producer)
+    uint64_t uq_empty[kUnitQ];        // queue entry read by every consumer (MMA lane, loaders, epilogue)
+    MUnit uq[kUnitQ];                 // the block's units in order, decoded (e = -1: no more)
     uint32_t tmem_base;
     uint32_t n_jobs;
   };
@@ -229,16 +249,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 // ------------------------------------------------------------------ units and schedule
 
-struct MUnit {
-  int down;    // 0: gate/up, 1: down
-  int chunk;   // index into chunk_list
-  int blk;     // 64-row block of I (gate/up) or 128-row block of H (down)
-  int e;       // expert (E: the shared expert)
-  int start;   // first rank of the chunk within the expert's rows
-  int n;       // token rows of the chunk (1..128)
-  int npad;    // n rounded up to 16 (the MMA's N)
-  int nch;     // chunks of the expert
-};
 
 // An expert with cnt rows is split into ceil(cnt/NMAX) chunks of nearly equal
 // size. The units of one expert are consecutive: for each of its blocks in
@@ -248,6 +258,7 @@ struct MUnit {
 template <int NMAX>
 __device__ __forceinline__ MUnit decode_unit(const ExpertArgs &a, int u, int n_chunks, int mbg, int hbd) {
   MUnit m;
+  m.u = u;
   const int ng = n_chunks * mbg;
   int nb;  // blocks per chunk
   if (u < ng) {
@@ -275,20 +286,6 @@ __device__ __forceinline__ MUnit decode_unit(const ExpertArgs &a, int u, int n_c
   return m;
 }
 
-struct Sched {
-  int b, G, NG, ND, ng;
-  __device__ Sched(int n_chunks, int mbg, int hbd)
-      : b(blockIdx.x), G(gridDim.x), NG(n_chunks * mbg), ND(n_chunks * hbd) {
-    ng = b < NG ? (NG - 1 - b) / G + 1 : 0;
-  }
-  // The i-th unit of this block, or -1 past its end.
-  __device__ __forceinline__ int unit(int i) const {
-    if (i < ng) return b + i * G;
-    const int d = (G - 1 - b) + (i - ng) * G;
-    return d < ND ? NG + d : -1;
-  }
-};
-
 __device__ __forceinline__ bool aborted(const ExpertArgs &a) { return ld_volatile(a.work + 1) != 0; }
 
 __device__ __forceinline__ void fail(const ExpertArgs &a, int64_t site, int64_t unit, int64_t where, int64_t seen,
@@ -297,33 +294,88 @@ __device__ __forceinline__ void fail(const ExpertArgs &a, int64_t site, int64_t 
   atomicExch(a.work + 1, 1u);
 }
 
+// ------------------------------------------------------------------ unit queue
+// Units are handed out while the kernel runs: the TMA producer takes the next
+// unit index from the step's counter (work[0], zeroed by the route kernel) and
+// passes it to the block's other roles through a queue of kUnitQ entries in
+// shared memory. Blocks that stream faster take more units, so the blocks
+// finish within about one unit of each other. The counter hands out every
+// gate/up unit before any down unit, so a down unit only ever waits for gate/up
+// units that some block has already taken.
+
+// Entry i of the queue (blocking, bounded); e = -1 after a timeout.
+template <class C>
+__device__ __forceinline__ MUnit queue_pop(const ExpertArgs &a, typename C::Smem &sm, uint32_t i) {
+  const uint32_t qs = i % kUnitQ;
+  int64_t waited = 0;
+  MUnit m = {};
+  if (!mbar_wait(&sm.uq_full[qs], (i / kUnitQ) & 1u, a.timeout_ns, &waited)) {
+    fail(a, kDiagQueueWait, -1, qs, i, -16, waited);
+    m.u = m.e = -1;
+    return m;
+  }
+  m = sm.uq[qs];
+  mbar_arrive(&sm.uq_empty[qs]);
+  return m;
+}
+
 // ------------------------------------------------------------------ TMA producer (one lane)
 
 template <class C>
-__device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename C::Smem &sm, const Sched &sc,
-                             int n_chunks, int mbg, int hbd) {
+__device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename C::Smem &sm, int n_chunks, int mbg,
+                             int hbd) {
   constexpr int kMStages = C::STAGES;
   const uint64_t pol_first = l2_evict_first_policy(), pol_normal = l2_evict_normal_policy();
   // MXFP4 boxes move half the bytes (the transaction count is the packed
   // global bytes; each 16-code group lands in 16 bytes of shared memory)
   const uint32_t a_tx_bytes = a.fp4 ? kABytes / 2 : kABytes;
+  const int total = n_chunks * (mbg + hbd);
   uint32_t g = 0;  // stages issued
-  for (int i = 0;; ++i) {
-    const int u = sc.unit(i);
-    if (u < 0 || aborted(a)) break;
-    const MUnit m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
+  uint32_t q = 0;  // queue entries published
+  // Decode unit u (-1, or past the last unit: the end of the work) into the
+  // next queue entry. Consumers read the decoded unit from shared memory.
+  const auto publish = [&](int u) -> MUnit {
+    MUnit d = {};
+    d.u = d.e = -1;
+    if (u >= 0 && u < total && !aborted(a)) d = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
+    const uint32_t qs = q % kUnitQ;
+    int64_t waited = 0;
+    if (!mbar_wait(&sm.uq_empty[qs], ((q / kUnitQ) & 1u) ^ 1u, a.timeout_ns, &waited)) {
+      fail(a, kDiagQueueWait, u, qs, q, -17, waited);
+      d.u = d.e = -1;
+      return d;  // not published: the consumers' waits end at their limit
+    }
+    sm.uq[qs] = d;
+    mbar_arrive(&sm.uq_full[qs]);
+    ++q;
+    return d;
+  };
+  // Block b starts with unit b; the counter hands out units G, G + 1, ...
+  MUnit m = publish(int(blockIdx.x));
+  while (m.e >= 0) {
     const bool sh = m.e == a.E;
     // the chunks of a multi-chunk expert read the same weights at about the same time
     const uint64_t pol = m.nch > 1 ? pol_normal : pol_first;
     const int kcs = (m.down ? a.I : a.H) / kKC;
+    const int nst = (kcs + C::KPS - 1) / C::KPS;  // stages of the unit
+    // The next unit is taken four stages before this unit's last stage and
+    // published two stages before it, so the other roles find it decoded
+    // when they reach the end of this unit.
+    const int st_take = nst > 4 ? nst - 4 : 0, st_pub = nst > 2 ? nst - 2 : 0;
+    int nxt = -1;
+    MUnit mn = {};
+    mn.u = mn.e = -2;  // not published yet
     bool ok = true;
-    for (int kc0 = 0; kc0 < kcs; kc0 += C::KPS) {
+    for (int st = 0; st < nst; ++st) {
+      if (st == st_take) nxt = int(gridDim.x + atomicAdd(a.work, 1u));
+      if (st == st_pub) mn = publish(nxt);
+      const int kc0 = st * C::KPS;
       const int s = int(g % kMStages);
       const uint32_t ph = (g / kMStages) & 1u;
       const int nck = kcs - kc0 < C::KPS ? kcs - kc0 : C::KPS;
       int64_t waited = 0;
       if (!mbar_wait(&sm.empty[s], ph ^ 1u, a.timeout_ns, &waited)) {
-        fail(a, kDiagEmptyWait, u, s, kc0, -10, waited);
+        fail(a, kDiagEmptyWait, m.u, s, kc0, -10, waited);
         ok = false;
         break;
       }
@@ -341,7 +393,13 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
       }
       ++g;
     }
-    if (!ok) break;
+    if (!ok) {
+      // a failed unit ends the block's work (the abort flag is up); an end
+      // entry follows the last unit published
+      if (mn.e != -1) publish(-1);
+      break;
+    }
+    m = mn;
   }
   // No copy may still be in flight when the block exits: wait for the last
   // load of every slot (already complete unless the MMA side stopped early).
@@ -355,19 +413,18 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
 // ------------------------------------------------------------------ MMA issuer (one lane)
 
 template <class C>
-__device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t tmem, const Sched &sc, int n_chunks,
-                           int mbg, int hbd) {
+__device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t tmem, int n_chunks, int mbg,
+                           int hbd) {
   constexpr int kMStages = C::STAGES;
   uint32_t g = 0, nu = 0;  // stages consumed, units done
-  for (int i = 0;; ++i) {
-    const int u = sc.unit(i);
-    if (u < 0 || aborted(a)) break;
-    const MUnit m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
+  for (uint32_t i = 0;; ++i) {
+    const MUnit m = queue_pop<C>(a, sm, i);
+    if (m.e < 0 || aborted(a)) break;
     const int acc = int(nu & 1u);
     const uint32_t aph = (nu >> 1) & 1u;
     int64_t waited = 0;
     if (!mbar_wait(&sm.acc_empty[acc], aph ^ 1u, a.timeout_ns, &waited)) {
-      fail(a, kDiagEmptyWait, u, acc, -1, -11, waited);
+      fail(a, kDiagEmptyWait, m.u, acc, -1, -11, waited);
       break;
     }
     tmem_fence_after();
@@ -383,7 +440,7 @@ __device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t t
       const uint32_t ph = (g / kMStages) & 1u;
       const int nck = kcs - kc0 < C::KPS ? kcs - kc0 : C::KPS;
       if (!mbar_wait(&sm.full[s], ph, a.timeout_ns, &waited)) {
-        fail(a, kDiagFullWait, u, s, kc0, -12, waited);
+        fail(a, kDiagFullWait, m.u, s, kc0, -12, waited);
         ok = false;
         break;
       }
@@ -535,8 +592,7 @@ __device__ __forceinline__ int wait_chunk_ready(const ExpertArgs &a, int chunk, 
 }
 
 template <class C>
-__device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, const Sched &sc, int n_chunks,
-                            int mbg, int hbd) {
+__device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, int n_chunks, int mbg, int hbd) {
   constexpr int kMStages = C::STAGES;
   const int tau = int(threadIdx.x) - kWarpLoad * 32;
   const void *zero_src = a.xq;  // any valid address: zero-byte copies read nothing
@@ -550,17 +606,22 @@ __device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, co
   };
   MUnit m;
   LoaderRows<C::NMAX> lr;
-  int kc = 0, kcs = 0, next = 0;
+  int kc = 0, kcs = 0;
+  uint32_t next = 0;  // queue entries read
   while (true) {
     if (kc == kcs) {  // start the next unit
-      const int u = sc.unit(next++);
-      if (u < 0 || aborted(a)) break;
-      m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
+      // the stages in flight keep reaching the MMA while the entry is not there yet
+      if (gc < g && !mbar_test(&sm.uq_full[next % kUnitQ], (next / kUnitQ) & 1u)) {
+        complete_oldest();
+        continue;
+      }
+      m = queue_pop<C>(a, sm, next++);
+      if (m.e < 0 || aborted(a)) break;
       if (m.down && ld_acquire_gpu(a.ready + m.chunk) < uint32_t(mbg)) {
         // h of the chunk is not complete: everything in flight reaches the MMA
         // before this thread waits on other blocks
         while (gc < g) complete_oldest();
-        if (!wait_chunk_ready(a, m.chunk, uint32_t(mbg), u)) break;
+        if (!wait_chunk_ready(a, m.chunk, uint32_t(mbg), m.u)) break;
       }
       lr = loader_rows<C::NMAX>(a, T, m, tau);
       kc = 0;
@@ -591,8 +652,8 @@ __device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, co
 // ------------------------------------------------------------------ epilogue (warps 6-9)
 
 template <class C>
-__device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, uint32_t tmem, const Sched &sc,
-                             int n_chunks, int mbg, int hbd) {
+__device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, uint32_t tmem, int n_chunks, int mbg,
+                             int hbd) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ew = warp - kWarpEpi;
   const int et = ew * 32 + lane;
   const int64_t tk = int64_t(T) * a.k;
@@ -600,10 +661,10 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
   const float lim = a.swiglu_limit;
   uint32_t nu = 0, xc = 0;  // units done, gate/up column slices done
   static_assert(C::NMAX <= 32, "one pair id per lane");
-  for (int i = 0;; ++i) {
-    const int u = sc.unit(i);
-    if (u < 0) break;
-    const MUnit m = decode_unit<C::NMAX>(a, u, n_chunks, mbg, hbd);
+  for (uint32_t i = 0;; ++i) {
+    const MUnit m = queue_pop<C>(a, sm, i);
+    // every epilogue thread read the same entry (or timed out): they leave together
+    if (!bar_and(kBarEpi, kEpiThreads, m.e >= 0 ? 1 : 0)) break;
     const int acc = int(nu & 1u);
     const uint32_t aph = (nu >> 1) & 1u;
     // pair id of column `lane` of the chunk (-1 past its end), loaded before the wait
@@ -613,7 +674,7 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
     if (ok) {
       int64_t waited = 0;
       ok = mbar_wait(&sm.acc_full[acc], aph, a.timeout_ns, &waited) ? 1 : 0;
-      if (!ok) fail(a, kDiagFullWait, u, acc, -1, -15, waited);
+      if (!ok) fail(a, kDiagFullWait, m.u, acc, -1, -15, waited);
     }
     if (!bar_and(kBarEpi, kEpiThreads, ok)) break;
     tmem_fence_after();
@@ -725,6 +786,10 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
       mbar_init(&sm.acc_empty[i], kEpiThreads);
     }
     mbar_init(&sm.mma_done, 1);
+    for (int i = 0; i < kUnitQ; ++i) {
+      mbar_init(&sm.uq_full[i], 1);
+      mbar_init(&sm.uq_empty[i], 1 + kLoaders + kEpiThreads);
+    }
     sm.n_jobs = 0;
     fence_mbar_init();
   }
@@ -752,15 +817,14 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
   }
   const int n_chunks = __ldcg(a.n_chunks);
   const int mbg = a.I / 64, hbd = a.H / kBM;
-  const Sched sc(n_chunks, mbg, hbd);
   if (warp == kWarpTma) {
-    if (lane == 0) mma_producer<C>(maps, a, sm, sc, n_chunks, mbg, hbd);
+    if (lane == 0) mma_producer<C>(maps, a, sm, n_chunks, mbg, hbd);
   } else if (warp == kWarpMma) {
-    if (lane == 0) mma_issuer<C>(a, sm, tmem, sc, n_chunks, mbg, hbd);
+    if (lane == 0) mma_issuer<C>(a, sm, tmem, n_chunks, mbg, hbd);
   } else if (warp < kWarpEpi) {
-    mma_loaders<C>(a, T, sm, sc, n_chunks, mbg, hbd);
+    mma_loaders<C>(a, T, sm, n_chunks, mbg, hbd);
   } else {
-    mma_epilogue<C>(a, T, sm, tmem, sc, n_chunks, mbg, hbd);
+    mma_epilogue<C>(a, T, sm, tmem, n_chunks, mbg, hbd);
   }
   __syncwarp();
   tmem_fence_before();

@@ -38,7 +38,7 @@ struct Scratch {
   int32_t *n_chunks;    // [1]
   uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile (per chunk on the tensor-core path)
   uint32_t *comb_cnt;   // [Tmax][down blocks] down blocks of a token row finished (fused combine)
-  uint32_t *work;       // [4] (unused), abort flag, route-kernel ticket, (unused)
+  uint32_t *work;       // [4] expert-kernel unit counter, abort flag, route-kernel ticket, (unused)
   int32_t *status;      // [1] plan-owned status word
   int64_t *diag;        // [8] first device-side error of the last step (site, unit, tile, ...)
   uint8_t *xq, *xs;     // [Tmax][H], [Tmax][H/32]

@@ -491,6 +491,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
     if (tid < 8) a.diag[tid] = 0;
     if (tid == 0) {
       *a.status = MOE_OK;  // start of the step
+      a.work[0] = 0;       // unit counter of the tensor-core expert kernel
       a.work[1] = 0;       // abort flag
       if (bad_T) report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
       if (T == 0) {        // an empty step: empty work lists
