@@ -610,7 +610,7 @@ def run_gpu(args):
             from moe_expert_layer_top_gb300.layer import MoEWeightsMXFP8
             w0 = weights_for(w_l)
             sets = [w0]
-            for _ in range(LAYER_COPIES - 1):
+            for _ in range(args.layer_copies - 1):
                 sets.append(MoEWeightsMXFP8(*[None if getattr(w0, f) is None else getattr(w0, f).clone()
                                               for f in MoEWeightsMXFP8.__dataclass_fields__]))
             torch.cuda.synchronize()
@@ -743,11 +743,11 @@ def run_gpu(args):
             "us_max": round(main["ms_max"] * 1e3, 3),
             "l2": ("flushed before every step (memset of a buffer >= 2x L2, outside the timed events)"
                    if args.l2 == "flush" else
-                   f"inputs larger than L2: no flush; steps cycle through {LAYER_COPIES} copies of the layer's "
-                   f"weights (a stack of identical layers), so every step streams "
-                   f"{main['weight_bytes'] / 1e6:.0f} MB of active expert weights that the last {LAYER_COPIES - 1} "
-                   f"steps did not touch through the {l2 / 1e6:.0f} MB L2; the kernels' code and the step's small "
-                   f"inputs stay in L2"),
+                   f"inputs larger than L2: no flush; steps cycle through {args.layer_copies} copies of the "
+                   f"layer's weights (a stack of identical layers), so every step streams "
+                   f"{main['weight_bytes'] / 1e6:.0f} MB of active expert weights that the last "
+                   f"{args.layer_copies - 1} steps did not touch through the {l2 / 1e6:.0f} MB L2; the kernels' "
+                   f"code and the step's small inputs stay in L2"),
             ("us_l2_flushed" if args.l2 != "flush" else "us_no_flush"): round(other["ms_mean"] * 1e3, 3),
             ("expert_kernel_us_l2_flushed" if args.l2 != "flush" else "expert_kernel_us_no_flush"):
                 round(other["expert_ms_mean"] * 1e3, 3),
@@ -860,9 +860,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--experts", type=int, default=0,
                     help="smaller expert count for profiling captures (default: the workload's E)")
+    ap.add_argument("--layer-copies", type=int, default=LAYER_COPIES,
+                    help=f"copies of the layer's weights the timed steps cycle through (default {LAYER_COPIES}; "
+                         "1 keeps a profiling capture's device memory small)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    args.layer_copies = max(1, args.layer_copies)
     if args.impl == "reference":
         run_reference(args)
     else:

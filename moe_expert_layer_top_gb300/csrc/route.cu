@@ -281,9 +281,11 @@ __device__ void router_block(const RouteArgs &a, int T, int rg, int eb, RouteSme
 }
 
 // Top-k and combine weights, one warp per token row. Each lane keeps its NC
-// candidates (lane, lane + 32, ...) in registers as 64-bit keys: the
-// order-preserving bits of the logit, then the complemented expert id. So the
-// largest key is the largest logit and, among equal logits, the lower id.
+// candidates (lane, lane + 32, ...) in registers as the order-preserving bits
+// of the logit, with a mask of the candidates not taken yet. A round takes the
+// largest key in the warp (redux.sync max), then the lowest expert id that
+// holds it (redux.sync min): the largest logit and, among equal logits, the
+// lower id.
 // bm: the block's bitmap in shared memory when one block routes every row
 // (the bits are set here); NULL when the last block builds it in phase 2.
 // rg: the row group (rows 32 rg .. 32 rg + 31, one per warp). The logits are
@@ -298,35 +300,35 @@ __device__ __forceinline__ void route_topk(const RouteArgs &a, int T, int rg, Ro
     const int t = rg * kWarps + warp;
     if (t >= T) return;
     const float *row = a.logits + int64_t(t) * E;
-    uint64_t key[NC];
+    uint32_t ord[NC];
+    uint32_t live = 0;  // bit j: candidate j (expert 32 j + lane) not taken yet
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
       const int i = j * 32 + lane;
-      key[j] = 0;
+      ord[j] = 0;
       if (i < E) {
         const uint32_t b = __float_as_uint(__ldcg(row + i));
-        const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-        key[j] = (uint64_t(ord) << 32) | uint32_t(0xFFFFFFFFu - uint32_t(i));
+        ord[j] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        live |= 1u << j;
       }
     }
     for (int r = 0; r < k; ++r) {
-      uint64_t best = 0;
-#pragma unroll
-      for (int j = 0; j < NC; ++j) best = key[j] > best ? key[j] : best;
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        best = o > best ? o : best;
-      }
-      const int id = int(0xFFFFFFFFu - uint32_t(best));
-      if (id >= E) report_error(a.status, MOE_ERR_DEVICE_BOUNDS);  // cannot happen for k <= E
+      uint32_t lmax = 0;
 #pragma unroll
       for (int j = 0; j < NC; ++j)
-        if (key[j] == best) key[j] = 0;  // taken (only the owning lane matches)
+        if ((live >> j) & 1u) lmax = ord[j] > lmax ? ord[j] : lmax;
+      const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, lmax);
+      uint32_t lid = 0xFFFFFFFFu;  // this lane's lowest live id holding the best key
+#pragma unroll
+      for (int j = NC - 1; j >= 0; --j)
+        if (((live >> j) & 1u) && ord[j] == best) lid = uint32_t(j * 32 + lane);
+      const uint32_t uid = __reduce_min_sync(0xFFFFFFFFu, lid);
+      const int id = int(uid);
+      if (uid >= uint32_t(E)) report_error(a.status, MOE_ERR_DEVICE_BOUNDS);  // cannot happen for k <= E
+      if (lid == uid) live &= ~(1u << (uid >> 5));  // taken (only the owning lane matches)
       if (lane == 0) {
-        const uint32_t ord = uint32_t(best >> 32);
-        const uint32_t bits = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
-        sm.sel_i[warp][r] = id < E ? id : 0;
+        const uint32_t bits = (best & 0x80000000u) ? (best & 0x7FFFFFFFu) : ~best;
+        sm.sel_i[warp][r] = uid < uint32_t(E) ? id : 0;
         sm.sel_v[warp][r] = __uint_as_float(bits);
       }
     }
@@ -409,9 +411,14 @@ __device__ void route_place(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *
   } else {
     sm.tiles[tid] = 0;
   }
-  // block-wide exclusive prefix of tiles[] (work enumeration for the expert kernel)
-  int total = 0;
-  const int excl = block_exclusive_scan(sm, sm.tiles[tid], total);
+  // Block-wide exclusive prefixes of the tile and chunk counts (work
+  // enumeration for the expert kernels), in one scan of packed counts: each
+  // total is at most T (k + 1) / 8 + E + 1 < 2^15 (T <= 4096, k <= 32,
+  // E <= 1024), so the low half never carries into the high half.
+  const int nch = (a.chunk_list && tid < nexp) ? (cnt + a.chunk_rows - 1) / a.chunk_rows : 0;
+  int packed_total = 0;
+  const int packed_excl = block_exclusive_scan(sm, sm.tiles[tid] | (nch << 16), packed_total);
+  const int excl = packed_excl & 0xFFFF, total = packed_total & 0xFFFF;
   if (tid < nexp) {
     for (int j = 0; j < sm.tiles[tid]; ++j) {
       const int idx = excl + j;
@@ -423,9 +430,7 @@ __device__ void route_place(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *
 
   // chunks of <= chunk_rows rows per expert, for the tensor-core expert kernel
   if (a.chunk_list) {
-    const int nch = tid < nexp ? (cnt + a.chunk_rows - 1) / a.chunk_rows : 0;
-    int nch_total = 0;
-    const int cexcl = block_exclusive_scan(sm, nch, nch_total);
+    const int cexcl = packed_excl >> 16, nch_total = packed_total >> 16;
     for (int j = 0; j < nch; ++j) {
       const int idx = cexcl + j;
       if (idx < a.n_tiles_max) a.chunk_list[idx] = (tid << 16) | j;
