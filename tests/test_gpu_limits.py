@@ -4,6 +4,10 @@
   then a last-block placement over every pair.
 * E = 1024 and k = 32: the widest top-k (32 candidates per lane, 32 rounds).
 * I = 16384: 128 K chunks per down unit and 256 gate/up blocks per expert.
+* T = 4096, E = 256, k = 32 with the shared expert: about 17,000 tiles and
+  4,400 chunks, the largest work lists the bitmap's shared-memory limit
+  admits; the route kernel scans the tile and chunk counts packed in 16-bit
+  halves of one integer, so the totals must stay below 2^15.
 Routing, placement and x quantisation are compared with the oracle bit for
 bit, and y within the stated tolerance.
 """
@@ -33,6 +37,7 @@ LIMITS = [
     (4096, 128, 8, 2, 128, "zipf", 1),      # the largest max_rows
     (8, 128, 1024, 32, 128, "uniform", 0),  # the most experts and the widest top-k
     (2, 128, 4, 2, 16384, "uniform", 1),    # the largest intermediate size
+    (4096, 128, 256, 32, 128, "uniform", 1),  # the longest tile and chunk lists
 ]
 
 
