@@ -268,11 +268,14 @@ typedef struct moe_fused_io {
 moe_status_t moe_forward_fused(void *plan, const void *x, int32_t T, const moe_fused_io_t *io, void *y,
                                const moe_taps_t *taps, int32_t *d_status, void *cuda_stream);
 
-/* Runtime with host buffers: copies x and logits from host memory into
- * plan-owned device buffers, runs moe_forward and copies y back to y_host. It
- * then synchronises cuda_stream and returns the device-side status of the
- * step. Pinned host memory gives asynchronous copies; pageable memory works
- * too. x_host: bf16 [T][H]; logits_host: fp32 [T][E]; y_host: bf16 [T][H]. */
+/* Runtime with host buffers: runs moe_forward on x and logits in host memory
+ * and leaves y in host memory. It then synchronises cuda_stream and returns
+ * the device-side status of the step. A buffer in pinned (page-locked) host
+ * memory, 16-byte aligned, is read or written by the kernels in place over
+ * the host link; any other buffer is copied through plan-owned device memory
+ * (pageable memory works, with synchronous copies). The caller must not touch
+ * the buffers until the call returns.
+ * x_host: bf16 [T][H]; logits_host: fp32 [T][E]; y_host: bf16 [T][H]. */
 moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logits_host,
                               int32_t T, void *y_host, void *cuda_stream);
 

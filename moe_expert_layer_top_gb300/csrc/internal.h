@@ -76,6 +76,7 @@ struct Plan {
   Scratch s;
   void *arena;           // single device allocation backing Scratch
   size_t arena_bytes;
+  int32_t *status_host;  // pinned host word: the step's status, read back by moe_forward_host
   // timing
   cudaEvent_t ev_start[kMaxTimedCalls];
   cudaEvent_t ev_stop[kMaxTimedCalls];

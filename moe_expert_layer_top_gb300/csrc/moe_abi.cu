@@ -98,6 +98,7 @@ void destroy_plan(Plan *p) {
     }
   }
   if (p->arena) cudaFree(p->arena);
+  if (p->status_host) cudaFreeHost(p->status_host);
   delete p;
 }
 
@@ -261,6 +262,12 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   if (!encode_mma_maps(c, *weights, &p->maps)) {
     destroy_plan(p);
     return MOE_ERR_CUDA;
+  }
+  if (cudaHostAlloc(reinterpret_cast<void **>(&p->status_host), 4, cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    p->status_host = nullptr;
+    destroy_plan(p);
+    return MOE_ERR_OOM;
   }
   if (c.flags & MOE_FLAG_TIMING) {
     for (int i = 0; i < kMaxTimedCalls; ++i) {
@@ -498,16 +505,39 @@ moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logit
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const moe_config_t &c = p->cfg;
   const size_t xb = size_t(T) * c.hidden * 2, lb = size_t(T) * c.num_experts * 4;
-  if (cudaMemcpyAsync(p->s.x_dev, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemcpyAsync(p->s.logits_dev, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  moe_status_t r = moe_forward(plan, p->s.x_dev, p->s.logits_dev, T, p->s.y_dev, nullptr, nullptr, cuda_stream);
+  // Pinned (page-locked, mapped) host memory is in the device's address
+  // space: the kernels read x and the logits and write y there directly, over
+  // the host link, with no copy operation. Other host memory goes through
+  // plan-owned device buffers.
+  const auto mapped = [](const void *h) -> const void * {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+  };
+  const void *x_dev = mapped(x_host);
+  const void *l_dev = mapped(logits_host);
+  void *y_dev = const_cast<void *>(mapped(y_host));
+  if (!x_dev || !aligned16(x_dev)) {
+    if (cudaMemcpyAsync(p->s.x_dev, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return MOE_ERR_CUDA;
+    x_dev = p->s.x_dev;
+  }
+  if (!l_dev || !aligned16(l_dev)) {
+    if (cudaMemcpyAsync(p->s.logits_dev, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    l_dev = p->s.logits_dev;
+  }
+  const bool y_staged = !y_dev || !aligned16(y_dev);
+  if (y_staged) y_dev = p->s.y_dev;
+  moe_status_t r = moe_forward(plan, x_dev, static_cast<const float *>(l_dev), T, y_dev, nullptr, nullptr, cuda_stream);
   if (r != MOE_OK) return r;
-  if (cudaMemcpyAsync(y_host, p->s.y_dev, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
-  int32_t dev_status = 0;
-  if (cudaMemcpyAsync(&dev_status, p->s.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (y_staged && cudaMemcpyAsync(y_host, p->s.y_dev, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(p->status_host, p->s.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
-  return static_cast<moe_status_t>(dev_status);
+  return static_cast<moe_status_t>(*p->status_host);
 }
 
 moe_status_t moe_quantize_mxfp8(const void *x, int64_t rows, int32_t cols, uint8_t *q, uint8_t *s, void *cuda_stream) {

@@ -280,11 +280,30 @@ def test_bounded_wait_timeout_is_reported_and_recoverable(path):
 
 
 def test_forward_host_matches_device_forward():
+    """Pinned buffers: the kernels read x and the logits and write y in host memory."""
     T, H, E, k, I = 6, 512, 8, 2, 256
     g = CudaStep(T, H, E, k, I).run()
     xh = torch.from_numpy(g.x_bits.view(np.int16).copy()).pin_memory()
     lh = torch.from_numpy(g.lg.copy()).pin_memory()
     yh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    assert g.step.forward_host(xh, lh, yh) == abi.MOE_OK
+    np.testing.assert_array_equal(yh.numpy().view(np.uint16), g.y_bits)
+    g.close()
+
+
+@pytest.mark.parametrize("pinned", ["none", "x", "y"])
+def test_forward_host_pageable_buffers(pinned):
+    """Pageable buffers take copies through the plan's device buffers, alone or
+    mixed with pinned ones; the result is the same as the device-side step."""
+    T, H, E, k, I = 6, 512, 8, 2, 256
+    g = CudaStep(T, H, E, k, I).run()
+    xh = torch.from_numpy(g.x_bits.view(np.int16).copy())
+    lh = torch.from_numpy(g.lg.copy())
+    yh = torch.full((T, H), -1, dtype=torch.int16)
+    if pinned == "x":
+        xh = xh.pin_memory()
+    if pinned == "y":
+        yh = yh.pin_memory()
     assert g.step.forward_host(xh, lh, yh) == abi.MOE_OK
     np.testing.assert_array_equal(yh.numpy().view(np.uint16), g.y_bits)
     g.close()
