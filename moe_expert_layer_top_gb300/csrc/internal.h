@@ -76,7 +76,8 @@ struct Plan {
   Scratch s;
   void *arena;           // single device allocation backing Scratch
   size_t arena_bytes;
-  int32_t *status_host;  // pinned host word: the step's status, read back by moe_forward_host
+  int32_t *status_host;  // pinned host word: the status of moe_forward_host's steps
+  int32_t *status_mapped;  // the same word's device address (the kernels write it over the host link)
   // timing
   cudaEvent_t ev_start[kMaxTimedCalls];
   cudaEvent_t ev_stop[kMaxTimedCalls];

@@ -263,11 +263,15 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
     destroy_plan(p);
     return MOE_ERR_CUDA;
   }
-  if (cudaHostAlloc(reinterpret_cast<void **>(&p->status_host), 4, cudaHostAllocDefault) != cudaSuccess) {
+  if (cudaHostAlloc(reinterpret_cast<void **>(&p->status_host), 4, cudaHostAllocMapped) != cudaSuccess) {
     cudaGetLastError();
     p->status_host = nullptr;
     destroy_plan(p);
     return MOE_ERR_OOM;
+  }
+  if (cudaHostGetDevicePointer(reinterpret_cast<void **>(&p->status_mapped), p->status_host, 0) != cudaSuccess) {
+    destroy_plan(p);
+    return MOE_ERR_CUDA;
   }
   if (c.flags & MOE_FLAG_TIMING) {
     for (int i = 0; i < kMaxTimedCalls; ++i) {
@@ -531,13 +535,16 @@ moe_status_t moe_forward_host(void *plan, const void *x_host, const float *logit
   }
   const bool y_staged = !y_dev || !aligned16(y_dev);
   if (y_staged) y_dev = p->s.y_dev;
-  moe_status_t r = moe_forward(plan, x_dev, static_cast<const float *>(l_dev), T, y_dev, nullptr, nullptr, cuda_stream);
+  // The step's status goes straight to the plan's pinned word (the route
+  // kernel sets it at the start of the step; errors replace it).
+  *reinterpret_cast<volatile int32_t *>(p->status_host) = MOE_ERR_CUDA;
+  moe_status_t r = moe_forward(plan, x_dev, static_cast<const float *>(l_dev), T, y_dev, nullptr, p->status_mapped,
+                               cuda_stream);
   if (r != MOE_OK) return r;
   if (y_staged && cudaMemcpyAsync(y_host, p->s.y_dev, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (cudaMemcpyAsync(p->status_host, p->s.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
-  return static_cast<moe_status_t>(*p->status_host);
+  return static_cast<moe_status_t>(*reinterpret_cast<volatile int32_t *>(p->status_host));
 }
 
 moe_status_t moe_quantize_mxfp8(const void *x, int64_t rows, int32_t cols, uint8_t *q, uint8_t *s, void *cuda_stream) {
