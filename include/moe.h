@@ -84,8 +84,8 @@ typedef enum {
 #define MOE_FLAG_PATH_GEMV (1u << 1)
 #define MOE_FLAG_PATH_MMA (1u << 2)
 /* Expert kernel selection. By default every step runs the tensor-core expert
- * kernel: block-scaled MXFP8 tcgen05 MMA, one MMA covering up to 16 or 32
- * token rows of an expert, so each expert's weights stream once per step.
+ * kernel: block-scaled MXFP8 tcgen05 MMA, one MMA covering up to 16, 32 or
+ * 64 token rows of an expert, so each expert's weights stream once per step.
  * PATH_GEMV selects the CUDA-core GEMV expert kernel instead (8-row tiles;
  * an expert's weights stream once per tile). PATH_MMA pins the default.
  * Setting both is MOE_ERR_INVALID_ARG. Both kernels compute the same result

@@ -3,8 +3,8 @@
 //
 // The CUDA-core expert kernel streams an expert's weights once per 8-row tile,
 // so an expert with hundreds of rows re-reads them and spends CUDA-core FMAs
-// on every tile. Here each expert's rows are split into chunks of <= 16 or 32
-// rows, and one MMA per 32 K columns covers a whole chunk. The chunks of one
+// on every tile. Here each expert's rows are split into chunks of <= 16, 32 or
+// 64 rows, and one MMA per 32 K columns covers a whole chunk. The chunks of one
 // expert run side by side on neighbouring blocks and read each weight block
 // from HBM once (the others find it in L2). Tensor time is small next to the
 // weight stream, so the kernel stays bound by HBM, also at one token row.
@@ -131,6 +131,7 @@ struct MmaCfg {
 };
 using Cfg16 = MmaCfg<16, 5, 2>;
 using Cfg32 = MmaCfg<32, 5, 2>;
+using Cfg64 = MmaCfg<64, 4, 2>;
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -660,16 +661,18 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
   const uint32_t target = uint32_t(a.k + a.shared);
   const float lim = a.swiglu_limit;
   uint32_t nu = 0, xc = 0;  // units done, gate/up column slices done
-  static_assert(C::NMAX <= 32, "one pair id per lane");
+  static_assert(C::NMAX <= 64, "at most two pair ids per lane");
   for (uint32_t i = 0;; ++i) {
     const MUnit m = queue_pop<C>(a, sm, i);
     // every epilogue thread read the same entry (or timed out): they leave together
     if (!bar_and(kBarEpi, kEpiThreads, m.e >= 0 ? 1 : 0)) break;
     const int acc = int(nu & 1u);
     const uint32_t aph = (nu >> 1) & 1u;
-    // pair id of column `lane` of the chunk (-1 past its end), loaded before the wait
+    // pair id of column `lane` (and 32 + lane) of the chunk (-1 past its end), loaded before the wait
     const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
     const int pr = lane < m.n ? __ldcg(rows + lane) : -1;
+    int pr2 = -1;
+    if constexpr (C::NMAX > 32) pr2 = 32 + lane < m.n ? __ldcg(rows + 32 + lane) : -1;
     int ok = !aborted(a);
     if (ok) {
       int64_t waited = 0;
@@ -695,7 +698,13 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
           const int64_t col = int64_t(m.blk) * 64 + 32 * q + lane;
 #pragma unroll 4
           for (int c = 0; c < 16; ++c) {
-            const int p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
+            int p;
+            if constexpr (C::NMAX > 32) {
+              const int col = 16 * j + c;
+              p = __shfl_sync(0xFFFFFFFFu, col < 32 ? pr : pr2, col & 31);
+            } else {
+              p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
+            }
             if (p < 0) continue;  // the same for the whole warp
             float gb = bf16_bits_to_float(float_to_bf16_bits(v[c]));
             float ub = bf16_bits_to_float(xb[c][32 * q + lane]);
@@ -731,7 +740,13 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
         tmem_ld16(ta + uint32_t(16 * j), v);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const int p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
+          int p;
+          if constexpr (C::NMAX > 32) {
+            const int col = 16 * j + c;
+            p = __shfl_sync(0xFFFFFFFFu, col < 32 ? pr : pr2, col & 31);
+          } else {
+            p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
+          }
           if (p >= 0) a.o[int64_t(p) * a.H + h] = v[c];
         }
       }
@@ -741,8 +756,10 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
       // thread's fence orders every warp's o stores of the unit before its count.
       // The last of a row's k (+ shared) pairs queues the row's combine.
       named_bar(kBarEpi, kEpiThreads);
-      if (ew == 0 && pr >= 0) {
-        const int t = int(pr < tk ? pr / a.k : pr - tk);
+      // epilogue warp 0 counts columns 0-31, warp 1 columns 32-63
+      const int pc = ew == 0 ? pr : (C::NMAX > 32 && ew == 1 ? pr2 : -1);
+      if (pc >= 0) {
+        const int t = int(pc < tk ? pc / a.k : pc - tk);
         __threadfence();
         if (atomicAdd(a.comb_cnt + int64_t(t) * hbd + m.blk, 1u) == target - 1u) {
           const uint32_t idx = atomicAdd(&sm.n_jobs, 1u);
@@ -917,15 +934,17 @@ cudaError_t launch_cfg(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaS
 }  // namespace
 
 // Chunk size. A chunk never holds more rows than the step (an expert has at
-// most T rows), so T <= 16 uses 16-row chunks. Larger steps use 32-row chunks.
-// Chunks of 64 or 128 rows (fewer stages) were slower on GB300 at 48 to 384
-// rows: the deeper ring is worth more than the weight blocks that the chunks
-// of a hot expert read again from L2.
-int mma_chunk_rows(int T) { return T <= 16 ? 16 : 32; }
+// most T rows), so T <= 16 uses 16-row chunks, up to 128 rows 32-row chunks
+// (a 5-stage ring). Above 128 rows the hot experts hold many rows, and each
+// chunk lands the expert's weight tiles in shared memory again: 64-row chunks
+// (a 4-stage ring) land fewer bytes, which pays there (384 rows with Zipf
+// routing: 1,199 -> 1,185 us per step). 128-row chunks leave too few stages.
+int mma_chunk_rows(int T) { return T <= 16 ? 16 : (T <= 128 ? 32 : 64); }
 
 cudaError_t prepare_experts_mma() {
   cudaError_t e = prepare_cfg<Cfg16>();
   if (e == cudaSuccess) e = prepare_cfg<Cfg32>();
+  if (e == cudaSuccess) e = prepare_cfg<Cfg64>();
   return e;
 }
 
@@ -933,6 +952,7 @@ cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int gri
   switch (chunk_rows) {
     case 16: return launch_cfg<Cfg16>(maps, a, grid, st);
     case 32: return launch_cfg<Cfg32>(maps, a, grid, st);
+    case 64: return launch_cfg<Cfg64>(maps, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }

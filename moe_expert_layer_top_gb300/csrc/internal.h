@@ -103,7 +103,7 @@ struct RouteArgs {
   int32_t *n_tiles;
   int32_t *chunk_list;  // NULL: no chunk list (the GEMV expert kernel only)
   int32_t *n_chunks;
-  int chunk_rows;       // rows per chunk (16 or 32)
+  int chunk_rows;       // rows per chunk (16, 32 or 64)
   uint32_t *ready;
   int n_tiles_max;
   uint32_t *comb_cnt;
