@@ -257,21 +257,31 @@ def kernel_path(path, T):
     return "mma" if T >= MMA_MIN_ROWS else "gemv"
 
 
+def code_sha256(path):
+    """sha256 of a C++/CUDA source with its comments and whitespace removed: the
+    hash changes when the code does, not when a comment does."""
+    import hashlib
+    import re
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256("".join(text.split()).encode()).hexdigest()
+
+
 def traffic_per_launch(algorithmic_bytes, path="gemv"):
     """DRAM bytes per expert-kernel launch from the committed ncu capture, scaled
-    by the active weight bytes; None if the kernel source changed since then."""
-    import hashlib
+    by the active weight bytes; None if the kernel's code changed since then."""
     _, src_name, summary = EXPERT_KERNELS[path]
     p = os.path.join(ROOT, "profiles", summary)
     src = os.path.join(ROOT, "moe_expert_layer_top_gb300", "csrc", src_name)
     try:
         with open(p) as f:
             d = json.load(f)
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        sha = code_sha256(src)
     except OSError:
         return None
-    if sha != d["source_sha256"]:
+    if sha != d.get("source_code_sha256"):
         return None
     ratio = (d["dram_bytes_read"] + d["dram_bytes_write"]) / d["algorithmic_bytes"]
     return int(round(algorithmic_bytes * ratio))

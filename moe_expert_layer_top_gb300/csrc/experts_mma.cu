@@ -31,7 +31,8 @@
 //   warp 0      TMA producer: one lane takes the block's units from the
 //               counter and queues them for the other roles; it loads the A
 //               tiles (128 bytes of K x 64 or 128 rows per box, 128-byte
-//               swizzle) into a 5-stage ring of two K chunks per stage.
+//               swizzle) into a ring of two K chunks per stage (5 stages
+//               with 16- and 32-row chunks, 4 with 64-row chunks).
 //   warp 1      MMA issuer: one lane issues tcgen05.mma.kind::mxf8f6f4
 //               .block_scale (4 per stage, K = 32 each) into one of two TMEM
 //               accumulators and commits each stage back to the ring.
