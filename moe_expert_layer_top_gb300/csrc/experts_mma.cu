@@ -9,7 +9,7 @@
 // from HBM once (the others find it in L2). Tensor time is small next to the
 // weight stream, so the kernel stays bound by HBM, also at one token row.
 //
-// Work units, in each block's order:
+// Work units, in the order the step counter hands them out:
 //   gate/up unit (chunk c, block b): rows [64b, 64b + 64) of W_gate and of W_up
 //       as the MMA's A operand (M = 128: 64 gate rows, then 64 up rows); the
 //       chunk's token rows of x (MXFP8) as B (N = rows rounded up to 16).
