@@ -79,6 +79,7 @@ def cfg(**kw):
     (dict(num_experts=1025, top_k=8), abi.MOE_ERR_UNSUPPORTED),
     (dict(num_experts=64, top_k=33), abi.MOE_ERR_UNSUPPORTED),
     (dict(max_rows=5000), abi.MOE_ERR_UNSUPPORTED),
+    (dict(num_experts=1024, max_rows=4096), abi.MOE_ERR_UNSUPPORTED),  # 512 KB of bitmap: beyond shared memory
     (dict(flags=abi.MOE_FLAG_PATH_GEMV | abi.MOE_FLAG_PATH_MMA), abi.MOE_ERR_INVALID_ARG),
 ])
 def test_guard_rejects_before_device(lib, kw, expect):
