@@ -59,4 +59,5 @@ from .formats import (  # noqa: F401
 )
 from .fused import residual_norm_mxfp8, router_logits  # noqa: F401
 from .routing import exp_rn, placement, softmax_topk_weights, topk_ids  # noqa: F401
-from .step import ExpertWeights, expert_weights_from_synth, moe_step  # noqa: F401
+from .step import (ExpertWeights, combine, expert_mlp, expert_pairs, expert_weights_from_bf16,  # noqa: F401
+                   expert_weights_from_synth, moe_route, moe_step, pair_token)

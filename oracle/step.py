@@ -66,6 +66,16 @@ class ExpertWeights:
         return mxfp4_dequantize(q, s) if self.fmt == "mxfp4" else mxfp8_dequantize(q, s)
 
 
+def expert_weights_from_bf16(g_bits, u_bits, d_bits, fmt: str = "mxfp8") -> ExpertWeights:
+    """Quantise one expert's bf16 weights (bit patterns: gate [I][H], up [I][H],
+    down [H][I]) with the oracle's own MXFP8 (or MXFP4) rule along K."""
+    quant = mxfp4_quantize if fmt == "mxfp4" else mxfp8_quantize
+    wg, sgc = quant(bf16_bits_to_f64(np.asarray(g_bits, dtype=np.uint16)))
+    wu, suc = quant(bf16_bits_to_f64(np.asarray(u_bits, dtype=np.uint16)))
+    wd, sdc = quant(bf16_bits_to_f64(np.asarray(d_bits, dtype=np.uint16)))
+    return ExpertWeights(wg, sgc, wu, suc, wd, sdc, fmt)
+
+
 def expert_weights_from_synth(seed: int, e, H: int, I: int, fmt: str = "mxfp8") -> ExpertWeights:
     """Draw expert e's bf16 weights from the seeded generator, then quantise
     them with the oracle's own MXFP8 (or MXFP4) rule. e == "shared" selects
@@ -75,14 +85,9 @@ def expert_weights_from_synth(seed: int, e, H: int, I: int, fmt: str = "mxfp8") 
         sg, su, sd = synth.STREAM_SH_GATE, synth.STREAM_SH_UP, synth.STREAM_SH_DOWN
     else:
         sg, su, sd = synth.stream_gate(e), synth.stream_up(e), synth.stream_down(e)
-    g = bf16_bits_to_f64(synth.expert_weight_bf16(seed, sg, I, H))
-    u = bf16_bits_to_f64(synth.expert_weight_bf16(seed, su, I, H))
-    d = bf16_bits_to_f64(synth.expert_weight_bf16(seed, sd, H, I))
-    quant = mxfp4_quantize if fmt == "mxfp4" else mxfp8_quantize
-    wg, sgc = quant(g)
-    wu, suc = quant(u)
-    wd, sdc = quant(d)
-    return ExpertWeights(wg, sgc, wu, suc, wd, sdc, fmt)
+    return expert_weights_from_bf16(synth.expert_weight_bf16(seed, sg, I, H),
+                                    synth.expert_weight_bf16(seed, su, I, H),
+                                    synth.expert_weight_bf16(seed, sd, H, I), fmt)
 
 
 def _round_f32(v) -> np.ndarray:
@@ -117,6 +122,51 @@ def expert_mlp(xq, xs, w: ExpertWeights, swiglu_limit: float = 0.0):
     return g, u, h, hq, hs, o
 
 
+def moe_route(x_bits, logits, k: int):
+    """The step's front: top-k ids, combine weights, placement and the MXFP8
+    token rows. Returns a dict with ids, w, bitmap, counts, tiles,
+    slot_e/slot_tile/slot_row, rows_of, xq and xs."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    logits = np.asarray(logits, dtype=np.float32)
+    E = logits.shape[1]
+    ids = topk_ids(logits, k)
+    w = softmax_topk_weights(logits, ids)
+    plc = placement(ids, E)
+    xq, xs = mxfp8_quantize(bf16_bits_to_f64(x_bits))
+    return {"ids": ids, "w": w, "xq": xq, "xs": xs, **plc}
+
+
+def pair_token(p: int, T: int, k: int) -> int:
+    """Token row of pair p (routed pairs t*k + j, then shared pairs T*k + t)."""
+    return p // k if p < T * k else p - T * k
+
+
+def expert_pairs(route: dict, T: int, k: int, e, rows=None):
+    """Pair ids that expert e (or "shared") serves, restricted to the token
+    rows in `rows` (None: all), in rank order."""
+    row_set = None if rows is None else set(int(r) for r in rows)
+    if e == "shared":
+        src = range(T * k, T * k + T)
+    else:
+        src = (int(p) for p in route["rows_of"][e])
+    return [p for p in src if row_set is None or pair_token(p, T, k) in row_set]
+
+
+def combine(w, o_all, T: int, k: int, shared: bool, rows=None):
+    """y[t] = bf16( ((w_1*o_1 + w_2*o_2) + ...) + o_shared ) in binary32, rank
+    order; o_all is indexed by pair id. Rows outside `rows` are 0."""
+    H = o_all.shape[1]
+    y = np.zeros((T, H), dtype=np.uint16)
+    for t in (range(T) if rows is None else sorted(set(int(r) for r in rows))):
+        acc = w[t, 0] * o_all[t * k + 0]                          # binary32 products and sums
+        for j in range(1, k):
+            acc = acc + w[t, j] * o_all[t * k + j]
+        if shared:
+            acc = acc + o_all[T * k + t]
+        y[t] = f32_to_bf16_bits(acc.astype(np.float32))
+    return y
+
+
 def moe_step(x_bits, logits, k: int,
              experts: Mapping[int, ExpertWeights] | Callable[[int], ExpertWeights],
              shared: ExpertWeights | None = None,
@@ -137,35 +187,29 @@ def moe_step(x_bits, logits, k: int,
       g, u, h (bf16 bits), hq, hs, o (fp32), plus y (bf16 bits [T][H]).
     """
     x_bits = np.asarray(x_bits, dtype=np.uint16)
-    logits = np.asarray(logits, dtype=np.float32)
     T, H = x_bits.shape
-    E = logits.shape[1]
+    E = np.asarray(logits).shape[1]
     get = experts if callable(experts) else experts.__getitem__
-    ids = topk_ids(logits, k)
-    w = softmax_topk_weights(logits, ids)
-    plc = placement(ids, E)
-    xq, xs = mxfp8_quantize(bf16_bits_to_f64(x_bits))
-
-    row_set = set(range(T)) if rows is None else set(int(r) for r in rows)
+    out = moe_route(x_bits, logits, k)
+    xq, xs = out["xq"], out["xs"]
     n_pairs = T * k + (T if shared is not None else 0)
-    out = {"ids": ids, "w": w, "xq": xq, "xs": xs, **plc}
     I = None
     pair_res = {}
 
     def run(pair_ids, weights):
         nonlocal I
-        toks = np.array([p // k if p < T * k else p - T * k for p in pair_ids])
+        toks = np.array([pair_token(p, T, k) for p in pair_ids])
         g, u, h, hq, hs, o = expert_mlp(xq[toks], xs[toks], weights, swiglu_limit)
         I = g.shape[1]
         for n, p in enumerate(pair_ids):
             pair_res[int(p)] = (g[n], u[n], h[n], hq[n], hs[n], o[n])
 
     for e in range(E):
-        pairs = [int(p) for p in plc["rows_of"][e] if (int(p) // k) in row_set]
+        pairs = expert_pairs(out, T, k, e, rows)
         if pairs:
             run(pairs, get(e))
     if shared is not None:
-        pairs = [T * k + t for t in range(T) if t in row_set]
+        pairs = expert_pairs(out, T, k, "shared", rows)
         if pairs:
             run(pairs, shared)
 
@@ -180,12 +224,6 @@ def moe_step(x_bits, logits, k: int,
         for p, (g, u, h, hq, hs, o) in pair_res.items():
             g_all[p], u_all[p], h_all[p], hq_all[p], hs_all[p], o_all[p] = g, u, h, hq, hs, o
         out.update(g=g_all, u=u_all, h=h_all, hq=hq_all, hs=hs_all, o=o_all)
-        for t in sorted(row_set):
-            acc = w[t, 0] * o_all[t * k + 0]                      # binary32 products and sums
-            for j in range(1, k):
-                acc = acc + w[t, j] * o_all[t * k + j]
-            if shared is not None:
-                acc = acc + o_all[T * k + t]
-            y[t] = f32_to_bf16_bits(acc.astype(np.float32))
+        y = combine(out["w"], o_all, T, k, shared is not None, rows)
     out["y"] = y
     return out
