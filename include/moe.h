@@ -175,6 +175,14 @@ const char *moe_status_string(moe_status_t status);
  * device must be compute capability 10.3 (sm_103).
  * The Build step allocates every scratch buffer for max_rows. moe_forward
  * allocates nothing. It also records the weight pointers.
+ * Weight ownership: the plan does NOT copy or re-lay-out the weights. A plugin
+ * Build that reorganises the weights would own a copy and let the caller free
+ * its own; this one reads the caller's canonical K-major MXFP8/MXFP4 arrays in
+ * place (the tensor-core kernel's TMA tensor maps are encoded over them here),
+ * which saves a second copy of every expert (6.5 GB at E = 256, H = 4096,
+ * I = 2048). So the caller must keep the weight buffers allocated and
+ * unchanged until moe_destroy; changing them changes the next step's result,
+ * and freeing them first is undefined.
  * On success *plan_out receives an opaque handle; on failure it is set to NULL.
  * The plan belongs to the device that is current at this call. */
 moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights,
@@ -338,11 +346,15 @@ moe_status_t moe_plan_diagnostics(void *plan, int64_t *out8);
  * or two host threads) race and corrupt each other's results. Everything that
  * must start at zero is cleared by the step itself, except one counter at the
  * start of the array that every completed step leaves at zero.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and sets kernel
- * attributes. Make that first call before any stream capture. Each call also
- * raises the route kernel's dynamic shared-memory limit (cudaFuncSetAttribute,
- * host-side only).
+ * The first call on a device checks the device (with that device current)
+ * and may load this library's device code: make it before any stream capture.
+ * Every call looks up the array's device address (cudaGetSymbolAddress) and
+ * sets the two kernels' shared-memory limits (cudaFuncSetAttribute), with the
+ * device current; both are host-side and allocate nothing, so a
+ * cudaDeviceReset leaves no stale address behind.
+ * d_status NULL: the step's status is written into the array, and no call
+ * reads it back, so device-side errors (MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_BOUNDS)
+ * are then lost. Pass d_status to see them.
  * The pages have no counterpart to this entry point. */
 moe_status_t moe_forward_static_scratch(const moe_config_t *config, const moe_weights_t *weights, const void *x,
                                         const float *logits, int32_t T, void *y, int32_t *d_status,

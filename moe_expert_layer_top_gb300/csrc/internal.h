@@ -22,6 +22,7 @@ constexpr int kChunkRowsMax = 32;       // tensor-core expert kernel: most token
 constexpr int kMmaDownRows = 128;       // tensor-core expert kernel: W_down rows per down unit
 constexpr int kMmaMinRowsDefault = 1;   // steps with at least this many rows take the tensor-core kernel
 constexpr int kRouterExperts = 8;       // route kernel: experts per router-projection block
+constexpr size_t kRouteSmemMax = 200 * 1024;  // Guard: the route kernel's largest dynamic shared memory
 constexpr int kMaxStreams = 4;          // residual streams per token row in the fused epilogue
 
 // Device scratch and schedule of one plan (all sized for max_rows).
@@ -160,7 +161,10 @@ struct ResidArgs {
 size_t route_smem_bytes(int E, int words);
 cudaError_t prepare_residual_norm(int H);
 cudaError_t launch_residual_norm(const ResidArgs &a, cudaStream_t st);
-cudaError_t prepare_route(size_t smem);
+// Sets the route kernel's dynamic shared-memory limit to kRouteSmemMax. The
+// limit is one per-function setting for the whole process, so it is never
+// set lower: every plan and the static-scratch step work under it.
+cudaError_t prepare_route();
 cudaError_t prepare_experts(int H, int I);
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
 cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int cols, uint8_t *q, uint8_t *s, cudaStream_t st);

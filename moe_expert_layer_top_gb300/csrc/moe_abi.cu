@@ -55,7 +55,7 @@ moe_status_t guard_config(const moe_config_t &c) {
   if (c.top_k > 32) return MOE_ERR_UNSUPPORTED;
   if (c.max_rows > 4096) return MOE_ERR_UNSUPPORTED;
   const int words = (c.max_rows + 31) / 32;
-  if (route_smem_bytes(c.num_experts, words) > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  if (route_smem_bytes(c.num_experts, words) > kRouteSmemMax) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -253,7 +253,7 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
     destroy_plan(p);
     return MOE_ERR_CUDA;
   }
-  if (prepare_route(route_smem_bytes(E, p->words)) != cudaSuccess ||
+  if (prepare_route() != cudaSuccess ||
       (experts_shape_supported(H, I) && prepare_experts(H, I) != cudaSuccess) || prepare_experts_mma() != cudaSuccess ||
       prepare_residual_norm(H) != cudaSuccess) {
     destroy_plan(p);

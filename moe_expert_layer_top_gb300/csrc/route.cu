@@ -307,7 +307,9 @@ __device__ __forceinline__ void route_topk(const RouteArgs &a, int T, int rg, Ro
       const int i = j * 32 + lane;
       ord[j] = 0;
       if (i < E) {
-        const uint32_t b = __float_as_uint(__ldcg(row + i));
+        uint32_t b = __float_as_uint(__ldcg(row + i));
+        // -0.0 and +0.0 compare equal: one key for both, so they tie to the lower id
+        if (b == 0x80000000u) b = 0u;
         ord[j] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
         live |= 1u << j;
       }
@@ -556,8 +558,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
 
 size_t route_smem_bytes(int E, int words) { return sizeof(RouteSmem) + size_t(E) * words * sizeof(uint32_t); }
 
-cudaError_t prepare_route(size_t smem) {
-  return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+cudaError_t prepare_route() {
+  return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kRouteSmemMax));
 }
 
 // R routing blocks (R * ceil(E/8) projection blocks with a router weight),

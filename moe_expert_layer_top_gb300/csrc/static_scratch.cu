@@ -24,11 +24,16 @@
 //  - Everything that must start at zero is cleared by the step's first
 //    kernel: the per-tile ready counts, the work and abort words, the status
 //    word and the diagnostics.
-// The address of the array is looked up with cudaGetSymbolAddress the first
-// time the entry point runs on a device, with that device current. That
-// first call must come before any stream capture that includes a call. Each
-// call also raises the route kernel's dynamic shared-memory limit with
-// cudaFuncSetAttribute (host-side, allocates nothing).
+// Set-up. The first call on a device checks the device and records its SM
+// count, with that device current. Every call then looks up the array's device
+// address with cudaGetSymbolAddress and sets the kernels' dynamic
+// shared-memory limits with cudaFuncSetAttribute: host-side calls that
+// allocate nothing, repeated so that a cudaDeviceReset (which reloads the
+// module) never leaves a stale address or a lost attribute behind. The first
+// call on a device may load this library's device code: make it before any
+// stream capture that includes a call.
+// Status: with d_status NULL the step writes its status into the array,
+// where no call reads it back; pass d_status to see device-side errors.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -46,16 +51,14 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
   bool done = false;
-  unsigned char *scratch = nullptr;  // device address of g_static_scratch on this device
   int num_sms = 0;
 };
 
 DeviceSetup g_setup[kMaxDevices];
 std::mutex g_setup_mutex;
 
-// Once per device, with that device current: the array's device address and
-// the kernels' shared-memory limits.
-moe_status_t setup_device(int dev, DeviceSetup *&out) {
+// Once per device, with that device current: the device check and its SM count.
+moe_status_t setup_device(int dev, int *num_sms) {
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   DeviceSetup &d = g_setup[dev];
@@ -66,17 +69,21 @@ moe_status_t setup_device(int dev, DeviceSetup *&out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) return MOE_ERR_CUDA;
-    // every compiled expert shape
-    if (prepare_experts(4096, 2048) != cudaSuccess || prepare_experts(1024, 512) != cudaSuccess ||
-        prepare_experts(512, 256) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    d.scratch = static_cast<unsigned char *>(ptr);
     d.num_sms = sms;
     d.done = true;
   }
-  out = &d;
+  *num_sms = d.num_sms;
+  return MOE_OK;
+}
+
+// Every call, with the device current: the array's device address on this
+// device (host code cannot use g_static_scratch itself), and the shared-memory
+// limits of the two kernels the step launches. Host-side only; allocates nothing.
+moe_status_t bind_scratch(int H, int I, unsigned char **scratch) {
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) return MOE_ERR_CUDA;
+  if (prepare_experts(H, I) != cudaSuccess || prepare_route() != cudaSuccess) return MOE_ERR_CUDA;
+  *scratch = static_cast<unsigned char *>(ptr);
   return MOE_OK;
 }
 
@@ -157,13 +164,12 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  DeviceSetup *d = nullptr;
-  const moe_status_t sg = setup_device(dev, d);
+  int num_sms = 0;
+  const moe_status_t sg = setup_device(dev, &num_sms);
   if (sg != MOE_OK) return sg;
-  // The route kernel's shared-memory limit is a per-function setting that a
-  // plan may have lowered; raise it to the Guard's maximum (a host-side call).
-  if (prepare_route(200 * 1024) != cudaSuccess) return MOE_ERR_CUDA;
-  unsigned char *base = d->scratch;
+  unsigned char *base = nullptr;
+  const moe_status_t bs = bind_scratch(c.hidden, c.intermediate, &base);
+  if (bs != MOE_OK) return bs;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   int32_t *status = d_status ? d_status : reinterpret_cast<int32_t *>(base + L.status);
 
@@ -248,7 +254,7 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ea.skip_ready_tile = -1;
   ea.fp4 = 0;
   ea.swiglu_limit = c.swiglu_limit;
-  if (launch_experts(ea, d->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_experts(ea, num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   return MOE_OK;
 }
