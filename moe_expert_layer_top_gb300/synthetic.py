@@ -68,3 +68,24 @@ def make_inputs(seed: int, T: int, H: int, E: int, k: int, routing: str, device=
     x_dev = torch.from_numpy(x_bits.view(np.int16).copy()).view(torch.bfloat16).to(device)
     lg_dev = torch.from_numpy(lg.copy()).to(device)
     return x_dev, lg_dev, x_bits, lg
+
+
+def weights_from_bf16(gate: np.ndarray, up: np.ndarray, down: np.ndarray, sh_gate=None, sh_up=None, sh_down=None,
+                      device="cuda", fmt: str = "mxfp8") -> MoEWeightsMXFP8:
+    """Canonical weights from given bf16 bit patterns (host uint16 arrays:
+    gate, up [E][I][H], down [E][H][I]; sh_* without the E axis), uploaded and
+    quantised with this library's moe_quantize_mxfp8 (or _mxfp4)."""
+    quant = quantize_mxfp4 if fmt == "mxfp4" else quantize_mxfp8
+
+    def q(bits):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+        return quant(t)
+    wg, sg = q(gate)
+    wu, su = q(up)
+    wd, sd = q(down)
+    w = MoEWeightsMXFP8(wg, sg, wu, su, wd, sd)
+    if sh_gate is not None:
+        w.sh_w_gate, w.sh_s_gate = q(sh_gate)
+        w.sh_w_up, w.sh_s_up = q(sh_up)
+        w.sh_w_down, w.sh_s_down = q(sh_down)
+    return w

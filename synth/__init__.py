@@ -282,3 +282,92 @@ def mix_coefficients(seed: int, T: int, S: int):
     post = (uniform_open01(seed, STREAM_MIX_POST, 0, T * S) * 2.0).astype(np.float32)
     pre = uniform_open01(seed, STREAM_MIX_PRE, 0, T * S).astype(np.float32)
     return res.reshape(T, S, S), post.reshape(T, S), pre.reshape(T, S)
+
+
+# ----------------------------------------------------------------- structured inputs for exact parity
+
+STREAM_EXACT = 11
+STREAM_OUTLIER = 12
+
+
+def _f32_to_bf16_exact(v: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of float32 values that bf16 represents exactly."""
+    u = np.asarray(v, dtype=np.float32).view(np.uint32)
+    if np.any(u & np.uint32(0xFFFF)):
+        raise ValueError("value not representable in bf16")
+    return (u >> np.uint32(16)).astype(np.uint16)
+
+
+def _grid(seed: int, stream: int, rows: int, cols: int, base_choices, signed: bool) -> np.ndarray:
+    """[rows][cols] float32 values m * 2^(a - d): per row and 32-column group a
+    base exponent a from base_choices, per element m in {1, 1.5} and d in
+    {0, 1, 2} (and a sign when signed). A group then spans a factor of 6 at
+    most: every value is exact in bf16, in E4M3 and in E2M1 at the group's
+    shared power-of-two scale."""
+    groups = cols // 32
+    hb = counter_u64(seed, stream, 0, rows * groups).reshape(rows, groups)
+    base = np.asarray(base_choices, dtype=np.int64)[(hb % np.uint64(len(base_choices))).astype(np.int64)]
+    he = counter_u64(seed, stream + 1, 0, rows * cols).reshape(rows, cols)
+    m = np.where((he & np.uint64(1)) != 0, 1.5, 1.0)
+    d = ((he >> np.uint64(1)) % np.uint64(3)).astype(np.int64)
+    s = np.where(signed & ((he >> np.uint64(8)) & np.uint64(1) != 0), -1.0, 1.0)
+    a = np.repeat(base, 32, axis=1)
+    return (s * m * np.exp2(a - d)).astype(np.float32)
+
+
+def exact_case(seed: int, T: int, H: int, E: int, k: int, I: int, shared: int = 0, routing: str = "uniform"):
+    """Inputs on which every intermediate of the MoE step is exactly defined.
+
+    Token rows and weights take grid values (_grid), so every product of two
+    of them is a multiple of 2^-8, and every sum of H (or I) of them stays
+    below 2^24 of that unit: the binary32 sums are exact in any order. Per
+    expert:
+      gate row i = 2^(L_j + b_i) * r_g, with one positive row pattern r_g,
+                   b_i in {0, 1} and a level L_j in {0, 1, 2} per 32-row group j;
+      up row i   = +-r_u, with one signed row pattern r_u;
+      down       = independent signed grid values.
+    The token rows are positive, so each gate sum is at least H / 64, far into
+    the range where silu(g) rounds to g in binary32. A row's h values are then
+    +-2^(L_j + b_i) times one value: h's MXFP8 scale codes differ from group to
+    group along I, its groups are exact multiples of a common unit, and the
+    down sums are exact too.
+    Returns x (bf16 bits [T][H]), logits (fp32 [T][E]) and the bf16 bits of
+    gate [E][I][H], up [E][I][H], down [E][H][I] (+ sh_gate, sh_up, sh_down
+    when shared)."""
+    x = _grid(seed, STREAM_EXACT * 1000, T, H, (-1, 0, 1), False)
+
+    def expert(base_stream):
+        rg = _grid(seed, base_stream, 1, H, (-1, 0, 1), False)
+        ru = _grid(seed, base_stream + 2, 1, H, (-1, 0, 1), True)
+        hb = counter_u64(seed, base_stream + 4, 0, I + I // 32)
+        b = (hb[:I] & np.uint64(1)).astype(np.float32)
+        level = np.repeat((hb[I:] % np.uint64(3)).astype(np.float32), 32)
+        sgn = np.where(((hb[:I] >> np.uint64(1)) & np.uint64(1)) != 0, -1.0, 1.0).astype(np.float32)
+        gate = np.exp2(level + b)[:, None] * rg
+        up = sgn[:, None] * ru
+        down = _grid(seed, base_stream + 5, H, I, (-1, 0), True)
+        return _f32_to_bf16_exact(gate), _f32_to_bf16_exact(up), _f32_to_bf16_exact(down)
+
+    parts = [expert(STREAM_EXACT * 1000 + 10 * (e + 1)) for e in range(E)]
+    out = {
+        "x": _f32_to_bf16_exact(x),
+        "logits": router_logits(seed, T, E, k, routing),
+        "gate": np.stack([p[0] for p in parts]),
+        "up": np.stack([p[1] for p in parts]),
+        "down": np.stack([p[2] for p in parts]),
+    }
+    if shared:
+        out["sh_gate"], out["sh_up"], out["sh_down"] = expert(STREAM_EXACT * 1000 + 10 * (E + 1))
+    return out
+
+
+def x_bf16_outliers(seed: int, T: int, H: int, every: int = 97, lo: int = 4, hi: int = 12) -> np.ndarray:
+    """Token rows x ~ N(0, 1) (x_bf16) with about one element in `every`
+    multiplied by 2^s, s drawn from [lo, hi]: activation outliers that spread
+    the exponents inside a 32-group. A power-of-two factor is exact in bf16."""
+    x = bf16_bits_to_float32(x_bf16(seed, T, H)).reshape(-1)
+    h = counter_u64(seed, STREAM_OUTLIER, 0, T * H)
+    pick = (h % np.uint64(every)) == 0
+    s = (lo + ((h >> np.uint64(16)) % np.uint64(hi - lo + 1)).astype(np.int64)).astype(np.float32)
+    x = np.where(pick, x * np.exp2(s), x).astype(np.float32)
+    return _f32_to_bf16_exact(x).reshape(T, H)

@@ -54,3 +54,20 @@ def test_parity_at_the_limits(case):
     check_h_quantizer_bit_exact(g)
     check_y(g.y_bits, r["y"])
     g.close()
+
+
+def test_small_plan_after_large_plan_keeps_the_large_plan_working():
+    """The route kernel's shared-memory limit is one setting per kernel for the
+    whole process. A plan whose bitmap needs far more than the default (E = 256,
+    max_rows = 2048: 64 KB of bitmap) must still run after a small plan is built."""
+    T, H, E, k, I = 2048, 512, 256, 2, 256
+    big = CudaStep(T, H, E, k, I, "zipf", seed=77)
+    small = CudaStep(6, H, 8, 2, I, seed=78).run()
+    assert small.status_code == abi.MOE_OK
+    big.run()
+    assert big.status_code == abi.MOE_OK, (abi.moe_status_string(big.status_code), big.diag)
+    r = oracle.moe_step(big.x_bits, big.lg, k, oracle_experts(77, E, H, I), rows=[0, 1, T - 1])
+    check_routing_bit_exact(big, r)
+    check_y(big.y_bits[[0, 1, T - 1]], r["y"][[0, 1, T - 1]])
+    small.close()
+    big.close()

@@ -18,7 +18,8 @@ from moe_expert_layer_top_gb300 import abi, synthetic
 from moe_expert_layer_top_gb300.layer import MoEStep, quantize_mxfp4, quantize_mxfp8
 
 from gpu_cases import (CudaStep, bf16_dev_to_bits, check_h_close, check_h_quantizer_bit_exact,
-                       check_routing_bit_exact, check_xquant_bit_exact, check_y, oracle_experts, rel_fro, to_np)
+                       check_routing_bit_exact, check_xquant_bit_exact, check_y, oracle_abs_sums, oracle_experts,
+                       rel_fro, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -139,7 +140,8 @@ def test_small_case_parity(case, path):
     check_xquant_bit_exact(g, r)
     check_h_quantizer_bit_exact(g)
     P = T * k + T * shared
-    check_h_close(g, r, np.arange(P))
+    sg, su = oracle_abs_sums(r, T, k, get, sh)
+    check_h_close(g, r, np.arange(P), sg, su)
     assert rel_fro(g.t["o"], r["o"]) <= 1e-2
     check_y(g.y_bits, r["y"])
     g.close()
@@ -167,7 +169,8 @@ def test_mxfp4_weights_parity(case):
     check_xquant_bit_exact(g, r)
     check_h_quantizer_bit_exact(g)
     P = T * k + T * shared
-    check_h_close(g, r, np.arange(P))
+    sg, su = oracle_abs_sums(r, T, k, get, sh)
+    check_h_close(g, r, np.arange(P), sg, su, lim)
     assert rel_fro(g.t["o"], r["o"]) <= 1e-2
     check_y(g.y_bits, r["y"])
     # the device-prepared MXFP4 weights are the oracle's, bit for bit
@@ -188,7 +191,8 @@ def test_clipped_swiglu_parity(path):
     r0 = oracle.moe_step(g.x_bits, g.lg, k, get, shared=sh)
     assert np.mean(r["h"] != r0["h"]) > 0.1          # the clip changes h
     check_h_quantizer_bit_exact(g)
-    check_h_close(g, r, np.arange(T * k + T))
+    sg, su = oracle_abs_sums(r, T, k, get, sh)
+    check_h_close(g, r, np.arange(T * k + T), sg, su, lim)
     check_y(g.y_bits, r["y"])
     g.close()
 
