@@ -128,7 +128,8 @@ SILU_MIN_AT = -1.2784645427610738   # the one stationary point of silu(g) = g si
 
 
 def _silu(g):
-    return g / (1.0 + np.exp(-g))
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
 
 
 def h_envelope(g_bits, u_bits, sum_g, sum_u, K_gate: int, lim: float = 0.0):
@@ -141,7 +142,11 @@ def h_envelope(g_bits, u_bits, sum_g, sum_u, K_gate: int, lim: float = 0.0):
     bound), and its bf16 g' within that plus one bf16 step of the oracle's g.
     The same holds for u'. h = silu(min(g', L)) * clamp(u', -L, L) is taken
     at the ends of both intervals (and at silu's stationary point when it lies
-    inside), and the result may round by one more bf16 step each way."""
+    inside), and the result may round by one more bf16 step each way.
+    The device evaluates silu(g) = g / (1 + exp(-g)) in binary32, where exp(-g)
+    overflows for g < -88.72 and silu(g) becomes -0; there the exact value has
+    magnitude below 88.73 e^-88.72 < 2^-121, so h may also be off by up to
+    |u'| 2^-121 (a value below 1e-36 where it matters at all)."""
     gb = oracle.bf16_bits_to_f64(np.asarray(g_bits, dtype=np.uint16))
     ub = oracle.bf16_bits_to_f64(np.asarray(u_bits, dtype=np.uint16))
     eps = K_gate * 2.0 ** -24
@@ -158,8 +163,9 @@ def h_envelope(g_bits, u_bits, sum_g, sum_u, K_gate: int, lim: float = 0.0):
     vals = [_silu(g) * u for g in gs for u in us]
     lo = np.minimum.reduce(vals)
     hi = np.maximum.reduce(vals)
-    lo = lo - bf16_step(lo)
-    hi = hi + bf16_step(hi)
+    tail = np.maximum.reduce([np.abs(u) for u in us]) * 2.0 ** -121
+    lo = lo - bf16_step(lo) - tail
+    hi = hi + bf16_step(hi) + tail
     return lo, hi
 
 

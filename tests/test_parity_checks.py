@@ -79,3 +79,16 @@ def test_planted_gate_up_swap_leaves_envelope():
     sg, su = np.abs(x) @ np.abs(wg).T, np.abs(x) @ np.abs(wu).T
     h_bad = _device_like(x, wu, wg)
     assert np.mean(~_inside(h_bad, g_ref, u_ref, sg, su)) > 0.5
+
+
+def test_binary32_silu_overflow_tail_inside_envelope():
+    """g = -90: binary32 exp(90) overflows and g / (1 + exp(-g)) gives -0, so h = 0
+    where the exact h is about -7e-38 u. That stays inside the envelope; a
+    value of the wrong size there does not."""
+    g_bits = oracle.f32_to_bf16_bits(np.array([[-90.0, -100.0, -20.0]], dtype=np.float32))
+    u_bits = oracle.f32_to_bf16_bits(np.array([[31.0, -5.0, 3.0]], dtype=np.float32))
+    z = np.zeros((1, 3))
+    lo, hi = h_envelope(g_bits, u_bits, z, z, H)
+    assert lo[0, 0] <= 0.0 <= hi[0, 0] and lo[0, 1] <= 0.0 <= hi[0, 1]
+    exact = -20.0 / (1.0 + np.exp(20.0)) * 3.0
+    assert not (lo[0, 2] <= 0.0 <= hi[0, 2]) and lo[0, 2] <= exact <= hi[0, 2]
