@@ -197,3 +197,39 @@ def test_clip_with_a_large_limit_changes_nothing():
     b = oracle.step.expert_mlp(xq, xs, w, swiglu_limit=1e30)
     for p, q in zip(a, b):
         np.testing.assert_array_equal(p, q)
+
+
+def test_expert_weights_from_bf16_is_the_synth_path_and_lossless_on_grid_values():
+    """expert_weights_from_bf16 on the generator's bits equals
+    expert_weights_from_synth; on grid values (synth.exact_case) both formats
+    quantise without loss."""
+    import synth
+    H, I = 256, 128
+    a = oracle.expert_weights_from_synth(3, 1, H, I)
+    b = oracle.expert_weights_from_bf16(synth.expert_weight_bf16(3, synth.stream_gate(1), I, H),
+                                        synth.expert_weight_bf16(3, synth.stream_up(1), I, H),
+                                        synth.expert_weight_bf16(3, synth.stream_down(1), H, I))
+    for n in ("w_gate", "s_gate", "w_up", "s_up", "w_down", "s_down"):
+        np.testing.assert_array_equal(getattr(a, n), getattr(b, n))
+    c = synth.exact_case(4, 8, H, 2, 2, I)
+    for fmt in ("mxfp8", "mxfp4"):
+        w = oracle.expert_weights_from_bf16(c["gate"][1], c["up"][1], c["down"][1], fmt)
+        for n in ("gate", "up", "down"):
+            np.testing.assert_array_equal(w.dequant(n), oracle.bf16_bits_to_f64(c[n][1]))
+
+
+def test_exact_case_preconditions_hold():
+    """The structured inputs of the exact GPU parity case keep every binary32
+    sum of the step exact (the same checks the GPU test makes before it
+    compares bit for bit), for both weight formats and every case it runs."""
+    import synth
+    from test_gpu_exact import EXACT, _exact_sums_hold
+    H, E, k, I = 512, 8, 2, 256
+    for fmt in ("mxfp8", "mxfp4"):
+        for T, routing, shared in EXACT:
+            c = synth.exact_case(9, T, H, E, k, I, shared, routing)
+            ws = [oracle.expert_weights_from_bf16(c["gate"][e], c["up"][e], c["down"][e], fmt) for e in range(E)]
+            sh = oracle.expert_weights_from_bf16(c["sh_gate"], c["sh_up"], c["sh_down"], fmt) if shared else None
+            r = oracle.moe_step(c["x"], c["logits"], k, ws.__getitem__, shared=sh)
+            _exact_sums_hold(r, ws.__getitem__, sh, T, k)
+            assert np.mean([len(set(row)) for row in r["hs"]]) > 2.0   # h's scale codes vary along I
