@@ -92,47 +92,55 @@ struct MUnit {
 };
 
 // One instantiation per chunk size. A chunk of at most NMAX token rows is the
-// MMA's N. A stage holds KPS K-chunks of 128 (a 16 KB weight tile and an
-// NMAX-row token tile each): more chunks per stage spread the per-stage
-// costs of the MMA issuer (one barrier wait, one commit) over more MMAs.
+// MMA's N. A stage holds KPS K-chunks of 128 (MB weight tiles of 16 KB and one
+// NMAX-row token tile each): more chunks per stage spread the per-stage costs
+// of the MMA issuer (one barrier wait, one commit) over more MMAs.
+// MB weight blocks per unit (M = 128 each) share the stage's token tile: with
+// MB = 2 a unit covers 128 rows of I (gate/up) or 256 rows of H (down), and
+// each token tile lands once per 256 weight rows instead of once per 128.
 // The ring holds STAGES stages; smaller token tiles leave room for more.
-template <int NMAX_, int STAGES_, int KPS_>
+template <int NMAX_, int STAGES_, int KPS_, int MB_ = 1>
 struct MmaCfg {
   static constexpr int NMAX = NMAX_;
   static constexpr int STAGES = STAGES_;
   static constexpr int KPS = KPS_;
+  static constexpr int MB = MB_;
+  static constexpr int NPR = (NMAX + 31) / 32;                 // pair ids per epilogue lane
   static constexpr int BBYTES = NMAX * kKC;
-  static constexpr uint32_t ACC_COLS = NMAX < 32 ? 32 : NMAX;  // TMEM columns per accumulator
-  static constexpr uint32_t SCALE_COL0 = 2 * ACC_COLS;
+  static constexpr uint32_t ACC_COLS = NMAX < 32 ? 32 : NMAX;  // TMEM columns per accumulator (one M block)
+  static constexpr uint32_t BUF_COLS = MB * ACC_COLS;          // one unit's accumulators
+  static constexpr uint32_t SCALE_COL0 = 2 * BUF_COLS;
   static constexpr uint32_t SLOT_COLS = KPS * kScaleSlotCols;  // TMEM scale columns per stage
   struct Smem {
-    uint8_t a[STAGES][KPS][kABytes];  // weight tiles, 128-byte swizzled K-major (TMA)
-    uint8_t b[STAGES][KPS][BBYTES];   // token-row tiles, same layout (cp.async)
-    uint32_t sfa[STAGES][KPS][128];   // a chunk's 4 UE8M0 codes (one per 32 K) per weight row, TMEM image order
-    uint32_t sfb[STAGES][KPS][128];   // the same per token row (rows past NMAX unused)
-    uint16_t xchg[2][16][64];         // bf16 u of one 16-column slice, [column][i]
-    uint32_t jobs[NMAX];              // token rows whose combine a down unit completed
-    uint64_t full[STAGES];            // A landed (TMA bytes, producer arrival) and B + scale words in place
-                                      // (128 loader arrivals): one wait per stage for the MMA issuer
-    uint64_t empty[STAGES];           // the stage's MMAs are done (tcgen05.commit)
-    uint64_t acc_full[2];             // accumulator complete (tcgen05.commit)
-    uint64_t acc_empty[2];            // accumulator read out (128 epilogue arrivals)
-    uint64_t mma_done;                // every MMA of the block finished (before TMEM is freed)
-    uint64_t uq_full[kUnitQ];         // queue entry written (producer)
-    uint64_t uq_empty[kUnitQ];        // queue entry read by every consumer (MMA lane, loaders, epilogue)
-    MUnit uq[kUnitQ];                 // the block's units in order, decoded (e = -1: no more)
+    uint8_t a[STAGES][KPS][MB][kABytes];  // weight tiles, 128-byte swizzled K-major (TMA)
+    uint8_t b[STAGES][KPS][BBYTES];       // token-row tiles, same layout (cp.async)
+    uint32_t sfa[STAGES][KPS][MB][128];   // a chunk's 4 UE8M0 codes (one per 32 K) per weight row, TMEM image order
+    uint32_t sfb[STAGES][KPS][128];       // the same per token row (rows past NMAX unused)
+    uint16_t xchg[2][16][64];             // bf16 u of one 16-column slice, [column][i]
+    uint32_t jobs[NMAX];                  // token rows whose combine a down unit completed
+    uint64_t full[STAGES];                // A landed (TMA bytes, producer arrival) and B + scale words in place
+                                          // (128 loader arrivals): one wait per stage for the MMA issuer
+    uint64_t empty[STAGES];               // the stage's MMAs are done (tcgen05.commit)
+    uint64_t acc_full[2];                 // accumulators complete (tcgen05.commit)
+    uint64_t acc_empty[2];                // accumulators read out (128 epilogue arrivals)
+    uint64_t mma_done;                    // every MMA of the block finished (before TMEM is freed)
+    uint64_t uq_full[kUnitQ];             // queue entry written (producer)
+    uint64_t uq_empty[kUnitQ];            // queue entry read by every consumer (MMA lane, loaders, epilogue)
+    MUnit uq[kUnitQ];                     // the block's units in order, decoded (e = -1: no more)
     uint32_t tmem_base;
     uint32_t n_jobs;
   };
   static constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + alignment of the ring to 1024 bytes
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(SCALE_COL0 + STAGES * SLOT_COLS <= kTmemCols, "TMEM budget");
-  static_assert(NMAX % 16 == 0 && NMAX <= 128 && BBYTES % 1024 == 0, "token tile geometry");
+  static_assert(NMAX % 16 == 0 && NMAX <= 96 && BBYTES % 1024 == 0, "token tile geometry");
+  static_assert(MB == 1 || MB == 2, "one or two weight blocks per unit");
   static_assert(STAGES <= 11, "cp_async_wait_n covers at most 10 newer groups");
 };
 using Cfg16 = MmaCfg<16, 5, 2>;
 using Cfg32 = MmaCfg<32, 5, 2>;
 using Cfg64 = MmaCfg<64, 4, 2>;
+using Cfg96x2 = MmaCfg<96, 4, 1, 2>;
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -381,16 +389,19 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&sm.full[s], a_tx_bytes * uint32_t(nck));
+      mbar_arrive_expect_tx(&sm.full[s], a_tx_bytes * uint32_t(nck * C::MB));
       for (int j = 0; j < nck; ++j) {
         const int kc = kc0 + j;
-        if (!m.down) {
-          const int y = (sh ? 0 : m.e * a.I) + m.blk * 64;
-          tma_load_2d(sm.a[s][j], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full[s], pol);
-          tma_load_2d(sm.a[s][j] + kABytes / 2, sh ? &maps.sh_up : &maps.up, kc * kKC, y, &sm.full[s], pol);
-        } else {
-          const int y = (sh ? 0 : m.e * a.H) + m.blk * kBM;
-          tma_load_2d(sm.a[s][j], sh ? &maps.sh_down : &maps.down, kc * kKC, y, &sm.full[s], pol);
+#pragma unroll
+        for (int mb = 0; mb < C::MB; ++mb) {
+          if (!m.down) {
+            const int y = (sh ? 0 : m.e * a.I) + (m.blk * C::MB + mb) * 64;
+            tma_load_2d(sm.a[s][j][mb], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full[s], pol);
+            tma_load_2d(sm.a[s][j][mb] + kABytes / 2, sh ? &maps.sh_up : &maps.up, kc * kKC, y, &sm.full[s], pol);
+          } else {
+            const int y = (sh ? 0 : m.e * a.H) + (m.blk * C::MB + mb) * kBM;
+            tma_load_2d(sm.a[s][j][mb], sh ? &maps.sh_down : &maps.down, kc * kKC, y, &sm.full[s], pol);
+          }
         }
       }
       ++g;
@@ -430,7 +441,7 @@ __device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t t
       break;
     }
     tmem_fence_after();
-    const uint32_t d = tmem + uint32_t(acc) * C::ACC_COLS;
+    const uint32_t d = tmem + uint32_t(acc) * C::BUF_COLS;
     // kind::mxf8f6f4, A E4M3 (or E2M1 for MXFP4 weights, format 5), B E4M3,
     // K-major, UE8M0 scales, N = npad, M = 128
     const uint32_t idesc = (1u << 23) | (uint32_t(m.npad >> 3) << 17) | (uint32_t(kBM >> 4) << 24) |
@@ -448,18 +459,24 @@ __device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t t
       }
       tmem_fence_after();
       for (int j = 0; j < nck; ++j) {
+        // scale slot of the chunk: SFA of weight block mb at +8 mb (4 columns each), SFB at +16
         const uint32_t sfa = tmem + C::SCALE_COL0 + uint32_t(s) * C::SLOT_COLS + uint32_t(j) * kScaleSlotCols;
         const uint32_t sfb = sfa + 16;
         // the chunk's scale words into TMEM (in issue order before the MMAs that read them)
-        tmem_cp_32x128b_x4(sfa, sf_desc(smem_u32(sm.sfa[s][j])));
-        tmem_cp_32x128b_x4(sfb, sf_desc(smem_u32(sm.sfb[s][j])));
-        const uint64_t adesc = sw128_desc(smem_u32(sm.a[s][j])), bdesc = sw128_desc(smem_u32(sm.b[s][j]));
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          // +32 bytes of K per step: +2 in the descriptor's 16-byte start-address field
-          mma_mxf8(d, adesc + uint64_t(2 * k4), bdesc + uint64_t(2 * k4),
-                   idesc | (uint32_t(k4) << 4) | (uint32_t(k4) << 29), sfa, sfb,
-                   (kc0 + j + k4) != 0 ? 1u : 0u);
+        for (int mb = 0; mb < C::MB; ++mb) tmem_cp_32x128b_x4(sfa + 8u * mb, sf_desc(smem_u32(sm.sfa[s][j][mb])));
+        tmem_cp_32x128b_x4(sfb, sf_desc(smem_u32(sm.sfb[s][j])));
+        const uint64_t bdesc = sw128_desc(smem_u32(sm.b[s][j]));
+#pragma unroll
+        for (int mb = 0; mb < C::MB; ++mb) {
+          const uint64_t adesc = sw128_desc(smem_u32(sm.a[s][j][mb]));
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            // +32 bytes of K per step: +2 in the descriptor's 16-byte start-address field
+            mma_mxf8(d + uint32_t(mb) * C::ACC_COLS, adesc + uint64_t(2 * k4), bdesc + uint64_t(2 * k4),
+                     idesc | (uint32_t(k4) << 4) | (uint32_t(k4) << 29), sfa + 8u * mb, sfb,
+                     (kc0 + j + k4) != 0 ? 1u : 0u);
+          }
         }
       }
       mma_commit(&sm.empty[s]);
@@ -485,16 +502,16 @@ __device__ void mma_issuer(const ExpertArgs &a, typename C::Smem &sm, uint32_t t
 // on that stage's full barrier (fence.proxy.async first: the copies were written
 // through the generic proxy, the MMA reads through the async proxy).
 
-template <int NMAX>
+template <int NMAX, int MB>
 struct LoaderRows {
   const uint8_t *b[NMAX / 16];  // row i: token (pair) row r = tau/8 + 16 i of the chunk, its K-major codes
-  const uint8_t *sfa;   // scale row of weight row tau
-  const uint8_t *sfb;   // scale row of token row tau (or NULL past the chunk)
+  const uint8_t *sfa[MB];  // scale row of weight row tau of each weight block
+  const uint8_t *sfb;      // scale row of token row tau (or NULL past the chunk)
 };
 
-template <int NMAX>
-__device__ __forceinline__ LoaderRows<NMAX> loader_rows(const ExpertArgs &a, int T, const MUnit &m, int tau) {
-  LoaderRows<NMAX> lr;
+template <int NMAX, int MB>
+__device__ __forceinline__ LoaderRows<NMAX, MB> loader_rows(const ExpertArgs &a, int T, const MUnit &m, int tau) {
+  LoaderRows<NMAX, MB> lr;
   const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
   const int64_t tk = int64_t(T) * a.k;
   const int r0 = tau >> 3;
@@ -513,20 +530,23 @@ __device__ __forceinline__ LoaderRows<NMAX> loader_rows(const ExpertArgs &a, int
     lr.sfb = m.down ? a.hs + p * (a.I / kGroup) : a.xs + (p < tk ? p / a.k : p - tk) * (a.H / kGroup);
   }
   const bool sh = m.e == a.E;
-  if (!m.down) {
-    const int64_t row = int64_t(m.blk) * 64 + (tau & 63);
-    const uint8_t *base = tau < 64 ? (sh ? a.sh_s_gate : a.s_gate) : (sh ? a.sh_s_up : a.s_up);
-    lr.sfa = base + ((sh ? 0 : int64_t(m.e) * a.I) + row) * (a.H / kGroup);
-  } else {
-    const int64_t row = int64_t(m.blk) * kBM + tau;
-    lr.sfa = (sh ? a.sh_s_down : a.s_down) + ((sh ? 0 : int64_t(m.e) * a.H) + row) * (a.I / kGroup);
+#pragma unroll
+  for (int mb = 0; mb < MB; ++mb) {
+    if (!m.down) {
+      const int64_t row = int64_t(m.blk * MB + mb) * 64 + (tau & 63);
+      const uint8_t *base = tau < 64 ? (sh ? a.sh_s_gate : a.s_gate) : (sh ? a.sh_s_up : a.s_up);
+      lr.sfa[mb] = base + ((sh ? 0 : int64_t(m.e) * a.I) + row) * (a.H / kGroup);
+    } else {
+      const int64_t row = int64_t(m.blk * MB + mb) * kBM + tau;
+      lr.sfa[mb] = (sh ? a.sh_s_down : a.s_down) + ((sh ? 0 : int64_t(m.e) * a.H) + row) * (a.I / kGroup);
+    }
   }
   return lr;
 }
 
 // Issue the copies of stage slot s for K chunks kc0 .. kc0 + nck - 1 (one cp.async group).
 template <class C>
-__device__ __forceinline__ void loader_issue(typename C::Smem &sm, const MUnit &m, const LoaderRows<C::NMAX> &lr,
+__device__ __forceinline__ void loader_issue(typename C::Smem &sm, const MUnit &m, const LoaderRows<C::NMAX, C::MB> &lr,
                                              int s, int kc0, int nck, int tau, const void *zero_src) {
   const int c8 = tau & 7, r0 = tau >> 3;
   const int w = (tau & 31) * 4 + (tau >> 5);  // TMEM image order
@@ -544,7 +564,8 @@ __device__ __forceinline__ void loader_issue(typename C::Smem &sm, const MUnit &
                          v ? 16u : 0u);
       }
     }
-    cp_async4_zfill(&sm.sfa[s][j][w], lr.sfa + kc * 4, 4u);
+#pragma unroll
+    for (int mb = 0; mb < C::MB; ++mb) cp_async4_zfill(&sm.sfa[s][j][mb][w], lr.sfa[mb] + kc * 4, 4u);
     cp_async4_zfill(&sm.sfb[s][j][w], lr.sfb ? lr.sfb + kc * 4 : zero_src, lr.sfb ? 4u : 0u);
   }
   cp_async_commit();
@@ -607,7 +628,7 @@ __device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, in
     ++gc;
   };
   MUnit m;
-  LoaderRows<C::NMAX> lr;
+  LoaderRows<C::NMAX, C::MB> lr;
   int kc = 0, kcs = 0;
   uint32_t next = 0;  // queue entries read
   while (true) {
@@ -625,7 +646,7 @@ __device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, in
         while (gc < g) complete_oldest();
         if (!wait_chunk_ready(a, m.chunk, uint32_t(mbg), m.u)) break;
       }
-      lr = loader_rows<C::NMAX>(a, T, m, tau);
+      lr = loader_rows<C::NMAX, C::MB>(a, T, m, tau);
       kc = 0;
       kcs = (m.down ? a.I : a.H) / kKC;
     }
@@ -653,27 +674,36 @@ __device__ void mma_loaders(const ExpertArgs &a, int T, typename C::Smem &sm, in
 
 // ------------------------------------------------------------------ epilogue (warps 6-9)
 
+// Pair id of accumulator column col (0 .. NMAX - 1): lane l of the warp holds
+// the pair ids of columns l, 32 + l, 64 + l in prs[0], prs[1], prs[2].
+template <int NPR>
+__device__ __forceinline__ int pair_of_col(const int (&prs)[NPR], int col) {
+  int src = prs[0];
+  if constexpr (NPR == 2) src = col < 32 ? prs[0] : prs[1];
+  if constexpr (NPR == 3) src = col < 32 ? prs[0] : (col < 64 ? prs[1] : prs[2]);
+  return __shfl_sync(0xFFFFFFFFu, src, col & 31);
+}
+
 template <class C>
-__device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, uint32_t tmem, int n_chunks, int mbg,
-                             int hbd) {
+__device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ew = warp - kWarpEpi;
   const int et = ew * 32 + lane;
   const int64_t tk = int64_t(T) * a.k;
   const uint32_t target = uint32_t(a.k + a.shared);
   const float lim = a.swiglu_limit;
-  uint32_t nu = 0, xc = 0;  // units done, gate/up column slices done
-  static_assert(C::NMAX <= 64, "at most two pair ids per lane");
+  const int hcb = a.H / kBM;  // combine blocks (128 columns of y) per token row
+  uint32_t nu = 0, xc = 0;    // units done, gate/up column slices done
   for (uint32_t i = 0;; ++i) {
     const MUnit m = queue_pop<C>(a, sm, i);
     // every epilogue thread read the same entry (or timed out): they leave together
     if (!bar_and(kBarEpi, kEpiThreads, m.e >= 0 ? 1 : 0)) break;
     const int acc = int(nu & 1u);
     const uint32_t aph = (nu >> 1) & 1u;
-    // pair id of column `lane` (and 32 + lane) of the chunk (-1 past its end), loaded before the wait
+    // pair ids of columns lane, 32 + lane, ... of the chunk (-1 past its end), loaded before the wait
     const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
-    const int pr = lane < m.n ? __ldcg(rows + lane) : -1;
-    int pr2 = -1;
-    if constexpr (C::NMAX > 32) pr2 = 32 + lane < m.n ? __ldcg(rows + 32 + lane) : -1;
+    int prs[C::NPR];
+#pragma unroll
+    for (int r = 0; r < C::NPR; ++r) prs[r] = 32 * r + lane < m.n ? __ldcg(rows + 32 * r + lane) : -1;
     int ok = !aborted(a);
     if (ok) {
       int64_t waited = 0;
@@ -682,44 +712,43 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
     }
     if (!bar_and(kBarEpi, kEpiThreads, ok)) break;
     tmem_fence_after();
-    const uint32_t ta = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc) * C::ACC_COLS;
     const int slices = m.npad / 16;
     if (!m.down) {
-      // lanes of quadrants 0, 1 hold gate rows 64b + 32q + lane; quadrants 2, 3 the up rows
-      for (int j = 0; j < slices; ++j, ++xc) {
-        float v[16];
-        tmem_ld16(ta + uint32_t(16 * j), v);
-        uint16_t(*xb)[64] = sm.xchg[xc & 1u];
-        if (q >= 2) {
+      // Per weight block mb (64 rows of I): lanes of quadrants 0, 1 hold gate
+      // rows 64 blk + 32 q + lane; quadrants 2, 3 the up rows.
+#pragma unroll 1
+      for (int mb = 0; mb < C::MB; ++mb) {
+        const uint32_t ta = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc) * C::BUF_COLS + uint32_t(mb) * C::ACC_COLS;
+        const int blk = m.blk * C::MB + mb;
+        for (int j = 0; j < slices; ++j, ++xc) {
+          float v[16];
+          tmem_ld16(ta + uint32_t(16 * j), v);
+          uint16_t(*xb)[64] = sm.xchg[xc & 1u];
+          if (q >= 2) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) xb[c][32 * (q - 2) + lane] = float_to_bf16_bits(v[c]);
-        }
-        named_bar(kBarEpi, kEpiThreads);
-        if (q < 2) {
-          const int64_t col = int64_t(m.blk) * 64 + 32 * q + lane;
+            for (int c = 0; c < 16; ++c) xb[c][32 * (q - 2) + lane] = float_to_bf16_bits(v[c]);
+          }
+          named_bar(kBarEpi, kEpiThreads);
+          if (q < 2) {
+            const int64_t col = int64_t(blk) * 64 + 32 * q + lane;
 #pragma unroll 4
-          for (int c = 0; c < 16; ++c) {
-            int p;
-            if constexpr (C::NMAX > 32) {
-              const int col = 16 * j + c;
-              p = __shfl_sync(0xFFFFFFFFu, col < 32 ? pr : pr2, col & 31);
-            } else {
-              p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
+            for (int c = 0; c < 16; ++c) {
+              const int p = pair_of_col<C::NPR>(prs, 16 * j + c);
+              if (p < 0) continue;  // the same for the whole warp
+              float gb = bf16_bits_to_float(float_to_bf16_bits(v[c]));
+              float ub = bf16_bits_to_float(xb[c][32 * q + lane]);
+              if (lim > 0.0f) {  // clipped SwiGLU
+                gb = fminf(gb, lim);
+                ub = fminf(fmaxf(ub, -lim), lim);
+              }
+              const float silu = gb / (1.0f + expf(-gb));
+              const uint16_t hb = float_to_bf16_bits(silu * ub);
+              const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, uint32_t(hb) & 0x7FFFu);
+              const uint32_t code = mx_scale_code(bf16_bits_to_float(uint16_t(amax)));
+              a.hq[int64_t(p) * a.I + col] = float_to_e4m3(mx_unscale(bf16_bits_to_float(hb), code));
+              if (lane == 0) a.hs[int64_t(p) * (a.I / kGroup) + blk * 2 + q] = uint8_t(code);
+              if (a.h_bf16) a.h_bf16[int64_t(p) * a.I + col] = hb;
             }
-            if (p < 0) continue;  // the same for the whole warp
-            float gb = bf16_bits_to_float(float_to_bf16_bits(v[c]));
-            float ub = bf16_bits_to_float(xb[c][32 * q + lane]);
-            if (lim > 0.0f) {  // clipped SwiGLU
-              gb = fminf(gb, lim);
-              ub = fminf(fmaxf(ub, -lim), lim);
-            }
-            const float silu = gb / (1.0f + expf(-gb));
-            const uint16_t hb = float_to_bf16_bits(silu * ub);
-            const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, uint32_t(hb) & 0x7FFFu);
-            const uint32_t code = mx_scale_code(bf16_bits_to_float(uint16_t(amax)));
-            a.hq[int64_t(p) * a.I + col] = float_to_e4m3(mx_unscale(bf16_bits_to_float(hb), code));
-            if (lane == 0) a.hs[int64_t(p) * (a.I / kGroup) + m.blk * 2 + q] = uint8_t(code);
-            if (a.h_bf16) a.h_bf16[int64_t(p) * a.I + col] = hb;
           }
         }
       }
@@ -735,20 +764,18 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
         }
       }
     } else {
-      const int64_t h = int64_t(m.blk) * kBM + 32 * q + lane;
-      for (int j = 0; j < slices; ++j) {
-        float v[16];
-        tmem_ld16(ta + uint32_t(16 * j), v);
+#pragma unroll 1
+      for (int mb = 0; mb < C::MB; ++mb) {
+        const uint32_t ta = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc) * C::BUF_COLS + uint32_t(mb) * C::ACC_COLS;
+        const int64_t h = int64_t(m.blk * C::MB + mb) * kBM + 32 * q + lane;
+        for (int j = 0; j < slices; ++j) {
+          float v[16];
+          tmem_ld16(ta + uint32_t(16 * j), v);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          int p;
-          if constexpr (C::NMAX > 32) {
-            const int col = 16 * j + c;
-            p = __shfl_sync(0xFFFFFFFFu, col < 32 ? pr : pr2, col & 31);
-          } else {
-            p = __shfl_sync(0xFFFFFFFFu, pr, 16 * j + c);
+          for (int c = 0; c < 16; ++c) {
+            const int p = pair_of_col<C::NPR>(prs, 16 * j + c);
+            if (p >= 0) a.o[int64_t(p) * a.H + h] = v[c];
           }
-          if (p >= 0) a.o[int64_t(p) * a.H + h] = v[c];
         }
       }
       tmem_fence_before();
@@ -757,28 +784,37 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
       // thread's fence orders every warp's o stores of the unit before its count.
       // The last of a row's k (+ shared) pairs queues the row's combine.
       named_bar(kBarEpi, kEpiThreads);
-      // epilogue warp 0 counts columns 0-31, warp 1 columns 32-63
-      const int pc = ew == 0 ? pr : (C::NMAX > 32 && ew == 1 ? pr2 : -1);
-      if (pc >= 0) {
-        const int t = int(pc < tk ? pc / a.k : pc - tk);
-        __threadfence();
-        if (atomicAdd(a.comb_cnt + int64_t(t) * hbd + m.blk, 1u) == target - 1u) {
-          const uint32_t idx = atomicAdd(&sm.n_jobs, 1u);
-          sm.jobs[idx] = uint32_t(t);
+      // epilogue warp w counts columns 32 w .. 32 w + 31
+      int pc = ew == 0 ? prs[0] : -1;
+      if constexpr (C::NPR == 2) pc = ew == 0 ? prs[0] : (ew == 1 ? prs[1] : -1);
+      if constexpr (C::NPR == 3) pc = ew == 0 ? prs[0] : (ew == 1 ? prs[1] : (ew == 2 ? prs[2] : -1));
+#pragma unroll 1
+      for (int mb = 0; mb < C::MB; ++mb) {
+        const int blk = m.blk * C::MB + mb;
+        if (pc >= 0) {
+          const int t = int(pc < tk ? pc / a.k : pc - tk);
+          __threadfence();
+          if (atomicAdd(a.comb_cnt + int64_t(t) * hcb + blk, 1u) == target - 1u) {
+            const uint32_t idx = atomicAdd(&sm.n_jobs, 1u);
+            sm.jobs[idx] = uint32_t(t);
+          }
+        }
+        named_bar(kBarEpi, kEpiThreads);
+        const uint32_t nj = *reinterpret_cast<volatile uint32_t *>(&sm.n_jobs);
+        if (nj) {
+          __threadfence();  // the other pairs' o stores, before these reads
+          for (uint32_t jj = uint32_t(ew); jj < nj; jj += 4) {
+            const int t = int(sm.jobs[jj]);
+            uint16_t yb[kBM / 32];
+            combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, T, a.k, a.shared, a.H, t, int64_t(blk) * kBM, lane, yb);
+          }
+        }
+        named_bar(kBarEpi, kEpiThreads);
+        if (et == 0) sm.n_jobs = 0;
+        if constexpr (C::MB > 1) {
+          if (mb + 1 < C::MB) named_bar(kBarEpi, kEpiThreads);  // the reset, before the next block's counts
         }
       }
-      named_bar(kBarEpi, kEpiThreads);
-      const uint32_t nj = *reinterpret_cast<volatile uint32_t *>(&sm.n_jobs);
-      if (nj) {
-        __threadfence();  // the other pairs' o stores, before these reads
-        for (uint32_t jj = uint32_t(ew); jj < nj; jj += 4) {
-          const int t = int(sm.jobs[jj]);
-          uint16_t yb[kBM / 32];
-          combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, T, a.k, a.shared, a.H, t, int64_t(m.blk) * kBM, lane, yb);
-        }
-      }
-      named_bar(kBarEpi, kEpiThreads);
-      if (et == 0) sm.n_jobs = 0;
     }
     ++nu;
   }
@@ -834,7 +870,8 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
     T = td < 0 ? 0 : (td > a.Tmax ? a.Tmax : td);
   }
   const int n_chunks = __ldcg(a.n_chunks);
-  const int mbg = a.I / 64, hbd = a.H / kBM;
+  // units per chunk: gate/up units of MB x 64 rows of I, down units of MB x 128 rows of H
+  const int mbg = a.I / (64 * C::MB), hbd = a.H / (kBM * C::MB);
   if (warp == kWarpTma) {
     if (lane == 0) mma_producer<C>(maps, a, sm, n_chunks, mbg, hbd);
   } else if (warp == kWarpMma) {
@@ -842,7 +879,7 @@ __global__ void __launch_bounds__(kMThreads, 1) experts_mma_kernel(const __grid_
   } else if (warp < kWarpEpi) {
     mma_loaders<C>(a, T, sm, n_chunks, mbg, hbd);
   } else {
-    mma_epilogue<C>(a, T, sm, tmem, n_chunks, mbg, hbd);
+    mma_epilogue<C>(a, T, sm, tmem);
   }
   __syncwarp();
   tmem_fence_before();
@@ -937,15 +974,17 @@ cudaError_t launch_cfg(const MmaMaps &maps, const ExpertArgs &a, int grid, cudaS
 // Chunk size. A chunk never holds more rows than the step (an expert has at
 // most T rows), so T <= 16 uses 16-row chunks, up to 128 rows 32-row chunks
 // (a 5-stage ring). Above 128 rows the hot experts hold many rows, and each
-// chunk lands the expert's weight tiles in shared memory again: 64-row chunks
-// (a 4-stage ring) land fewer bytes, which pays there (384 rows with Zipf
-// routing: 1,199 -> 1,185 us per step). 128-row chunks leave too few stages.
-int mma_chunk_rows(int T) { return T <= 16 ? 16 : (T <= 128 ? 32 : 64); }
+// chunk lands the expert's weight tiles in shared memory again, and each unit
+// lands the chunk's token tile again: 96-row chunks with two 128-row weight
+// blocks per unit (sharing one token tile; a 4-stage ring) land the fewest
+// bytes, when H is a multiple of 256; otherwise 64-row chunks with one block.
+int mma_chunk_rows(int T, int H) { return T <= 16 ? 16 : (T <= 128 ? 32 : (H % 256 == 0 ? 96 : 64)); }
 
 cudaError_t prepare_experts_mma() {
   cudaError_t e = prepare_cfg<Cfg16>();
   if (e == cudaSuccess) e = prepare_cfg<Cfg32>();
   if (e == cudaSuccess) e = prepare_cfg<Cfg64>();
+  if (e == cudaSuccess) e = prepare_cfg<Cfg96x2>();
   return e;
 }
 
@@ -954,6 +993,7 @@ cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int gri
     case 16: return launch_cfg<Cfg16>(maps, a, grid, st);
     case 32: return launch_cfg<Cfg32>(maps, a, grid, st);
     case 64: return launch_cfg<Cfg64>(maps, a, grid, st);
+    case 96: return launch_cfg<Cfg96x2>(maps, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -18,7 +18,7 @@ constexpr int kStages = 5;              // pipeline depth
 constexpr int kRouteThreads = 1024;     // route kernel: block 0 (router + placement)
 constexpr int kQuantThreads = 256;      // route kernel: x-quantisation blocks (one group per thread)
 constexpr int kMaxTimedCalls = 4096;
-constexpr int kChunkRowsMax = 32;       // tensor-core expert kernel: most token rows per chunk (MMA N)
+constexpr int kChunkRowsMax = 96;       // tensor-core expert kernel: most token rows per chunk (MMA N)
 constexpr int kMmaDownRows = 128;       // tensor-core expert kernel: W_down rows per down unit
 constexpr int kMmaMinRowsDefault = 1;   // steps with at least this many rows take the tensor-core kernel
 constexpr int kRouterExperts = 8;       // route kernel: experts per router-projection block
@@ -35,7 +35,7 @@ struct Scratch {
   int32_t *rows_of;     // [E + 1][Tmax] pair ids in rank order
   int32_t *tile_list;   // [n_tiles_max] (expert << 16) | tile
   int32_t *n_tiles;     // [1]
-  int32_t *chunk_list;  // [n_tiles_max] (expert << 16) | chunk, chunks of <= mma_chunk_rows(T) rows
+  int32_t *chunk_list;  // [n_tiles_max] (expert << 16) | chunk, chunks of <= mma_chunk_rows(T, H) rows
   int32_t *n_chunks;    // [1]
   uint32_t *ready;      // [n_tiles_max] gate/up units finished per tile (per chunk on the tensor-core path)
   uint32_t *comb_cnt;   // [Tmax][down blocks] down blocks of a token row finished (fused combine)
@@ -125,7 +125,7 @@ struct ExpertArgs {
   const int32_t *rows_of;
   const int32_t *tile_list;
   const int32_t *n_tiles;
-  const int32_t *chunk_list;  // tensor-core kernel: chunks of <= mma_chunk_rows(T) rows per expert
+  const int32_t *chunk_list;  // tensor-core kernel: chunks of <= mma_chunk_rows(T, H) rows per expert
   const int32_t *n_chunks;
   const uint8_t *xq, *xs;
   uint8_t *hq, *hs;
@@ -176,7 +176,7 @@ moe_status_t guard_host(const moe_config_t &c, const moe_weights_t &w);
 // Tensor-core expert kernel (tcgen05 block-scaled MXFP8 MMA).
 bool experts_mma_shape_supported(int H, int I);
 bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *maps);
-int mma_chunk_rows(int T);
+int mma_chunk_rows(int T, int H);
 cudaError_t prepare_experts_mma();
 cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int grid, int chunk_rows, cudaStream_t st);
 

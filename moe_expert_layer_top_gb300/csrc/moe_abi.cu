@@ -340,7 +340,7 @@ moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T
   ra.n_tiles = s.n_tiles;
   ra.chunk_list = mma ? s.chunk_list : nullptr;
   ra.n_chunks = s.n_chunks;
-  ra.chunk_rows = mma_chunk_rows(T);
+  ra.chunk_rows = mma_chunk_rows(T, c.hidden);
   ra.ready = s.ready;
   ra.n_tiles_max = p->n_tiles_max;
   ra.comb_cnt = s.comb_cnt;

@@ -147,6 +147,36 @@ def test_small_case_parity(case, path):
     g.close()
 
 
+# Tensor-core kernel only: more than 128 rows, where a unit covers two 128-row
+# weight blocks with 96-row chunks (H a multiple of 256), or one block with
+# 64-row chunks (H = 640); I = 384 gives three gate/up units per chunk.
+WIDE = [
+    # T, H, E, k, I, routing, shared, weights
+    (200, 512, 8, 2, 384, "zipf", 1, "mxfp8"),
+    (129, 768, 16, 4, 256, "zipf", 0, "mxfp8"),
+    (150, 640, 8, 2, 256, "zipf", 0, "mxfp8"),
+    (200, 512, 8, 2, 384, "zipf", 1, "mxfp4"),
+]
+
+
+@pytest.mark.parametrize("case", WIDE, ids=[f"T{c[0]}_H{c[1]}_I{c[4]}_sh{c[6]}_{c[7]}" for c in WIDE])
+def test_wide_unit_parity(case):
+    T, H, E, k, I, routing, shared, fmt = case
+    g = CudaStep(T, H, E, k, I, routing, shared, seed=50 + T, flags=abi.MOE_FLAG_PATH_MMA, fmt=fmt).run()
+    assert g.status_code == abi.MOE_OK, (abi.moe_status_string(g.status_code), g.diag)
+    get = oracle_experts(50 + T, E, H, I, fmt=fmt)
+    sh = oracle.expert_weights_from_synth(50 + T, "shared", H, I, fmt=fmt) if shared else None
+    r = oracle.moe_step(g.x_bits, g.lg, k, get, shared=sh)
+    check_routing_bit_exact(g, r)
+    check_xquant_bit_exact(g, r)
+    check_h_quantizer_bit_exact(g)
+    sg, su = oracle_abs_sums(r, T, k, get, sh)
+    check_h_close(g, r, np.arange(T * k + T * shared), sg, su)
+    assert rel_fro(g.t["o"], r["o"]) <= 1e-2
+    check_y(g.y_bits, r["y"])
+    g.close()
+
+
 SMALL4 = [
     # T, H, E, k, I, routing, shared, swiglu_limit
     (6, 512, 8, 2, 256, "uniform", 0, 0.0),
