@@ -100,6 +100,15 @@ typedef enum {
  * undefined for that step. The GPU does not fault or hang, and the next
  * moe_forward on a plan without this flag is unaffected. */
 
+#define MOE_FLAG_TEST_BOUNDS (1u << 9)
+/* Test hook of the bounds-checked build (libmoe_debug.so, compiled with
+ * -DMOE_DEBUG_BOUNDS): the expert kernel's checks see only half of the
+ * combine counters the step uses (T rows x the kernel's blocks per row), so a
+ * check trips at an index that is still inside the buffer, and the step
+ * reports MOE_ERR_DEVICE_BOUNDS (site 6 in the
+ * diagnostics). It shows the checks are live without any access out of
+ * bounds; y is undefined for that step. No effect in the normal build. */
+
 /* moe_config_t.weight_format */
 #define MOE_WEIGHTS_MXFP8 0u  /* E4M3 elements, UE8M0 scale per 32 along K */
 #define MOE_WEIGHTS_MXFP4 1u  /* E2M1 elements (two per byte, element 2i in the low nibble), UE8M0 per 32 */
@@ -317,8 +326,10 @@ moe_status_t moe_plan_status(void *plan, int32_t *status_out);
 
 /* Diagnostics of the last device-side error on this plan: 8 int64 words
  *   [0] site: 1 ready-counter wait, 2 pipeline full wait, 3 pipeline empty wait, 4 router,
- *       5 unit-queue wait (tensor-core expert kernel)
- *   [1] work unit, [2] tile (or ring stage), [3] value observed, [4] value expected,
+ *       5 unit-queue wait (tensor-core expert kernel), 6 bounds check (only in the
+ *       bounds-checked build, libmoe_debug.so)
+ *   [1] work unit (site 6: the id of the check), [2] tile (or ring stage),
+ *   [3] value observed (site 6: the index), [4] value expected (site 6: the limit),
  *   [5] ns waited, [6] SM cycles waited, [7] block index.
  * All zero when the last step had no device-side error. Synchronises the device. */
 moe_status_t moe_plan_diagnostics(void *plan, int64_t *out8);

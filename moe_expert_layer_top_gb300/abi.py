@@ -29,6 +29,7 @@ MOE_FLAG_TIMING = 1 << 0
 MOE_FLAG_PATH_GEMV = 1 << 1
 MOE_FLAG_PATH_MMA = 1 << 2
 MOE_FLAG_TEST_SKIP_READY = 1 << 8
+MOE_FLAG_TEST_BOUNDS = 1 << 9
 
 # Every function declared in include/moe.h.
 EXPORTED = (
@@ -108,7 +109,8 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """libmoe.so, or the bounds-checked libmoe_debug.so when MOE_DEBUG_BOUNDS=1."""
+    return _build.DEBUG_LIB_PATH if os.environ.get("MOE_DEBUG_BOUNDS") == "1" else _build.LIB_PATH
 
 
 def load(path: str | None = None):

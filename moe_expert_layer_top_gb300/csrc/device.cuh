@@ -48,7 +48,8 @@ struct WaitClock {
 
 // Diagnostic record of the first device-side error of a step (plan-owned, 8 words):
 // site, unit, tile, observed, expected, elapsed ns, elapsed cycles, block.
-enum DiagSite : int64_t { kDiagReadyWait = 1, kDiagFullWait = 2, kDiagEmptyWait = 3, kDiagRoute = 4, kDiagQueueWait = 5 };
+enum DiagSite : int64_t { kDiagReadyWait = 1, kDiagFullWait = 2, kDiagEmptyWait = 3, kDiagRoute = 4, kDiagQueueWait = 5,
+                          kDiagBounds = 6 };
 
 __device__ __forceinline__ void report_diag(int32_t *status, int64_t *diag, int32_t code, int64_t site, int64_t unit,
                                             int64_t tile, int64_t observed, int64_t expected, int64_t ns,
@@ -63,6 +64,29 @@ __device__ __forceinline__ void report_diag(int32_t *status, int64_t *diag, int3
     diag[6] = cycles;
     diag[7] = blockIdx.x;
   }
+}
+
+// ------------------------------------------------------------------ bounds checks
+// Built with -DMOE_DEBUG_BOUNDS (libmoe_debug.so), every global and shared
+// index the kernels compute is checked before its access: in_bounds(i, n)
+// is true when 0 <= i < n; otherwise it records MOE_ERR_DEVICE_BOUNDS with a
+// diagnostics record (site kDiagBounds, the check's id, the index, the limit)
+// and returns false, and the caller skips the access. No check traps. In the
+// normal build in_bounds is the constant true and adds no code.
+#ifdef MOE_DEBUG_BOUNDS
+constexpr bool kBoundsChecked = true;
+#else
+constexpr bool kBoundsChecked = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(int32_t *status, int64_t *diag, int check, int64_t i, int64_t n) {
+  if constexpr (kBoundsChecked) {
+    if (i < 0 || i >= n) {
+      report_diag(status, diag, MOE_ERR_DEVICE_BOUNDS, kDiagBounds, check, -1, i, n, 0, 0);
+      return false;
+    }
+  }
+  return true;
 }
 
 // ------------------------------------------------------------------ mbarrier

@@ -272,6 +272,7 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     if (u >= total) return -1;
     int down, tile, block;
     unit_coords<S>(u, n_tiles, down, tile, block);
+    if (!in_bounds(a.status, a.diag, 30, tile, a.n_tiles_max)) return -1;
     return __ldcg(a.tile_list + tile);
   };
   struct Fetch {
@@ -282,9 +283,19 @@ __device__ void producer(const ExpertArgs &a, ExpertSmem &sm, int n_tiles) {
     Fetch f{te, 0, 0};
     if (te < 0) return f;
     const int expert = te >> 16, tile_in = te & 0xFFFF;
+    if (!in_bounds(a.status, a.diag, 31, expert, a.E + 1)) {
+      f.te = -1;
+      return f;
+    }
     f.cnt = __ldcg(a.counts + expert);
     const int row = min(kTileRows * tile_in + (lane & 7), a.Tmax - 1);
     f.pair = __ldcg(a.rows_of + int64_t(expert) * a.Tmax + row);
+    if constexpr (kBoundsChecked) {  // a pair id outside [0, P) becomes 0 (reported for the tile's own rows)
+      if (f.pair < 0 || f.pair >= a.pairs_cap) {
+        if ((lane & 7) < f.cnt - kTileRows * tile_in) in_bounds(a.status, a.diag, 32, f.pair, a.pairs_cap);
+        f.pair = 0;
+      }
+    }
     return f;
   };
   auto publish = [&](uint32_t i, const Fetch &f) {
@@ -683,6 +694,9 @@ __device__ __forceinline__ void down_unit_done(const ExpertArgs &a, ExpertSmem &
   for (int r = 0; r < m.n; ++r) {
     const int64_t p = m.pairs[r];
     const int t = p < int64_t(a.T) * a.k ? int(p / a.k) : int(p - int64_t(a.T) * a.k);
+    if (!in_bounds(a.status, a.diag, 33, t, a.T) ||
+        !in_bounds(a.status, a.diag, 34, int64_t(t) * S::NBD + m.block, a.comb_cap))
+      continue;
     uint32_t before = 0;
     if (lane == 0) before = atomicAdd(a.comb_cnt + int64_t(t) * S::NBD + m.block, 1u);
     before = __shfl_sync(0xFFFFFFFFu, before, 0);

@@ -280,8 +280,16 @@ __device__ __forceinline__ MUnit decode_unit(const ExpertArgs &a, int u, int n_c
     nb = hbd;
   }
   const int ci0 = u / nb;  // a chunk of the unit's expert
+  if (!in_bounds(a.status, a.diag, 10, ci0, a.n_tiles_max)) {
+    m.u = m.e = -1;
+    return m;
+  }
   const int ent = __ldcg(a.chunk_list + ci0);
   m.e = ent >> 16;
+  if (!in_bounds(a.status, a.diag, 11, m.e, a.E + 1)) {
+    m.u = m.e = -1;
+    return m;
+  }
   const int cbase = ci0 - (ent & 0xFFFF);  // the expert's first chunk
   const int cnt = __ldcg(a.counts + m.e);
   m.nch = (cnt + NMAX - 1) / NMAX;
@@ -293,6 +301,11 @@ __device__ __forceinline__ MUnit decode_unit(const ExpertArgs &a, int u, int n_c
   m.start = c * cs;
   m.n = min(cs, cnt - m.start);
   m.npad = (m.n + 15) & ~15;
+  if (!in_bounds(a.status, a.diag, 12, m.chunk, a.n_tiles_max) ||
+      !in_bounds(a.status, a.diag, 13, int64_t(m.start) + m.n - 1, a.Tmax) ||
+      !in_bounds(a.status, a.diag, 14, m.n - 1, NMAX)) {
+    m.u = m.e = -1;
+  }
   return m;
 }
 
@@ -396,10 +409,12 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
         for (int mb = 0; mb < C::MB; ++mb) {
           if (!m.down) {
             const int y = (sh ? 0 : m.e * a.I) + (m.blk * C::MB + mb) * 64;
+            if (!in_bounds(a.status, a.diag, 15, y, int64_t(sh ? 1 : a.E) * a.I - 63)) continue;
             tma_load_2d(sm.a[s][j][mb], sh ? &maps.sh_gate : &maps.gate, kc * kKC, y, &sm.full[s], pol);
             tma_load_2d(sm.a[s][j][mb] + kABytes / 2, sh ? &maps.sh_up : &maps.up, kc * kKC, y, &sm.full[s], pol);
           } else {
             const int y = (sh ? 0 : m.e * a.H) + (m.blk * C::MB + mb) * kBM;
+            if (!in_bounds(a.status, a.diag, 16, y, int64_t(sh ? 1 : a.E) * a.H - (kBM - 1))) continue;
             tma_load_2d(sm.a[s][j][mb], sh ? &maps.sh_down : &maps.down, kc * kKC, y, &sm.full[s], pol);
           }
         }
@@ -521,24 +536,30 @@ __device__ __forceinline__ LoaderRows<NMAX, MB> loader_rows(const ExpertArgs &a,
     lr.b[i] = nullptr;
     if (r < m.n) {
       const int64_t p = __ldcg(rows + r);
-      lr.b[i] = m.down ? a.hq + p * a.I : a.xq + (p < tk ? p / a.k : p - tk) * a.H;
+      const int64_t t = p < tk ? p / a.k : p - tk;
+      if (in_bounds(a.status, a.diag, 17, p, a.pairs_cap) && in_bounds(a.status, a.diag, 18, t, a.Tmax))
+        lr.b[i] = m.down ? a.hq + p * a.I : a.xq + t * a.H;
     }
   }
   lr.sfb = nullptr;
   if (tau < m.n) {
     const int64_t p = __ldcg(rows + tau);
-    lr.sfb = m.down ? a.hs + p * (a.I / kGroup) : a.xs + (p < tk ? p / a.k : p - tk) * (a.H / kGroup);
+    const int64_t t = p < tk ? p / a.k : p - tk;
+    if (in_bounds(a.status, a.diag, 17, p, a.pairs_cap) && in_bounds(a.status, a.diag, 18, t, a.Tmax))
+      lr.sfb = m.down ? a.hs + p * (a.I / kGroup) : a.xs + t * (a.H / kGroup);
   }
   const bool sh = m.e == a.E;
 #pragma unroll
   for (int mb = 0; mb < MB; ++mb) {
     if (!m.down) {
-      const int64_t row = int64_t(m.blk * MB + mb) * 64 + (tau & 63);
+      int64_t row = (sh ? 0 : int64_t(m.e) * a.I) + int64_t(m.blk * MB + mb) * 64 + (tau & 63);
+      if (!in_bounds(a.status, a.diag, 19, row, int64_t(sh ? 1 : a.E) * a.I)) row = 0;
       const uint8_t *base = tau < 64 ? (sh ? a.sh_s_gate : a.s_gate) : (sh ? a.sh_s_up : a.s_up);
-      lr.sfa[mb] = base + ((sh ? 0 : int64_t(m.e) * a.I) + row) * (a.H / kGroup);
+      lr.sfa[mb] = base + row * (a.H / kGroup);
     } else {
-      const int64_t row = int64_t(m.blk * MB + mb) * kBM + tau;
-      lr.sfa[mb] = (sh ? a.sh_s_down : a.s_down) + ((sh ? 0 : int64_t(m.e) * a.H) + row) * (a.I / kGroup);
+      int64_t row = (sh ? 0 : int64_t(m.e) * a.H) + int64_t(m.blk * MB + mb) * kBM + tau;
+      if (!in_bounds(a.status, a.diag, 20, row, int64_t(sh ? 1 : a.E) * a.H)) row = 0;
+      lr.sfa[mb] = (sh ? a.sh_s_down : a.s_down) + row * (a.I / kGroup);
     }
   }
   return lr;
@@ -703,7 +724,10 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
     const int32_t *rows = a.rows_of + int64_t(m.e) * a.Tmax + m.start;
     int prs[C::NPR];
 #pragma unroll
-    for (int r = 0; r < C::NPR; ++r) prs[r] = 32 * r + lane < m.n ? __ldcg(rows + 32 * r + lane) : -1;
+    for (int r = 0; r < C::NPR; ++r) {
+      prs[r] = 32 * r + lane < m.n ? __ldcg(rows + 32 * r + lane) : -1;
+      if (prs[r] >= 0 && !in_bounds(a.status, a.diag, 21, prs[r], a.pairs_cap)) prs[r] = -1;
+    }
     int ok = !aborted(a);
     if (ok) {
       int64_t waited = 0;
@@ -794,17 +818,20 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
         if (pc >= 0) {
           const int t = int(pc < tk ? pc / a.k : pc - tk);
           __threadfence();
-          if (atomicAdd(a.comb_cnt + int64_t(t) * hcb + blk, 1u) == target - 1u) {
+          if (in_bounds(a.status, a.diag, 22, int64_t(t) * hcb + blk, a.comb_cap) &&
+              atomicAdd(a.comb_cnt + int64_t(t) * hcb + blk, 1u) == target - 1u) {
             const uint32_t idx = atomicAdd(&sm.n_jobs, 1u);
-            sm.jobs[idx] = uint32_t(t);
+            if (in_bounds(a.status, a.diag, 23, idx, C::NMAX)) sm.jobs[idx] = uint32_t(t);
           }
         }
         named_bar(kBarEpi, kEpiThreads);
-        const uint32_t nj = *reinterpret_cast<volatile uint32_t *>(&sm.n_jobs);
+        uint32_t nj = *reinterpret_cast<volatile uint32_t *>(&sm.n_jobs);
+        if constexpr (kBoundsChecked) nj = min(nj, uint32_t(C::NMAX));  // entries past NMAX were not stored
         if (nj) {
           __threadfence();  // the other pairs' o stores, before these reads
           for (uint32_t jj = uint32_t(ew); jj < nj; jj += 4) {
             const int t = int(sm.jobs[jj]);
+            if (!in_bounds(a.status, a.diag, 24, t, T)) continue;
             uint16_t yb[kBM / 32];
             combine_row_block<kBM / 32>(a.o, a.topk_w, a.y, T, a.k, a.shared, a.H, t, int64_t(blk) * kBM, lane, yb);
           }

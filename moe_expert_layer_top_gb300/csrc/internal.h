@@ -71,6 +71,7 @@ struct Plan {
   int words;             // ceil(max_rows / 32)
   int n_tiles_max;       // upper bound on tiles in a step
   int64_t pairs_max;     // P for T = max_rows
+  int comb_per_row_max;  // combine counters per token row (the larger of the two expert kernels' block counts)
   int64_t timeout_ns;
   int mma_min_rows;      // steps with T >= this take the tensor-core expert kernel
   MmaMaps maps;
@@ -143,6 +144,10 @@ struct ExpertArgs {
   int skip_ready_tile;  // fault injection: tile index whose ready count is never published, or -1
   int fp4;              // weights are MXFP4 (E2M1) rather than MXFP8 (tensor-core kernel only)
   float swiglu_limit;   // clipped SwiGLU limit; <= 0: no clip
+  // Capacities for the bounds checks of a -DMOE_DEBUG_BOUNDS build (unused otherwise):
+  int n_tiles_max;      // entries of tile_list, chunk_list and ready
+  int64_t pairs_cap;    // rows of hq, hs, h_bf16 and o
+  int64_t comb_cap;     // entries of comb_cnt
 };
 
 // The residual-stream + RMSNorm + MXFP8 epilogue (residual_norm.cu), one block per token row.

@@ -208,6 +208,7 @@ moe_status_t moe_plan(const moe_config_t *config, const moe_weights_t *weights, 
   const size_t o_cl = take(size_t(p->n_tiles_max) * 4), o_nc = take(4);
   const size_t o_ready = take(size_t(p->n_tiles_max) * 4), o_work = take(16), o_status = take(4);
   const int down_blocks = experts_down_blocks(H, I) > H / kMmaDownRows ? experts_down_blocks(H, I) : H / kMmaDownRows;
+  p->comb_per_row_max = down_blocks;
   const size_t o_comb = take(size_t(Tm) * down_blocks * 4);
   const size_t o_diag = take(8 * 8);
   const size_t o_xq = take(size_t(Tm) * H), o_xs = take(size_t(Tm) * (H / 32));
@@ -397,6 +398,12 @@ moe_status_t enqueue_step(Plan *p, const void *x, const float *logits, int32_t T
   ea.skip_ready_tile = (c.flags & MOE_FLAG_TEST_SKIP_READY) ? 0 : -1;
   ea.fp4 = c.weight_format == MOE_WEIGHTS_MXFP4 ? 1 : 0;
   ea.swiglu_limit = c.swiglu_limit;
+  ea.n_tiles_max = p->n_tiles_max;
+  ea.pairs_cap = p->pairs_max;
+  ea.comb_cap = int64_t(c.max_rows) * p->comb_per_row_max;
+  // test hook of the bounds-checked build: the checks see half of the combine
+  // counters this step uses, so one trips at an index still inside the buffer
+  if (c.flags & MOE_FLAG_TEST_BOUNDS) ea.comb_cap = int64_t(T) * ra.comb_per_row / 2;
   const bool timed = (c.flags & MOE_FLAG_TIMING) && p->timed_calls < kMaxTimedCalls;
   if (timed && cudaEventRecord(p->ev_start[p->timed_calls], st) != cudaSuccess) return MOE_ERR_CUDA;
   const cudaError_t le = mma ? launch_experts_mma(p->maps, ea, p->num_sms, ra.chunk_rows, st) : launch_experts(ea, p->num_sms, st);

@@ -347,7 +347,8 @@ __device__ __forceinline__ void route_topk(const RouteArgs &a, int T, int rg, Ro
       const int id = sm.sel_i[warp][lane];
       a.topk_ids[int64_t(t) * k + lane] = id;
       a.topk_w[int64_t(t) * k + lane] = __fdiv_rn(e, s);
-      if (bm) atomicOr(&bm[id * W + (t >> 5)], 1u << (t & 31));
+      if (bm && in_bounds(a.status, a.diag, 1, int64_t(id) * W + (t >> 5), int64_t(E) * W))
+        atomicOr(&bm[id * W + (t >> 5)], 1u << (t & 31));
     }
     __syncwarp();
   }
@@ -393,7 +394,8 @@ __device__ void route_place(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *
     for (int p = tid; p < T * k; p += blockDim.x) {
       const int t = p / k;
       const int id = __ldcg(a.topk_ids + p);
-      atomicOr(&bm[id * W + (t >> 5)], 1u << (t & 31));
+      if (in_bounds(a.status, a.diag, 2, id, E) && in_bounds(a.status, a.diag, 3, t >> 5, W))
+        atomicOr(&bm[id * W + (t >> 5)], 1u << (t & 31));
     }
   }
   __syncthreads();
@@ -445,11 +447,12 @@ __device__ void route_place(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *
   for (int p = tid; p < T * k; p += blockDim.x) {
     const int t = p / k;
     const int e = __ldcg(a.topk_ids + p);
+    if (!in_bounds(a.status, a.diag, 2, e, E) || !in_bounds(a.status, a.diag, 3, t >> 5, W)) continue;
     const uint32_t *b = bm + e * W;
     int rank = __popc(b[t >> 5] & ((1u << (t & 31)) - 1u));
     for (int w = 0; w < (t >> 5); ++w) rank += __popc(b[w]);
     a.slot[p] = (e << 16) | rank;
-    a.rows_of[int64_t(e) * a.Tmax + rank] = p;
+    if (in_bounds(a.status, a.diag, 4, rank, a.Tmax)) a.rows_of[int64_t(e) * a.Tmax + rank] = p;
   }
   if (a.shared)
     for (int t = tid; t < T; t += blockDim.x) a.rows_of[int64_t(E) * a.Tmax + t] = T * k + t;

@@ -254,6 +254,9 @@ extern "C" moe_status_t moe_forward_static_scratch(const moe_config_t *config, c
   ea.skip_ready_tile = -1;
   ea.fp4 = 0;
   ea.swiglu_limit = c.swiglu_limit;
+  ea.n_tiles_max = n_tiles_max;
+  ea.pairs_cap = pairs_routed + int64_t(T) * c.num_shared;
+  ea.comb_cap = int64_t(T) * experts_down_blocks(c.hidden, c.intermediate);
   if (launch_experts(ea, num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   return MOE_OK;

@@ -38,6 +38,14 @@ def test_library_exports_every_declared_symbol(lib):
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
+def test_bounds_checked_library_exports_every_declared_symbol(lib):
+    """libmoe_debug.so (the -DMOE_DEBUG_BOUNDS build) has the same ABI."""
+    dbg = ctypes.CDLL(pkg.build.DEBUG_LIB_PATH)
+    for name in header_functions():
+        assert ctypes.cast(getattr(dbg, name), ctypes.c_void_p).value, name
+    assert dbg.moe_abi_version() == abi.MOE_ABI_VERSION
+
+
 def test_abi_version_and_status_strings(lib):
     assert lib.moe_abi_version() == abi.MOE_ABI_VERSION
     assert abi.moe_status_string(abi.MOE_OK) == "MOE_OK"

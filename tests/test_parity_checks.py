@@ -92,3 +92,23 @@ def test_binary32_silu_overflow_tail_inside_envelope():
     assert lo[0, 0] <= 0.0 <= hi[0, 0] and lo[0, 1] <= 0.0 <= hi[0, 1]
     exact = -20.0 / (1.0 + np.exp(20.0)) * 3.0
     assert not (lo[0, 2] <= 0.0 <= hi[0, 2]) and lo[0, 2] <= exact <= hi[0, 2]
+
+
+def test_pooled_oracle_equals_the_plain_step():
+    """full_oracle (the expert MLPs of several steps in spawned processes, as the
+    full-size GPU tests use it) gives exactly what oracle.moe_step gives."""
+    from gpu_cases import full_oracle
+    T, E, k = 40, 8, 2
+    x = synth.x_bf16(5, T, H)
+    lg = synth.router_logits(5, T, E, k, "zipf")
+    x2 = synth.x_bf16(6, 6, H)
+    lg2 = synth.router_logits(6, 6, E, k, "uniform")
+    ref, hashes = full_oracle(5, {"a": (x, lg, k, True), "b": (x2, lg2, k, False)}, H, I)
+    get = lambda e: oracle.expert_weights_from_synth(5, e, H, I)  # noqa: E731
+    sh = oracle.expert_weights_from_synth(5, "shared", H, I)
+    r = oracle.moe_step(x, lg, k, get, shared=sh)
+    for n in ("ids", "w", "xq", "xs", "g", "u", "h", "hq", "hs", "o", "y"):
+        np.testing.assert_array_equal(ref["a"][n], r[n])
+    np.testing.assert_array_equal(ref["b"]["y"], oracle.moe_step(x2, lg2, k, get)["y"])
+    import oracle_pool
+    assert hashes["shared"]["w_up"] == oracle_pool.sha256_of(sh.w_up)
