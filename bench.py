@@ -362,6 +362,17 @@ def time_gpu_workload(wl, weight_sets, steps, warmup, flush_buf, seed, flags=0):
         ends[i].record(stream)
     torch.cuda.synchronize()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # the same steps back to back, one event pair around all of them: consecutive
+    # steps overlap through programmatic dependent launch, as layers of a model would
+    b2b = None
+    if flush_buf is None:
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        for i in range(steps):
+            steps_[(warmup + i) % len(steps_)].forward(x, lg, y=y)
+        b_ev.record(stream)
+        torch.cuda.synchronize()
+        b2b = a_ev.elapsed_time(b_ev) / steps
     words = st_words.cpu().tolist()
     bad = [(i, w) for i, w in enumerate(words) if w != abi.MOE_OK]
     status = 0 if not bad else bad[0][1]
@@ -393,6 +404,7 @@ def time_gpu_workload(wl, weight_sets, steps, warmup, flush_buf, seed, flags=0):
     step_bytes = weight_bytes + wl.T * wl.H * 2 + wl.T * wl.E * 4 + wl.T * wl.H * 2
     res = {
         "ms_steps": per_step,
+        "ms_back_to_back": b2b,
         "ms_mean": sum(per_step) / len(per_step),
         "ms_median": statistics.median(per_step),
         "ms_min": min(per_step),
@@ -774,6 +786,7 @@ def run_gpu(args):
             "us_median": round(main["ms_median"] * 1e3, 3),
             "us_min": round(main["ms_min"] * 1e3, 3),
             "us_max": round(main["ms_max"] * 1e3, 3),
+            "us_back_to_back": None if main["ms_back_to_back"] is None else round(main["ms_back_to_back"] * 1e3, 3),
             "active_weight_mb": round(main["weight_bytes"] / 1e6, 1),
             "l2_mb": round(l2 / 1e6, 1),
             ("us_l2_flushed" if args.l2 != "flush" else "us_no_flush"): round(other["ms_mean"] * 1e3, 3),

@@ -175,6 +175,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 
 // ------------------------------------------------------------------ acquire / release on global counters
 
+// Moves `bytes` (a multiple of 16, from a 16-byte aligned address) of global
+// memory into L2 without waiting (an untiled bulk prefetch; no completion to track).
+__device__ __forceinline__ void l2_prefetch_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

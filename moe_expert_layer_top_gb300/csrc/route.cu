@@ -465,8 +465,21 @@ __device__ __host__ __forceinline__ int route_blocks(int T) { return (T + kRoute
 
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a) {
   extern __shared__ __align__(16) unsigned char route_smem[];
-  // Let the expert kernel's blocks get scheduled early; it waits for this grid before reading.
+  // Let the expert kernel's blocks get scheduled early; it waits for this grid
+  // before reading. Every block of this grid is running when it triggers, so
+  // the expert kernel's blocks cannot take the SMs this grid still needs.
   pdl_launch_dependents();
+  // This grid is itself launched behind the previous kernel on the stream
+  // (programmatic dependent launch): its blocks get scheduled while that
+  // kernel finishes. The router weight is a constant, so a projection block
+  // moves its 8 rows of W_r towards L2 first; everything else waits here
+  // for the previous kernel (x, the logits, and this plan's scratch that the
+  // previous step's expert kernel may still read).
+  if (a.w_router && !a.d_T && int(blockIdx.x) < route_blocks(a.T) * a.n_eblk) {
+    const int e = (int(blockIdx.x) % a.n_eblk) * kRouterExperts + int(threadIdx.x);  // one W_r row per thread
+    if (threadIdx.x < kRouterExperts && e < a.E) l2_prefetch_bulk(a.w_router + int64_t(e) * a.H, uint32_t(a.H) * 2u);
+  }
+  pdl_wait_primary();
   RouteSmem &sm = *reinterpret_cast<RouteSmem *>(route_smem);
   uint32_t *bm = reinterpret_cast<uint32_t *>(route_smem + sizeof(RouteSmem));
   const int tid = threadIdx.x;
@@ -573,9 +586,17 @@ int route_grid(int T, int H, int nproj) {
 }
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
-  const size_t smem = route_smem_bytes(a.E, a.words);
-  route_kernel<<<route_grid(a.T, a.H, a.w_router ? a.n_eblk : 1), kRouteThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(route_grid(a.T, a.H, a.w_router ? a.n_eblk : 1));
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = route_smem_bytes(a.E, a.words);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_kernel, a);
 }
 
 cudaError_t launch_quantize_fp4(const uint16_t *x, int64_t rows, int cols, uint8_t *q, uint8_t *s, cudaStream_t st) {
