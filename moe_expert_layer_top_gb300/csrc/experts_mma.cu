@@ -405,6 +405,15 @@ __device__ void mma_producer(const MmaMaps &maps, const ExpertArgs &a, typename 
       mbar_arrive_expect_tx(&sm.full[s], a_tx_bytes * uint32_t(nck * C::MB));
       for (int j = 0; j < nck; ++j) {
         const int kc = kc0 + j;
+        if (C::MB == 2 && !m.down) {
+          // gate rows 128 blk .. 128 blk + 127 into tile 0, the same rows of W_up into tile 1
+          const int y = (sh ? 0 : m.e * a.I) + m.blk * kBM;
+          if (in_bounds(a.status, a.diag, 15, y, int64_t(sh ? 1 : a.E) * a.I - (kBM - 1))) {
+            tma_load_2d(sm.a[s][j][0], sh ? &maps.sh_gate2 : &maps.gate2, kc * kKC, y, &sm.full[s], pol);
+            tma_load_2d(sm.a[s][j][C::MB - 1], sh ? &maps.sh_up2 : &maps.up2, kc * kKC, y, &sm.full[s], pol);
+          }
+          continue;
+        }
 #pragma unroll
         for (int mb = 0; mb < C::MB; ++mb) {
           if (!m.down) {
@@ -552,9 +561,13 @@ __device__ __forceinline__ LoaderRows<NMAX, MB> loader_rows(const ExpertArgs &a,
 #pragma unroll
   for (int mb = 0; mb < MB; ++mb) {
     if (!m.down) {
-      int64_t row = (sh ? 0 : int64_t(m.e) * a.I) + int64_t(m.blk * MB + mb) * 64 + (tau & 63);
+      // one block: rows 64 blk .. + 63 of W_gate then of W_up; two blocks: block 0 is
+      // rows 128 blk .. + 127 of W_gate, block 1 the same rows of W_up
+      int64_t row = (sh ? 0 : int64_t(m.e) * a.I) +
+                    (MB == 2 ? int64_t(m.blk) * kBM + tau : int64_t(m.blk * MB + mb) * 64 + (tau & 63));
       if (!in_bounds(a.status, a.diag, 19, row, int64_t(sh ? 1 : a.E) * a.I)) row = 0;
-      const uint8_t *base = tau < 64 ? (sh ? a.sh_s_gate : a.s_gate) : (sh ? a.sh_s_up : a.s_up);
+      const bool gate = MB == 2 ? mb == 0 : tau < 64;
+      const uint8_t *base = gate ? (sh ? a.sh_s_gate : a.s_gate) : (sh ? a.sh_s_up : a.s_up);
       lr.sfa[mb] = base + row * (a.H / kGroup);
     } else {
       int64_t row = (sh ? 0 : int64_t(m.e) * a.H) + int64_t(m.blk * MB + mb) * kBM + tau;
@@ -737,7 +750,44 @@ __device__ void mma_epilogue(const ExpertArgs &a, int T, typename C::Smem &sm, u
     if (!bar_and(kBarEpi, kEpiThreads, ok)) break;
     tmem_fence_after();
     const int slices = m.npad / 16;
-    if (!m.down) {
+    if (C::MB == 2 && !m.down) {
+      // Two-block gate/up unit: accumulator 0 holds gate rows 128 blk + 32 q + lane
+      // in this warp's TMEM lanes, accumulator 1 the same rows of the up
+      // projection. Every warp forms h for its 32 rows (one MXFP8 group) itself.
+      const uint32_t ta = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc) * C::BUF_COLS;
+      const int64_t col = int64_t(m.blk) * kBM + 32 * q + lane;
+      for (int j = 0; j < slices; ++j) {
+        float gv[16], uv[16];
+        tmem_ld16(ta + uint32_t(16 * j), gv);
+        tmem_ld16(ta + C::ACC_COLS + uint32_t(16 * j), uv);
+#pragma unroll 4
+        for (int c = 0; c < 16; ++c) {
+          const int p = pair_of_col<C::NPR>(prs, 16 * j + c);
+          if (p < 0) continue;  // the same for the whole warp
+          float gb = bf16_bits_to_float(float_to_bf16_bits(gv[c]));
+          float ub = bf16_bits_to_float(float_to_bf16_bits(uv[c]));
+          if (lim > 0.0f) {  // clipped SwiGLU
+            gb = fminf(gb, lim);
+            ub = fminf(fmaxf(ub, -lim), lim);
+          }
+          const float silu = gb / (1.0f + expf(-gb));
+          const uint16_t hb = float_to_bf16_bits(silu * ub);
+          const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, uint32_t(hb) & 0x7FFFu);
+          const uint32_t code = mx_scale_code(bf16_bits_to_float(uint16_t(amax)));
+          a.hq[int64_t(p) * a.I + col] = float_to_e4m3(mx_unscale(bf16_bits_to_float(hb), code));
+          if (lane == 0) a.hs[int64_t(p) * (a.I / kGroup) + m.blk * 4 + q] = uint8_t(code);
+          if (a.h_bf16) a.h_bf16[int64_t(p) * a.I + col] = hb;
+        }
+      }
+      tmem_fence_before();
+      mbar_arrive(&sm.acc_empty[acc]);
+      // every warp's h stores, then one release of the ready count
+      named_bar(kBarEpi, kEpiThreads);
+      if (et == 0 && m.chunk != a.skip_ready_tile) {
+        __threadfence();
+        red_release_gpu_add(a.ready + m.chunk, 1u);
+      }
+    } else if (!m.down) {
       // Per weight block mb (64 rows of I): lanes of quadrants 0, 1 hold gate
       // rows 64 blk + 32 q + lane; quadrants 2, 3 the up rows.
 #pragma unroll 1
@@ -965,11 +1015,15 @@ bool encode_mma_maps(const moe_config_t &c, const moe_weights_t &w, MmaMaps *map
   const bool f4 = c.weight_format == MOE_WEIGHTS_MXFP4;
   bool ok = encode_rows(enc, &maps->gate, w.w_gate, H, E * I, 64, f4) &&
             encode_rows(enc, &maps->up, w.w_up, H, E * I, 64, f4) &&
-            encode_rows(enc, &maps->down, w.w_down, I, E * H, kBM, f4);
+            encode_rows(enc, &maps->down, w.w_down, I, E * H, kBM, f4) &&
+            encode_rows(enc, &maps->gate2, w.w_gate, H, E * I, kBM, f4) &&
+            encode_rows(enc, &maps->up2, w.w_up, H, E * I, kBM, f4);
   if (ok && c.num_shared)
     ok = encode_rows(enc, &maps->sh_gate, w.sh_w_gate, H, I, 64, f4) &&
          encode_rows(enc, &maps->sh_up, w.sh_w_up, H, I, 64, f4) &&
-         encode_rows(enc, &maps->sh_down, w.sh_w_down, I, H, kBM, f4);
+         encode_rows(enc, &maps->sh_down, w.sh_w_down, I, H, kBM, f4) &&
+         encode_rows(enc, &maps->sh_gate2, w.sh_w_gate, H, I, kBM, f4) &&
+         encode_rows(enc, &maps->sh_up2, w.sh_w_up, H, I, kBM, f4);
   return ok;
 }
 

@@ -57,10 +57,11 @@ struct Scratch {
 
 // TMA tensor maps over the caller's weights (canonical layout, 128-byte swizzle),
 // for the tensor-core expert kernel. Boxes: 128 bytes of K x 64 rows (gate, up)
-// or x 128 rows (down).
+// or x 128 rows (down, and gate/up of the two-block units).
 struct MmaMaps {
-  CUtensorMap gate, up, down;           // rows: E*I, E*I, E*H
+  CUtensorMap gate, up, down;           // rows: E*I, E*I, E*H (boxes of 64, 64, 128 rows)
   CUtensorMap sh_gate, sh_up, sh_down;  // shared expert (zero when absent)
+  CUtensorMap gate2, up2, sh_gate2, sh_up2;  // the same gate/up rows in boxes of 128 (two-block units)
 };
 
 struct Plan {
@@ -105,7 +106,7 @@ struct RouteArgs {
   int32_t *n_tiles;
   int32_t *chunk_list;  // NULL: no chunk list (the GEMV expert kernel only)
   int32_t *n_chunks;
-  int chunk_rows;       // rows per chunk (16, 32 or 64)
+  int chunk_rows;       // rows per chunk (16, 32, 64 or 96)
   uint32_t *ready;
   int n_tiles_max;
   uint32_t *comb_cnt;
