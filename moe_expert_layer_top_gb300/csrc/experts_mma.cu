@@ -3,22 +3,27 @@
 //
 // The CUDA-core expert kernel streams an expert's weights once per 8-row tile,
 // so an expert with hundreds of rows re-reads them and spends CUDA-core FMAs
-// on every tile. Here each expert's rows are split into chunks of <= 16, 32 or
-// 64 rows, and one MMA per 32 K columns covers a whole chunk. The chunks of one
-// expert run side by side on neighbouring blocks and read each weight block
-// from HBM once (the others find it in L2). Tensor time is small next to the
-// weight stream, so the kernel stays bound by HBM, also at one token row.
+// on every tile. Here each expert's rows are split into chunks of <= 16, 32,
+// 64 or 96 rows, and one MMA per 32 K columns covers a whole chunk. The chunks
+// of one expert run side by side on neighbouring blocks and read each weight
+// block from HBM once (the others find it in L2). Tensor time is small next to
+// the weight stream, so the kernel stays bound by HBM, also at one token row.
 //
-// Work units, in the order the step counter hands them out:
-//   gate/up unit (chunk c, block b): rows [64b, 64b + 64) of W_gate and of W_up
-//       as the MMA's A operand (M = 128: 64 gate rows, then 64 up rows); the
-//       chunk's token rows of x (MXFP8) as B (N = rows rounded up to 16).
+// Work units, in the order the step counter hands them out (MB = 1 weight
+// block per unit for chunks of <= 64 rows, MB = 2 for the 96-row chunks):
+//   gate/up unit (chunk c, block b):
+//       MB = 1: rows [64b, 64b + 64) of W_gate and of W_up as the MMA's A
+//       operand (M = 128: 64 gate rows, then 64 up rows);
+//       MB = 2: rows [128b, 128b + 128) of W_gate as block 0 and the same rows
+//       of W_up as block 1 (two M = 128 MMAs per K step on one token tile);
+//       the chunk's token rows of x (MXFP8) as B (N = rows rounded up to 16).
 //       Epilogue: g, u -> bf16, h = bf16(silu(g) * u), h -> MXFP8 along I,
 //       one 32-group per warp. Then ready[c] is bumped.
-//   down unit (chunk c, block b): rows [128b, 128b + 128) of W_down as A; the
-//       chunk's rows of h (MXFP8) as B. It waits (bounded) until ready[c]
-//       counts every gate/up unit of c. Epilogue: o[pair][h] in fp32, then the
-//       fused combine of every (token row, block) this unit completes.
+//   down unit (chunk c, block b): rows [128 MB b, 128 MB (b + 1)) of W_down
+//       as A (MB blocks of 128 rows); the chunk's rows of h (MXFP8) as B. It
+//       waits (bounded) until ready[c] counts every gate/up unit of c.
+//       Epilogue: o[pair][h] in fp32, then the fused combine of every (token
+//       row, 128-row block) this unit completes.
 // Dynamic schedule: every block takes its next unit from the step's counter
 // when it is about to need it, so blocks that stream faster take more units
 // and all blocks finish within about one unit of each other (a static split of
@@ -31,17 +36,19 @@
 //   warp 0      TMA producer: one lane takes the block's units from the
 //               counter and queues them for the other roles; it loads the A
 //               tiles (128 bytes of K x 64 or 128 rows per box, 128-byte
-//               swizzle) into a ring of two K chunks per stage (5 stages
-//               with 16- and 32-row chunks, 4 with 64-row chunks).
+//               swizzle) into a ring of K chunks (5 stages of two chunks
+//               with 16- and 32-row chunks, 4 of two with 64-row chunks, 4 of
+//               one chunk of two weight blocks with 96-row chunks).
 //   warp 1      MMA issuer: one lane issues tcgen05.mma.kind::mxf8f6f4
-//               .block_scale (4 per stage, K = 32 each) into one of two TMEM
-//               accumulators and commits each stage back to the ring.
+//               .block_scale (K = 32 each, 4 per K chunk and weight block)
+//               into one of two sets of TMEM accumulators and commits each
+//               stage back to the ring.
 //   warps 2-5   loaders: gather the chunk's token rows into the B ring slot
 //               with cp.async in the 128-byte swizzled K-major layout, with
 //               the stage's UE8M0 scale words of A and B (the MMA issuer
 //               moves those into TMEM with tcgen05.cp).
-//   warps 6-9   epilogue: read the accumulator (tcgen05.ld), run the unit's
-//               epilogue, and hand the accumulator back to the MMA issuer.
+//   warps 6-9   epilogue: read the accumulators (tcgen05.ld), run the unit's
+//               epilogue, and hand them back to the MMA issuer.
 //
 // Pages followed:
 // - "Beyond Day-0: Optimizing DeepSeek-V4.1 Flash in SGLang", 2.1: group-32
