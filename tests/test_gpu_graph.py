@@ -92,3 +92,48 @@ def test_forward_dev_argument_errors():
     gemv = MoEStep(H, I, E, k, w, tmax, 0, abi.MOE_FLAG_PATH_GEMV)
     assert abi.moe_forward_dev(gemv.plan, x, lg, d_T, y) == abi.MOE_ERR_UNSUPPORTED
     gemv.close()
+
+
+def test_graph_of_a_layer_stack():
+    """Three layers in one captured graph, each layer's y the next layer's x
+    (separate plans and weights). Inside the graph each route kernel follows
+    the previous layer's expert kernel through a programmatic edge. Replays
+    for several row counts equal the same three steps run one by one."""
+    dev = torch.device("cuda", 0)
+    H, E, k, I, tmax = 512, 8, 2, 256, 24
+    layers = []
+    for li in range(3):
+        w = synthetic.make_weights(40 + li, E, H, I, 0, dev)
+        layers.append((w, MoEStep(H, I, E, k, w, tmax, 0)))
+    x, _, _, _ = synthetic.make_inputs(40, tmax, H, E, k, "zipf", dev)
+    lgs = [synthetic.make_inputs(50 + li, tmax, H, E, k, "zipf", dev)[1] for li in range(3)]
+    d_T = torch.full((1,), tmax, dtype=torch.int32, device=dev)
+    ys = [torch.empty((tmax, H), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    status = [torch.full((1,), -1, dtype=torch.int32, device=dev) for _ in range(3)]
+
+    def stack():
+        inp = x
+        for li, (_, st) in enumerate(layers):
+            st.forward_dev(inp, lgs[li], d_T, ys[li], status[li])
+            inp = ys[li]
+    stack()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        stack()
+    torch.cuda.synchronize()
+    for T in (tmax, 7, 1):
+        for y in ys:
+            y.fill_(float("nan"))
+        d_T.fill_(T)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert all(int(s.item()) == abi.MOE_OK for s in status), T
+        inp = x[:T].contiguous()
+        for li, (_, st) in enumerate(layers):
+            ref = st.forward(inp, lgs[li][:T].contiguous())
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(bf16_dev_to_bits(ys[li][:T]), bf16_dev_to_bits(ref))
+            inp = ref
+    for _, st in layers:
+        st.close()

@@ -373,3 +373,35 @@ def test_timing_flag_records_expert_kernel():
     ms, n = g.step.kernel_times()
     assert n == 3 and ms > 0
     g.close()
+
+
+@pytest.mark.parametrize("path,fused", [("mma", False), ("gemv", False), ("mma", True)])
+def test_back_to_back_steps_match_isolated_steps(path, fused):
+    """Consecutive steps on one plan, enqueued with no synchronisation between
+    them, overlap through programmatic dependent launch (the route kernel of a
+    step starts while the previous step's last kernel finishes). Alternating
+    between two inputs, every step's y must equal that input's isolated step
+    bit for bit: the route kernel must not reset the plan's counters or lists
+    while the previous expert kernel still reads them."""
+    H, E, k, I, T = 512, 16, 4, 256, 40
+    w = synthetic.make_weights(31, E, H, I, 1)
+    step = MoEStep(H, I, E, k, w, T, 1, PATHS[path])
+    ins = [synthetic.make_inputs(31 + i, T, H, E, k, "zipf") for i in range(2)]
+    resid = torch.from_numpy(synth.residual_bf16(5, T, 1, H).view(np.int16).copy()).view(torch.bfloat16).cuda()
+    gamma = torch.from_numpy(synth.norm_weight_bf16(5, H).view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+    def one(i):
+        x, lg = ins[i][0], ins[i][1]
+        if fused:
+            return step.forward_fused(x, logits=lg, resid=resid, norm_weight=gamma)["zq"]
+        return step.forward(x, lg)
+    ref = []
+    for i in range(2):
+        ref.append(one(i).clone())
+        torch.cuda.synchronize()
+    outs = [one(n % 2) for n in range(12)]          # back to back, no sync
+    torch.cuda.synchronize()
+    assert step.status() == abi.MOE_OK
+    for n, y in enumerate(outs):
+        assert torch.equal(y, ref[n % 2]), n
+    step.close()
