@@ -148,6 +148,8 @@ using Cfg16 = MmaCfg<16, 5, 2>;
 using Cfg32 = MmaCfg<32, 5, 2>;
 using Cfg64 = MmaCfg<64, 4, 2>;
 using Cfg96x2 = MmaCfg<96, 4, 1, 2>;
+using Cfg16x2 = MmaCfg<16, 5, 1, 2>;  // MXFP4 weights
+using Cfg32x2 = MmaCfg<32, 5, 1, 2>;
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -1073,13 +1075,22 @@ cudaError_t prepare_experts_mma() {
   if (e == cudaSuccess) e = prepare_cfg<Cfg32>();
   if (e == cudaSuccess) e = prepare_cfg<Cfg64>();
   if (e == cudaSuccess) e = prepare_cfg<Cfg96x2>();
+  if (e == cudaSuccess) e = prepare_cfg<Cfg16x2>();
+  if (e == cudaSuccess) e = prepare_cfg<Cfg32x2>();
   return e;
 }
 
+// Weight blocks per unit. MXFP8 weights: one block up to 128 rows (the
+// 5-stage ring of two K chunks keeps more bytes in flight, which is what the
+// HBM-bound row counts need), two above. MXFP4 weights: two blocks at every
+// row count when H is a multiple of 256; same-box A/B, us per step:
+// bs1_fp4 192.4 -> 169.8, bs4_fp4 565.7 -> 477.1, while MXFP8 lost 3-4 % at
+// bs1 and bs4 with two blocks.
 cudaError_t launch_experts_mma(const MmaMaps &maps, const ExpertArgs &a, int grid, int chunk_rows, cudaStream_t st) {
+  const bool two = a.fp4 && a.H % 256 == 0;
   switch (chunk_rows) {
-    case 16: return launch_cfg<Cfg16>(maps, a, grid, st);
-    case 32: return launch_cfg<Cfg32>(maps, a, grid, st);
+    case 16: return two ? launch_cfg<Cfg16x2>(maps, a, grid, st) : launch_cfg<Cfg16>(maps, a, grid, st);
+    case 32: return two ? launch_cfg<Cfg32x2>(maps, a, grid, st) : launch_cfg<Cfg32>(maps, a, grid, st);
     case 64: return launch_cfg<Cfg64>(maps, a, grid, st);
     case 96: return launch_cfg<Cfg96x2>(maps, a, grid, st);
   }
