@@ -84,8 +84,10 @@ typedef enum {
 #define MOE_FLAG_PATH_GEMV (1u << 1)
 #define MOE_FLAG_PATH_MMA (1u << 2)
 /* Expert kernel selection. By default every step runs the tensor-core expert
- * kernel: block-scaled MXFP8 tcgen05 MMA, one MMA covering up to 16, 32 or
- * 64 token rows of an expert, so each expert's weights stream once per step.
+ * kernel: block-scaled MXFP8 tcgen05 MMA, one MMA covering up to 16, 32, 64 or
+ * 96 token rows of an expert (above 128 rows, and for MXFP4 weights at every
+ * row count, each unit covers two 128-row weight blocks on one token tile), so
+ * each expert's weights stream from HBM about once per step.
  * PATH_GEMV selects the CUDA-core GEMV expert kernel instead (8-row tiles;
  * an expert's weights stream once per tile). PATH_MMA pins the default.
  * Setting both is MOE_ERR_INVALID_ARG. Both kernels compute the same result
