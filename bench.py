@@ -266,11 +266,11 @@ def measured_peaks():
 
 
 EXPERT_KERNELS = {
-    # path -> (kernel, source file, committed ncu traffic summary)
-    "gemv": ("experts_kernel (persistent CUDA-core gate/up + down GEMV)", "experts.cu",
-             "experts_kernel_traffic.json"),
-    "mma": ("experts_mma_kernel (persistent tcgen05 block-scaled MXFP8 MMA)", "experts_mma.cu",
-            "experts_mma_kernel_traffic.json"),
+    # path -> (kernel, source files of its device code, committed ncu traffic summary)
+    "gemv": ("experts_kernel (persistent CUDA-core gate/up + down GEMV)",
+             ("experts.cu", "combine.cuh", "device.cuh"), "experts_kernel_traffic.json"),
+    "mma": ("experts_mma_kernel (persistent tcgen05 block-scaled MXFP8 MMA)",
+            ("experts_mma.cu", "combine.cuh", "device.cuh"), "experts_mma_kernel_traffic.json"),
 }
 PATH_FLAGS = {"auto": 0, "gemv": 1 << 1, "mma": 1 << 2}
 MMA_MIN_ROWS = 1  # the library's default: the tensor-core kernel at every row count
@@ -282,28 +282,36 @@ def kernel_path(path, T):
     return "mma" if T >= MMA_MIN_ROWS else "gemv"
 
 
-def code_sha256(path):
-    """sha256 of a C++/CUDA source with its comments and whitespace removed: the
-    hash changes when the code does, not when a comment does."""
+def code_sha256(*paths):
+    """sha256 of C++/CUDA sources (in the given order) with comments and
+    whitespace removed: the hash changes when the code does, not when a
+    comment does."""
     import hashlib
     import re
-    with open(path) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-    text = re.sub(r"//[^\n]*", " ", text)
-    return hashlib.sha256("".join(text.split()).encode()).hexdigest()
+    parts = []
+    for path in paths:
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        parts.append("".join(text.split()))
+    return hashlib.sha256("\n".join(parts).encode()).hexdigest()
+
+
+def kernel_code_sha256(path="mma"):
+    """code_sha256 of the device sources an expert kernel is compiled from."""
+    return code_sha256(*(os.path.join(ROOT, "moe_expert_layer_top_gb300", "csrc", f) for f in EXPERT_KERNELS[path][1]))
 
 
 def traffic_per_launch(algorithmic_bytes, path="gemv"):
     """DRAM bytes per expert-kernel launch from the committed ncu capture, scaled
     by the active weight bytes; None if the kernel's code changed since then."""
-    _, src_name, summary = EXPERT_KERNELS[path]
+    summary = EXPERT_KERNELS[path][2]
     p = os.path.join(ROOT, "profiles", summary)
-    src = os.path.join(ROOT, "moe_expert_layer_top_gb300", "csrc", src_name)
     try:
         with open(p) as f:
             d = json.load(f)
-        sha = code_sha256(src)
+        sha = kernel_code_sha256(path)
     except OSError:
         return None
     if sha != d.get("source_code_sha256"):

@@ -25,14 +25,20 @@ __device__ __forceinline__ void combine_row_block(const float *__restrict__ o, c
                                                   uint16_t *__restrict__ y, int T, int k, int shared, int H, int t,
                                                   int64_t h0, int lane, uint16_t (&yb)[Q]) {
   const int64_t hl = h0 + lane;
-  float acc[Q];
+  float acc[Q], sv[Q];
 #pragma unroll
   for (int q = 0; q < Q; ++q) acc[q] = 0.0f;
-  // pairs in chunks of 4: all loads of a chunk are in flight together
-  for (int j0 = 0; j0 < k; j0 += 4) {
-    float w[4], v[4][Q];
+  // the shared expert's row and the routed pairs in chunks of 8: all loads of
+  // a chunk (and the shared row) are in flight together
+  if (shared) {
+    const float *src = o + (int64_t(T) * k + t) * H + hl;
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
+    for (int q = 0; q < Q; ++q) sv[q] = __ldcg(src + 32 * q);
+  }
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    float w[8], v[8][Q];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
       const int j = j0 + jj < k ? j0 + jj : k - 1;
       w[jj] = __ldcg(topk_w + int64_t(t) * k + j);
       const float *src = o + (int64_t(t) * k + j) * H + hl;
@@ -40,7 +46,7 @@ __device__ __forceinline__ void combine_row_block(const float *__restrict__ o, c
       for (int q = 0; q < Q; ++q) v[jj][q] = __ldcg(src + 32 * q);
     }
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
+    for (int jj = 0; jj < 8; ++jj) {
       if (j0 + jj >= k) break;
 #pragma unroll
       for (int q = 0; q < Q; ++q)
@@ -48,9 +54,8 @@ __device__ __forceinline__ void combine_row_block(const float *__restrict__ o, c
     }
   }
   if (shared) {
-    const float *src = o + (int64_t(T) * k + t) * H + hl;
 #pragma unroll
-    for (int q = 0; q < Q; ++q) acc[q] = __fadd_rn(acc[q], __ldcg(src + 32 * q));
+    for (int q = 0; q < Q; ++q) acc[q] = __fadd_rn(acc[q], sv[q]);
   }
 #pragma unroll
   for (int q = 0; q < Q; ++q) {

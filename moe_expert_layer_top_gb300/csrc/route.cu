@@ -29,7 +29,8 @@
 //   chunk_list[]       (expert, chunk) items of <= 16..128 rows for the
 //                      tensor-core expert kernel.
 // The lists' per-expert offsets come from block-wide prefixes over the E+1
-// tile (chunk) counts. That is work enumeration, not row placement.
+// tile (chunk) counts, the shared expert first, then the routed experts by id.
+// That is work enumeration, not row placement.
 //
 // x is quantised to MXFP8 one 32-group per thread. "Beyond Day-0" 2.1 fuses
 // activation quantisation into the producer, and here it shares the launch
@@ -400,17 +401,22 @@ __device__ void route_place(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *
   }
   __syncthreads();
 
-  // --- counts and tiles per expert (index E: the shared expert, every row)
+  // --- counts and tiles per expert (index E: the shared expert, every row).
+  // Thread p enumerates expert ex: the shared expert first, then the routed
+  // experts by id. The expert kernels take units in this order, so the shared
+  // expert, which completes the combine of every row it is the last
+  // contribution to, runs first and not in the last wave of units.
   const int nexp = E + a.shared;
+  const int ex = a.shared ? (tid == 0 ? E : tid - 1) : tid;
   int cnt = 0;
   if (tid < nexp) {
-    if (tid < E) {
+    if (ex < E) {
       cnt = 0;
-      for (int w = 0; w < W; ++w) cnt += __popc(bm[tid * W + w]);
+      for (int w = 0; w < W; ++w) cnt += __popc(bm[ex * W + w]);
     } else {
       cnt = T;
     }
-    a.counts[tid] = cnt;
+    a.counts[ex] = cnt;
     sm.tiles[tid] = (cnt + kTileRows - 1) / kTileRows;
   } else {
     sm.tiles[tid] = 0;
@@ -426,7 +432,7 @@ __device__ void route_place(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *
   if (tid < nexp) {
     for (int j = 0; j < sm.tiles[tid]; ++j) {
       const int idx = excl + j;
-      if (idx < a.n_tiles_max) a.tile_list[idx] = (tid << 16) | j;
+      if (idx < a.n_tiles_max) a.tile_list[idx] = (ex << 16) | j;
       else report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
     }
   }
@@ -437,7 +443,7 @@ __device__ void route_place(const RouteArgs &a, int T, RouteSmem &sm, uint32_t *
     const int cexcl = packed_excl >> 16, nch_total = packed_total >> 16;
     for (int j = 0; j < nch; ++j) {
       const int idx = cexcl + j;
-      if (idx < a.n_tiles_max) a.chunk_list[idx] = (tid << 16) | j;
+      if (idx < a.n_tiles_max) a.chunk_list[idx] = (ex << 16) | j;
       else report_error(a.status, MOE_ERR_DEVICE_BOUNDS);
     }
     if (tid == 0) *a.n_chunks = min(nch_total, a.n_tiles_max);

@@ -28,8 +28,8 @@ def test_committed_traffic_record_matches_the_expert_kernel():
     algorithmic bytes at capture), not null."""
     with open(os.path.join(ROOT, "profiles", "experts_mma_kernel_traffic.json")) as f:
         d = json.load(f)
-    src = os.path.join(ROOT, "moe_expert_layer_top_gb300", "csrc", "experts_mma.cu")
-    assert bench.code_sha256(src) == d["source_code_sha256"]
+    assert bench.kernel_code_sha256("mma") == d["source_code_sha256"]
+    assert d["sources"] == [os.path.join("moe_expert_layer_top_gb300", "csrc", f) for f in bench.EXPERT_KERNELS["mma"][1]]
     algo = 1167851520  # bs1: 45 active experts x 3 x 2048 x 4096 x 33/32
     t = bench.traffic_per_launch(algo, "mma")
     ratio = (d["dram_bytes_read"] + d["dram_bytes_write"]) / d["algorithmic_bytes"]
