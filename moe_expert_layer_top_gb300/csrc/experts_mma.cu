@@ -31,6 +31,10 @@
 // The counter hands out every gate/up unit before any down unit, so a down
 // unit only waits on gate/up units that blocks have already taken, and those
 // never wait. The waits cannot form a cycle, and every wait is bounded anyway.
+// Experts come in the chunk list's order, the shared expert first: its down
+// units are the last contribution to every token row they cover, and at the
+// end of the order they left a few blocks combining every row after the
+// others had finished.
 //
 // Warp roles (10 warps):
 //   warp 0      TMA producer: one lane takes the block's units from the
