@@ -1,8 +1,10 @@
 """Host-side logic of bench.py that needs no GPU: the staleness check of the
-committed ncu traffic record, and the traffic scaling that fills the bench
-line's roofline.traffic."""
+committed ncu traffic record, the traffic scaling that fills the bench
+line's roofline.traffic, and the reference arm (the oracle on the host cores)
+end to end on the tiny workload."""
 import json
 import os
+import subprocess
 import sys
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -35,3 +37,22 @@ def test_committed_traffic_record_matches_the_expert_kernel():
     ratio = (d["dram_bytes_read"] + d["dram_bytes_write"]) / d["algorithmic_bytes"]
     assert t == int(round(algo * ratio))
     assert 0.99 < t / algo < 1.02
+
+
+def test_reference_arm_line():
+    """bench.py --impl reference prints one JSON line: the oracle's step time
+    as value, cpu_baseline and e2e describing the same run."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+           "--steps", "3", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["value"] > 0 and d["unit"] == "us/step" and d["higher_is_better"] is False
+    assert d["steps"] == 3 and d["warmup"] == 3
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("tiny")
