@@ -36,7 +36,7 @@ pytestmark = pytest.mark.gpu
 SEED = synth.BASE_SEED
 MXFP8_RUNS = [("bs1", "default"), ("bs4", "default"), ("bs16", "default"), ("bs64", "default"),
               ("bs1", "gemv"), ("bs4", "gemv"), ("bs16", "gemv")]
-MXFP4_RUNS = [("bs1", "default"), ("bs64", "default")]
+MXFP4_RUNS = [("bs1", "default"), ("bs4", "default"), ("bs64", "default")]  # 16-, 32- and 96-row units
 MXFP4_I, MXFP4_LIMIT = 2304, 1.0   # the pages' I = 4 x 576; the clip limit is not given on the pages
 FLAGS = {"default": 0, "gemv": abi.MOE_FLAG_PATH_GEMV}
 
